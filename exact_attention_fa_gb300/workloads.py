@@ -1,0 +1,146 @@
+"""Seeded synthetic workloads: the only module shared by the CUDA path's tests and the oracle.
+
+It holds no attention arithmetic. It only draws inputs (i.i.d. standard normal Q, K, V, dO and a
+Bernoulli block mask) and rounds them to bf16, so that both sides of a parity test see exactly the
+same input values.
+
+Generator: numpy's PCG64 seeded with ``SeedSequence([seed, stream])`` (one stream per tensor), its
+standard-normal sampler in float32, then round-to-nearest-even to bf16 by integer arithmetic on
+the fp32 bit pattern. The shapes and distributions follow the workloads of the FlashAttention pages
+(multi-head attention, ``[B, H, N, d]`` tensors, N(0, 1) entries, 128x128 tile block mask).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+# One independent random stream per tensor so that, e.g., the mask never depends on d.
+STREAM_Q, STREAM_K, STREAM_V, STREAM_DO, STREAM_MASK = 1, 2, 3, 4, 5
+
+TILE = 128  # block-mask granularity (query tiles x key tiles)
+
+
+def normal_f32(shape, seed: int, stream: int) -> np.ndarray:
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, stream])))
+    return rng.standard_normal(size=shape, dtype=np.float32)
+
+
+def bf16_bits_from_f32(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to bf16 (round to nearest, ties to even); returns the uint16 bit patterns.
+
+    Inputs here are finite normals, so the NaN/overflow corner of the rounding never arises.
+    """
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    u = u + np.uint32(0x7FFF) + lsb
+    return (u >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def block_mask(n_tiles: int, seed: int, p: float = 0.25) -> np.ndarray:
+    """Bernoulli(p) tile mask [n_tiles, n_tiles] (row = query tile, column = key tile), diagonal on."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, STREAM_MASK])))
+    m = (rng.random((n_tiles, n_tiles)) < p).astype(np.uint8)
+    np.fill_diagonal(m, 1)
+    return m
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One attention problem: shapes, dtype, masking mode and seed."""
+
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    dtype: str = "bf16"  # "bf16" or "fp32" (Q, K, V, dO and O)
+    causal: bool = False
+    block_sparse: bool = False
+    backward: bool = False
+    seed: int = 0
+    scale: float | None = None  # None means 1/sqrt(d)
+
+    @property
+    def softmax_scale(self) -> float:
+        return 1.0 / math.sqrt(self.d) if self.scale is None else float(self.scale)
+
+    def with_(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+# The five workloads the hot path is specified on (seed = position in this list, 1-based).
+WORKLOADS = {
+    "single_head_fp32": Workload("single_head_fp32", 1, 1, 256, 64, dtype="fp32", seed=1),
+    "mha_N2048_d64": Workload("mha_N2048_d64", 4, 16, 2048, 64, seed=2),
+    "causal_N8192_d128": Workload("causal_N8192_d128", 8, 32, 8192, 128, causal=True, seed=3),
+    "blocksparse_N16384_d64": Workload("blocksparse_N16384_d64", 2, 16, 16384, 64,
+                                       block_sparse=True, seed=4),
+    "bwd_causal_N4096_d128": Workload("bwd_causal_N4096_d128", 4, 16, 4096, 128, causal=True,
+                                      backward=True, seed=5),
+}
+
+
+@dataclasses.dataclass
+class Inputs:
+    """Host-side inputs of one workload.
+
+    ``*_bits`` are uint16 bf16 bit patterns (bf16 workloads) and ``*_f32`` the fp32 arrays
+    (fp32 workloads); ``f64(name)`` returns the exact values as float64 for the oracle.
+    """
+
+    w: Workload
+    arrays: dict
+
+    def f64(self, name: str) -> np.ndarray:
+        a = self.arrays[name]
+        if a.dtype == np.uint16:
+            return bf16_bits_to_f64(a)
+        return a.astype(np.float64)
+
+    def raw(self, name: str) -> np.ndarray:
+        return self.arrays[name]
+
+
+def make_inputs(w: Workload, with_do: bool | None = None) -> Inputs:
+    shape = (w.B, w.H, w.N, w.d)
+    names = [("q", STREAM_Q), ("k", STREAM_K), ("v", STREAM_V)]
+    if with_do or (with_do is None and w.backward):
+        names.append(("do", STREAM_DO))
+    arrays = {}
+    for nm, st in names:
+        x = normal_f32(shape, w.seed, st)
+        arrays[nm] = bf16_bits_from_f32(x) if w.dtype == "bf16" else x
+        del x
+    if w.block_sparse:
+        if w.N % TILE:
+            raise ValueError("block-sparse workloads need N to be a multiple of 128")
+        arrays["mask"] = block_mask(w.N // TILE, w.seed)
+    return Inputs(w, arrays)
+
+
+def flop_count(w: Workload, mask: np.ndarray | None = None, part: str = "fwd") -> float:
+    """Algorithmic FLOPs: 4*B*H*N^2*d forward (causal: half; block-sparse: active tiles only);
+    the backward counts its five contractions, 2.5 times the forward."""
+    if w.block_sparse:
+        if mask is None:
+            mask = block_mask(w.N // TILE, w.seed)
+        fwd = 4.0 * w.B * w.H * w.d * TILE * TILE * float(mask.sum())
+    else:
+        fwd = 4.0 * w.B * w.H * w.N * w.N * w.d * (0.5 if w.causal else 1.0)
+    if part == "fwd":
+        return fwd
+    if part == "bwd":
+        return 2.5 * fwd
+    if part == "fwd+bwd":
+        return 3.5 * fwd
+    raise ValueError(part)
