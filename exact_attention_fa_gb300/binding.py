@@ -1,0 +1,182 @@
+"""Thin ctypes binding of libfa_gb300.so: argument marshalling only.
+
+Each function takes torch tensors, checks dtype/shape/device/contiguity, and passes raw device
+pointers and the current CUDA stream to the C entry point of the same name (include/fa.h). Every
+step of the computation runs in the library's kernels; there is no fallback: if the library is
+missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+FA_OK = 0
+_STATUS = {
+    1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA",
+    5: "FA_ERR_DEVICE_TIMEOUT", 6: "FA_ERR_NO_DEVICE", 7: "FA_ERR_TOO_LARGE",
+}
+
+# (name, restype, argtypes) of every symbol declared in include/fa.h
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+SIGNATURES = [
+    ("fa_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    ("fa_fwd_fp32", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    ("fa_fwd_blocksparse", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _P]),
+    ("fa_bwd_workspace_bytes", ctypes.c_size_t, [_I, _I, _I, _I]),
+    ("fa_bwd", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
+    ("fa_check_device_error", _I, [_P]),
+    ("fa_status_string", ctypes.c_char_p, [_I]),
+    ("fa_abi_version", _I, []),
+]
+
+
+class FAError(RuntimeError):
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__(f"{fn} failed: {_STATUS.get(status, status)} ({text})")
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Loads (building first if needed) the library and declares every entry point."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.build_library()
+    if not os.path.exists(path):
+        raise FAError("load", -1, f"{path} is missing")
+    lib = ctypes.CDLL(path)
+    for name, res, args in SIGNATURES:
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, status: int):
+    if status != FA_OK:
+        raise FAError(fn, status, load().fa_status_string(status).decode())
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _bhnd(q: torch.Tensor, *others: torch.Tensor, dtype=torch.bfloat16):
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    for t in (q,) + others:
+        if t.shape != q.shape:
+            raise ValueError(f"shape mismatch: {tuple(t.shape)} vs {tuple(q.shape)}")
+        if t.dtype != dtype:
+            raise TypeError(f"expected {dtype}, got {t.dtype}")
+        if not t.is_cuda or t.device != q.device:
+            raise ValueError("all tensors must be on the same CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous [B, H, N, d]")
+    return q.shape
+
+
+def _rows(t: torch.Tensor, shape, dtype=torch.float32):
+    if tuple(t.shape) != tuple(shape[:3]) or t.dtype != dtype or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"expected a contiguous {dtype} CUDA tensor of shape {tuple(shape[:3])}")
+
+
+def fa_fwd(q, k, v, o, lse, scale: float, causal: bool = False):
+    """bf16 forward into preallocated o [B,H,N,d] bf16 and lse [B,H,N] fp32."""
+    B, H, N, d = _bhnd(q, k, v, o)
+    _rows(lse, q.shape)
+    _check("fa_fwd", load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                                   float(scale), int(bool(causal)), _stream(q)))
+
+
+def fa_fwd_fp32(q, k, v, o, lse, scale: float, causal: bool = False):
+    """fp32 forward (FMA pipes) into preallocated o [B,H,N,d] fp32 and lse [B,H,N] fp32."""
+    B, H, N, d = _bhnd(q, k, v, o, dtype=torch.float32)
+    _rows(lse, q.shape)
+    _check("fa_fwd_fp32", load().fa_fwd_fp32(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
+                                             N, d, float(scale), int(bool(causal)), _stream(q)))
+
+
+def fa_fwd_blocksparse(q, k, v, o, lse, scale: float, block_mask):
+    """Block-sparse bf16 forward; block_mask is a uint8 CUDA tensor [N/128, N/128]."""
+    B, H, N, d = _bhnd(q, k, v, o)
+    _rows(lse, q.shape)
+    nt = (N + 127) // 128
+    if (block_mask.dtype != torch.uint8 or tuple(block_mask.shape) != (nt, nt)
+            or not block_mask.is_cuda or not block_mask.is_contiguous()):
+        raise ValueError(f"block_mask must be a contiguous uint8 CUDA tensor [{nt}, {nt}]")
+    _check("fa_fwd_blocksparse",
+           load().fa_fwd_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                                     float(scale), _ptr(block_mask), _stream(q)))
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load().fa_bwd_workspace_bytes(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool, workspace):
+    """Backward: dq fp32, dk/dv bf16 (preallocated); workspace from fa_bwd_workspace_bytes."""
+    B, H, N, d = _bhnd(q, k, v, o, do, dk, dv)
+    _bhnd(dq, dtype=torch.float32)
+    if tuple(dq.shape) != tuple(q.shape):
+        raise ValueError("dq must have the shape of q")
+    _rows(lse, q.shape)
+    need = fa_bwd_workspace_bytes(B, H, N, d)
+    if workspace.numel() * workspace.element_size() < need or not workspace.is_cuda:
+        raise ValueError(f"workspace must hold at least {need} bytes on the device")
+    _check("fa_bwd", load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+                                   int(bool(causal)), _ptr(workspace), _stream(q)))
+
+
+def fa_check_device_error(device=None):
+    """Synchronises the current stream and raises if a kernel recorded a device-side error."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    s = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    _check("fa_check_device_error", load().fa_check_device_error(s))
+
+
+# ------------------------------------------------------------------------------- conveniences
+
+def attention_forward(q, k, v, scale: float | None = None, causal: bool = False, block_mask=None):
+    """Allocates O and lse with torch and runs the matching entry point (bf16 or fp32)."""
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    if q.dtype == torch.float32:
+        if block_mask is not None:
+            raise ValueError("block-sparse attention is bf16 only")
+        fa_fwd_fp32(q, k, v, o, lse, scale, causal)
+    elif block_mask is not None:
+        if causal:
+            raise ValueError("block-sparse and causal masks are not combined")
+        fa_fwd_blocksparse(q, k, v, o, lse, scale, block_mask)
+    else:
+        fa_fwd(q, k, v, o, lse, scale, causal)
+    return o, lse
+
+
+def attention_backward(q, k, v, o, lse, do, scale: float | None = None, causal: bool = False):
+    """Allocates dq (fp32), dk, dv (bf16) and the workspace, and runs fa_bwd."""
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    B, H, N, d = q.shape
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    ws = torch.empty(fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=q.device)
+    fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, causal, ws)
+    return dq, dk, dv

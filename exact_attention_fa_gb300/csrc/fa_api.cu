@@ -1,0 +1,250 @@
+// C ABI of the exact-attention library: argument validation, per-device state, TMA descriptor
+// creation and kernel launches. Declarations and semantics: include/fa.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per barrier wait
+
+// Device error word written by kernels that give up on a barrier (see fa::kErrTimeout).
+__device__ unsigned g_error_word;
+
+struct DeviceState {
+  bool ready = false;
+  int status = FA_OK;
+  int num_sms = 0;
+  unsigned* err = nullptr;  // device address of g_error_word on this device
+};
+
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Per-device set-up, once, with that device current: check it is an sm_103 part, look up the
+// device address of the error word and the SM count.
+int device_state(DeviceState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return FA_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    st.ready = true;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        major != 10 || minor != 3) {
+      cudaGetLastError();
+      st.status = FA_ERR_NO_DEVICE;
+    } else if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) !=
+                   cudaSuccess ||
+               cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err), g_error_word) !=
+                   cudaSuccess) {
+      cudaGetLastError();
+      st.status = FA_ERR_CUDA;
+    }
+    if (st.status == FA_OK && g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q{};
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        cudaGetLastError();
+        st.status = FA_ERR_CUDA;
+      } else {
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      }
+    }
+  }
+  *out = &st;
+  return st.status;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int B, int H, int N, float scale) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh * N > (1ll << 31) - 1 || bh > (1ll << 30)) return FA_ERR_TOO_LARGE;
+  return FA_OK;
+}
+
+// 3-D view [B*H][N][d] of a bf16 tensor, box 64 x 128 x 1, 128-byte swizzle, zero fill outside.
+bool encode_bf16_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(N) * d * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int N, int d, float scale, int mode, const uint8_t* block_mask, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (mode == fa::kBlockSparse && !block_mask) return FA_ERR_INVALID_ARG;
+  int st = check_common(B, H, N, scale);
+  if (st != FA_OK) return st;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (mode == fa::kBlockSparse && N % 128 != 0) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != FA_OK) return st;
+
+  fa::FwdParams p{};
+  const int BH = B * H;
+  if (!encode_bf16_map(&p.tm_q, q, BH, N, d) || !encode_bf16_map(&p.tm_k, k, BH, N, d) ||
+      !encode_bf16_map(&p.tm_v, v, BH, N, d))
+    return FA_ERR_CUDA;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.block_mask = block_mask;
+  p.BH = BH;
+  p.N = N;
+  p.n_tiles = (N + 127) / 128;
+  p.n_pairs = (p.n_tiles + 1) / 2;
+  const long long kv_bytes_per_head = 2ll * N * d * 2;
+  long long g = (32ll << 20) / kv_bytes_per_head;
+  p.heads_per_group = static_cast<int>(g < 1 ? 1 : (g > BH ? BH : g));
+  p.mode = mode;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.err = ds->err;
+  p.timeout_ns = kWaitTimeoutNs;
+  if (static_cast<long long>(p.n_pairs) * BH > 0x7fffffffll) return FA_ERR_TOO_LARGE;
+  return to_status(fa::launch_fwd_tc(p, d, ds->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_abi_version(void) { return (1 << 16) | 0; }
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported head dimension or sequence length";
+    case FA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case FA_ERR_CUDA: return "CUDA call failed";
+    case FA_ERR_DEVICE_TIMEOUT: return "kernel gave up waiting on an on-chip barrier";
+    case FA_ERR_NO_DEVICE: return "no current sm_103 CUDA device";
+    case FA_ERR_TOO_LARGE: return "problem too large for the kernels' indexing";
+    default: return "unknown status";
+  }
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, float scale, int causal, fa_stream_t stream) {
+  return fwd_bf16(q, k, v, o, lse, B, H, N, d, scale, causal ? fa::kCausal : fa::kDense, nullptr,
+                  stream);
+}
+
+int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int N, int d, float scale, const uint8_t* block_mask,
+                       fa_stream_t stream) {
+  return fwd_bf16(q, k, v, o, lse, B, H, N, d, scale, fa::kBlockSparse, block_mask, stream);
+}
+
+int fa_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
+                int H, int N, int d, float scale, int causal, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  int st = check_common(B, H, N, scale);
+  if (st != FA_OK) return st;
+  if (d < 32 || d > 128 || d % 32 != 0) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  if (static_cast<long long>(B) * H > 65535) return FA_ERR_TOO_LARGE;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != FA_OK) return st;
+  fa::Fp32FwdParams p{q, k, v, o, lse, B * H, N, d, causal ? 1 : 0,
+                      scale * 1.4426950408889634f};
+  return to_status(fa::launch_fwd_fp32(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+  (void)d;
+  if (B < 1 || H < 1 || N < 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return (2 * rows * sizeof(float) + 255) & ~static_cast<size_t>(255);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+           const float* lse, float* dq, void* dk, void* dv, int B, int H, int N, int d,
+           float scale, int causal, void* workspace, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace)
+    return FA_ERR_INVALID_ARG;
+  int st = check_common(B, H, N, scale);
+  if (st != FA_OK) return st;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(workspace))
+    return FA_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != FA_OK) return st;
+  fa::BwdParams p{};
+  const int BH = B * H;
+  if (!encode_bf16_map(&p.tm_q, q, BH, N, d) || !encode_bf16_map(&p.tm_k, k, BH, N, d) ||
+      !encode_bf16_map(&p.tm_v, v, BH, N, d) || !encode_bf16_map(&p.tm_do, dO, BH, N, d))
+    return FA_ERR_CUDA;
+  p.o = static_cast<const __nv_bfloat16*>(o);
+  p.dO = static_cast<const __nv_bfloat16*>(dO);
+  p.lse = lse;
+  p.dq = dq;
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  const size_t rows = static_cast<size_t>(BH) * N;
+  p.lse2 = static_cast<float*>(workspace);
+  p.Dsum = static_cast<float*>(workspace) + rows;
+  p.BH = BH;
+  p.N = N;
+  p.d = d;
+  p.n_tiles = (N + 127) / 128;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.err = ds->err;
+  p.timeout_ns = kWaitTimeoutNs;
+  return to_status(fa::launch_bwd(p, ds->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fa_check_device_error(fa_stream_t stream) {
+  DeviceState* ds = nullptr;
+  int st = device_state(&ds);
+  if (st != FA_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  unsigned word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word)) != cudaSuccess) return FA_ERR_CUDA;
+  if (word != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_DEVICE_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,114 @@
+// fp32 forward: tiled online softmax on the FMA pipes, for fp32 inputs where a bf16/tf32 tensor-
+// core product would miss a 1e-5 accuracy bar.
+//
+// A CTA owns kRows consecutive query rows of one (b, h), one warp per row. Key/value blocks of
+// 32 rows are staged in shared memory and shared by the CTA's warps. Lane j scores key j of the
+// block (a d-long dot product from shared memory); the warp then applies the online-softmax
+// update of "FlashAttention：メモリ効率的なアテンション計算", section "オンライン softmax":
+//   m_new = max(m, block max),  alpha = exp(m - m_new),  l = l*alpha + sum p,  o = o*alpha + sum p v
+// with each lane owning d/32 output columns, and divides by l once at the end. Exponentials are
+// base 2 with log2(e) folded into the scale.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr int kRows = 8;   // query rows (warps) per CTA
+constexpr int kKeys = 32;  // keys per shared-memory block
+
+template <int D>
+__global__ void __launch_bounds__(kRows * 32) fwd_fp32_kernel(const Fp32FwdParams p) {
+  constexpr int C = D / 32;
+  __shared__ float ks[kKeys][D + 1];  // +1: lane j reads row j without bank conflicts
+  __shared__ float vs[kKeys][D];
+  __shared__ float qs[kRows][D];
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int row0 = blockIdx.x * kRows;
+  const int row = row0 + warp;
+  const size_t head = static_cast<size_t>(blockIdx.y) * p.N * D;
+  const float* q = p.q + head;
+  const float* k = p.k + head;
+  const float* v = p.v + head;
+
+  for (int i = threadIdx.x; i < kRows * D; i += blockDim.x) {
+    const int r = row0 + i / D;
+    qs[i / D][i % D] = r < p.N ? q[static_cast<size_t>(r) * D + i % D] : 0.f;
+  }
+
+  float m = -INFINITY, l = 0.f;
+  float acc[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) acc[c] = 0.f;
+
+  const int kend = p.causal ? min(p.N, row0 + kRows) : p.N;
+  for (int kb = 0; kb < kend; kb += kKeys) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < kKeys * D; i += blockDim.x) {
+      const int j = kb + i / D, c = i % D;
+      const bool in = j < p.N;
+      ks[i / D][c] = in ? k[static_cast<size_t>(j) * D + c] : 0.f;
+      vs[i / D][c] = in ? v[static_cast<size_t>(j) * D + c] : 0.f;
+    }
+    __syncthreads();
+    if (row >= p.N) continue;
+
+    const int j = kb + lane;
+    float s = 0.f;
+#pragma unroll 16
+    for (int c = 0; c < D; ++c) s = fmaf(qs[warp][c], ks[lane][c], s);
+    const bool ok = j < p.N && (!p.causal || j <= row);
+    s = ok ? s * p.scale_log2 : -INFINITY;
+
+    float bmax = s;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(~0u, bmax, off));
+    const float m_new = fmaxf(m, bmax);
+    if (m_new == -INFINITY) continue;  // no allowed key for this row yet
+    const float alpha = exp2f(m - m_new);  // 0 while nothing has been accumulated
+    const float pj = ok ? exp2f(s - m_new) : 0.f;
+    float psum = pj;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) psum += __shfl_xor_sync(~0u, psum, off);
+    l = l * alpha + psum;
+#pragma unroll
+    for (int c = 0; c < C; ++c) acc[c] *= alpha;
+#pragma unroll 4
+    for (int jj = 0; jj < kKeys; ++jj) {
+      const float pjj = __shfl_sync(~0u, pj, jj);
+#pragma unroll
+      for (int c = 0; c < C; ++c) acc[c] = fmaf(pjj, vs[jj][lane + 32 * c], acc[c]);
+    }
+    m = m_new;
+  }
+
+  if (row < p.N) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    float* o = p.o + head + static_cast<size_t>(row) * D;
+#pragma unroll
+    for (int c = 0; c < C; ++c) o[lane + 32 * c] = acc[c] * inv;
+    if (lane == 0)
+      p.lse[static_cast<size_t>(blockIdx.y) * p.N + row] =
+          l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_fp32(const Fp32FwdParams& p, cudaStream_t s) {
+  const dim3 grid((p.N + kRows - 1) / kRows, p.BH);
+  const dim3 block(kRows * 32);
+  switch (p.d) {
+    case 32: fwd_fp32_kernel<32><<<grid, block, 0, s>>>(p); break;
+    case 64: fwd_fp32_kernel<64><<<grid, block, 0, s>>>(p); break;
+    case 96: fwd_fp32_kernel<96><<<grid, block, 0, s>>>(p); break;
+    case 128: fwd_fp32_kernel<128><<<grid, block, 0, s>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fa

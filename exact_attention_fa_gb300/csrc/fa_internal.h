@@ -1,0 +1,71 @@
+// Internal launch interface between the C ABI (fa_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+enum MaskMode : int { kDense = 0, kCausal = 1, kBlockSparse = 2 };
+
+// Everything a forward kernel needs. The three tensor maps describe Q, K, V as 3-D tensors
+// [B*H][N][d] (bf16, 128-byte swizzle, box 64 x 128 x 1) so that out-of-range rows of a tile
+// read as zero.
+struct FwdParams {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  __nv_bfloat16* o;
+  float* lse;
+  const uint8_t* block_mask;  // [n_tiles][n_tiles] or null
+  int BH, N;
+  int n_tiles;                // ceil(N / 128)
+  int n_pairs;                // ceil(n_tiles / 2): a CTA owns two 128-row query tiles
+  int heads_per_group;        // CTA order: groups of heads whose K/V fit in L2
+  int mode;                   // MaskMode
+  float scale_log2;           // scale * log2(e)
+  unsigned* err;
+  unsigned long long timeout_ns;
+};
+
+struct Fp32FwdParams {
+  const float* q;
+  const float* k;
+  const float* v;
+  float* o;
+  float* lse;
+  int BH, N, d;
+  int causal;
+  float scale_log2;
+};
+
+struct BwdParams {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  CUtensorMap tm_do;
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* dO;
+  const float* lse;
+  float* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  float* lse2;   // workspace: lse * log2(e) per row (+inf for rows >= N)
+  float* Dsum;   // workspace: D_i = sum_k dO_ik O_ik
+  int BH, N, d;
+  int n_tiles;
+  int causal;
+  float scale;       // softmax scale
+  float scale_log2;  // scale * log2(e)
+  unsigned* err;
+  unsigned long long timeout_ns;
+};
+
+// Launchers; return a cudaError_t (cudaSuccess on success).
+cudaError_t launch_fwd_tc(const FwdParams& p, int d, int num_sms, cudaStream_t s);
+cudaError_t launch_fwd_fp32(const Fp32FwdParams& p, cudaStream_t s);
+cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t s);
+
+}  // namespace fa

@@ -1,0 +1,105 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library (libfa_gb300.so).
+ *
+ * What is computed. For every batch b < B and head h < H, with Q, K, V in R^{N x d}:
+ *     S = scale * Q K^T   (S_ij = -inf where masked),
+ *     O = softmax(S) V,   lse_i = m_i + ln sum_j exp(S_ij - m_i),  m_i = max_j S_ij
+ * -- "3 · FlashAttention" (mkdocs.reaper.mx), 3.1; "FlashAttention：メモリ効率的なアテンション計算"
+ * (tech-tldr.com), first formula. The kernels reach it with the online-softmax recurrence of
+ * "FlashAttention：メモリ効率的なアテンション計算", section "オンライン softmax" (running max m,
+ * running sum l, unnormalised accumulator rescaled by exp(m - m_new), one division by l at the end;
+ * FlashAttention-2 order as in "출력을 누적해 메모리 이동을 줄이는 FlashAttention"), so that no N x N
+ * matrix is ever written to device memory.
+ *
+ * Common conventions of every entry point:
+ *   - Layout: Q, K, V, O, dO, dQ, dK, dV are dense row-major [B, H, N, d] (d contiguous);
+ *     lse and the backward workspace rows are [B, H, N] fp32.
+ *   - Pointers are DEVICE pointers owned by the caller, 16-byte aligned; outputs must not alias
+ *     inputs. The library allocates no memory on any call.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Every call only enqueues work:
+ *     it returns after the launches, without synchronising. The current CUDA device must be an
+ *     sm_103 GPU and must own the pointers.
+ *   - Arguments are validated before anything is enqueued; a non-zero return means nothing
+ *     was launched (except FA_ERR_CUDA from a failed launch).
+ *   - Kernels never spin forever: every wait on an on-chip barrier gives up after a bounded time
+ *     and records FA_ERR_DEVICE_TIMEOUT in a device error word, read by fa_check_device_error.
+ *   - Masked rows: a query row with no allowed key gets O = 0 and lse = -inf.
+ */
+#ifndef FA_GB300_H_
+#define FA_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fa_stream_t; /* identical to cudaStream_t */
+
+enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,    /* null pointer, B/H/N < 1, non-finite or non-positive scale      */
+  FA_ERR_UNSUPPORTED = 2,    /* head dim d or N not supported by this entry point               */
+  FA_ERR_MISALIGNED = 3,     /* a pointer is not 16-byte aligned                                */
+  FA_ERR_CUDA = 4,           /* a CUDA runtime or driver call failed (tensor map, launch)       */
+  FA_ERR_DEVICE_TIMEOUT = 5, /* a kernel gave up waiting on an on-chip barrier                  */
+  FA_ERR_NO_DEVICE = 6,      /* no current CUDA device, or it is not compute capability 10.3   */
+  FA_ERR_TOO_LARGE = 7       /* B*H*N or a grid dimension exceeds what the kernels index        */
+};
+
+/* Forward, bf16 inputs and output, fp32 accumulation (tensor cores: tcgen05.mma, TMEM).
+ * q, k, v : [B,H,N,d] bf16 (read);  o : [B,H,N,d] bf16 (written);  lse : [B,H,N] fp32 (written,
+ * natural log of the row's softmax denominator of the scaled scores, the statistic the backward
+ * recomputes P from -- "FlashAttention: IOを意識した高速かつメモリ効率の高い厳密なアテンション"
+ * (xyznot.com), "主要なアイデア", recomputation from O and (l, m)).
+ * d in {64, 128}; any N >= 1 (the last tile is masked). causal != 0 applies the lower-triangular
+ * mask key j <= query i and skips whole key tiles above the diagonal ("3 · FlashAttention",
+ * question on the causal mask). */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, float scale, int causal, fa_stream_t stream);
+
+/* Forward with fp32 inputs and outputs, computed with fp32 FMAs (no tensor cores), for accuracy
+ * at the 1e-5 level. Same semantics as fa_fwd; d a multiple of 32 in [32, 128]. */
+int fa_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
+                int H, int N, int d, float scale, int causal, fa_stream_t stream);
+
+/* Block-sparse forward ("FlashAttention: IOを意識した..." (xyznot.com), "拡張: Block-Sparse
+ * FlashAttention"): block_mask is a DEVICE uint8 array [N/128][N/128], row = query tile,
+ * column = key tile, shared by all (b, h); a zero entry masks the whole 128 x 128 tile of scores
+ * and the kernel never visits it. bf16 like fa_fwd; d in {64, 128}; N must be a multiple of 128. */
+int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int N, int d, float scale, const uint8_t* block_mask,
+                       fa_stream_t stream);
+
+/* Bytes of device workspace fa_bwd needs: 2 * B*H*N fp32 (rounded up to 256 bytes). */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/* Backward by recomputation ("3 · FlashAttention", 3.4; "FlashAttention：在线 softmax 与
+ * IO-aware 注意力" (quant67.com), section 五): S and P are rebuilt tile by tile from q, k and the
+ * saved lse, never stored. Given dO = dL/dO it writes
+ *     dq = scale * dS K (fp32, [B,H,N,d]),  dk = scale * dS^T Q (bf16),  dv = P^T dO (bf16),
+ * with dS = P * (dP - D), dP = dO V^T, D_i = sum_k dO_ik O_ik.
+ * q, k, v, o, dO : bf16 [B,H,N,d] (read; o and lse are the forward's outputs for the same
+ * q, k, v, scale, causal);  workspace : fa_bwd_workspace_bytes(...) bytes of scratch, contents
+ * undefined on entry and on exit. d in {64, 128}; any N >= 1. */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+           const float* lse, float* dq, void* dk, void* dv, int B, int H, int N, int d,
+           float scale, int causal, void* workspace, fa_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the device error word of the current device.
+ * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (a kernel gave up on a barrier; its outputs are invalid),
+ * or FA_ERR_CUDA if the synchronisation itself failed. */
+int fa_check_device_error(fa_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* fa_status_string(int status);
+
+/* ABI version: (major << 16) | minor. */
+int fa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H_ */

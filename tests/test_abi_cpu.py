@@ -1,0 +1,103 @@
+"""The C-ABI library builds, loads and exports every symbol include/fa.h declares (no GPU needed).
+
+Only argument validation runs here: each call below is rejected before anything touches a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "fa.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("fa_fwd", "fa_fwd_fp32", "fa_fwd_blocksparse", "fa_bwd", "fa_bwd_workspace_bytes",
+                 "fa_check_device_error", "fa_status_string", "fa_abi_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_signatures_cover_the_header(lib_path):
+    from exact_attention_fa_gb300 import binding
+    assert sorted(n for n, _, _ in binding.SIGNATURES) == declared_functions()
+    binding.load(lib_path)
+
+
+@pytest.fixture(scope="module")
+def lib(lib_path):
+    from exact_attention_fa_gb300 import binding
+    return binding.load(lib_path)
+
+
+P = ctypes.c_void_p
+
+
+def fake(addr=0x10000):
+    return P(addr)
+
+
+def test_status_strings(lib):
+    assert lib.fa_status_string(0) == b"ok"
+    assert b"aligned" in lib.fa_status_string(3)
+    assert lib.fa_status_string(999) == b"unknown status"
+    assert lib.fa_abi_version() >> 16 == 1
+
+
+@pytest.mark.parametrize("args,want", [
+    # null pointer
+    ((P(0), fake(), fake(), fake(), fake(), 1, 1, 128, 64, 0.125, 0), 1),
+    # bad sizes / scale
+    ((fake(), fake(), fake(), fake(), fake(), 0, 1, 128, 64, 0.125, 0), 1),
+    ((fake(), fake(), fake(), fake(), fake(), 1, 1, 0, 64, 0.125, 0), 1),
+    ((fake(), fake(), fake(), fake(), fake(), 1, 1, 128, 64, 0.0, 0), 1),
+    ((fake(), fake(), fake(), fake(), fake(), 1, 1, 128, 64, float("nan"), 0), 1),
+    # unsupported head dim
+    ((fake(), fake(), fake(), fake(), fake(), 1, 1, 128, 96, 0.125, 0), 2),
+    # misaligned
+    ((fake(0x10008), fake(), fake(), fake(), fake(), 1, 1, 128, 64, 0.125, 0), 3),
+    # too large
+    ((fake(), fake(), fake(), fake(), fake(), 1 << 16, 1 << 16, 1024, 64, 0.125, 0), 7),
+])
+def test_fwd_validation(lib, args, want):
+    assert lib.fa_fwd(*args, None) == want
+
+
+def test_blocksparse_validation(lib):
+    base = (fake(), fake(), fake(), fake(), fake(), 1, 1)
+    assert lib.fa_fwd_blocksparse(*base, 256, 64, 0.125, P(0), None) == 1  # no mask
+    assert lib.fa_fwd_blocksparse(*base, 200, 64, 0.125, fake(), None) == 2  # N % 128
+
+
+def test_fp32_validation(lib):
+    base = (fake(), fake(), fake(), fake(), fake(), 1, 1, 64)
+    assert lib.fa_fwd_fp32(*base, 48, 0.125, 0, None) == 2
+    assert lib.fa_fwd_fp32(*base, 256, 0.125, 0, None) == 2
+
+
+def test_bwd_validation_and_workspace(lib):
+    assert lib.fa_bwd_workspace_bytes(2, 3, 100, 64) == (2 * 2 * 3 * 100 * 4 + 255) // 256 * 256
+    assert lib.fa_bwd_workspace_bytes(0, 3, 100, 64) == 0
+    ptrs = [fake()] * 9
+    assert lib.fa_bwd(*ptrs, 1, 1, 128, 64, 0.125, 1, P(0), None) == 1
+    assert lib.fa_bwd(*ptrs, 1, 1, 128, 80, 0.125, 1, fake(), None) == 2
+
+
+def test_no_device_here_is_reported_not_crashed(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.fa_fwd(fake(), fake(), fake(), fake(), fake(), 1, 1, 128, 64, 0.125, 0, None) == 6

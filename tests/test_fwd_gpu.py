@@ -1,0 +1,158 @@
+"""Forward parity: the CUDA kernels against the fp64 oracle on the same seeded inputs.
+
+Tolerances: fp32 path max-abs 1e-5 on O; bf16 path max-abs 1e-2 and mean-abs 1e-3 on O; lse
+max-abs 1e-4 (lse is formed in fp32 from exact bf16 x bf16 products, so its error is a few fp32
+ulps of values of size ~10).
+"""
+import numpy as np
+import pytest
+import torch
+
+import helpers as H
+from exact_attention_fa_gb300 import binding as fa
+from exact_attention_fa_gb300 import workloads as wl
+from oracle import attention as orc
+
+pytestmark = pytest.mark.gpu
+
+
+def run_and_compare(w: wl.Workload, device, rows_per_head=None, heads=None):
+    """Runs the forward of workload w on the GPU; compares every row (or sampled rows/heads)."""
+    inp = wl.make_inputs(w)
+    q, k, v = (H.to_device(inp, n, device) for n in ("q", "k", "v"))
+    mask_np = inp.raw("mask") if w.block_sparse else None
+    mask = H.to_device(inp, "mask", device) if w.block_sparse else None
+    o, lse = fa.attention_forward(q, k, v, w.softmax_scale, causal=w.causal, block_mask=mask)
+    fa.fa_check_device_error()
+    o = o.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    qf, kf, vf = inp.f64("q"), inp.f64("k"), inp.f64("v")
+    rng = np.random.default_rng(1234)
+    all_heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    if heads is not None:
+        sel = rng.choice(len(all_heads), size=min(heads, len(all_heads)), replace=False)
+        all_heads = [all_heads[i] for i in sorted(sel)]
+    worst = 0.0
+    for b, h in all_heads:
+        if rows_per_head is None:
+            rows = np.arange(w.N)
+        else:
+            rows = np.unique(np.concatenate([
+                rng.choice(w.N, size=rows_per_head, replace=False),
+                [0, w.N - 1, min(w.N - 1, 127), min(w.N - 1, 128)]]))
+        O_ref, lse_ref = orc.forward_head(qf[b, h], kf[b, h], vf[b, h], w.softmax_scale,
+                                          causal=w.causal, block_mask=mask_np, rows=rows)
+        mx, _ = H.compare_o(o[b, h, rows], O_ref, bf16=(w.dtype == "bf16"))
+        H.compare_lse(lse[b, h, rows], lse_ref)
+        worst = max(worst, mx)
+    return worst, o, lse
+
+
+# ------------------------------------------------------------------------- fp32 (FMA) path
+
+def test_single_head_fp32_full(cuda):
+    w = wl.WORKLOADS["single_head_fp32"]
+    worst, _, _ = run_and_compare(w, cuda)
+    assert worst < 1e-6  # the toy fp32 kernel of the quant67 page reports 4.12e-7
+
+
+@pytest.mark.parametrize("N", [1, 31, 257])
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp32_shapes(cuda, N, d, causal):
+    w = wl.Workload("fp32_small", 2, 3, N, d, dtype="fp32", causal=causal, seed=11)
+    run_and_compare(w, cuda)
+
+
+# ------------------------------------------------------------------------- bf16 tensor-core path
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 77, 128, 129, 256, 300, 640])
+def test_bf16_small(cuda, N, d, causal):
+    w = wl.Workload("bf16_small", 2, 3, N, d, causal=causal, seed=21)
+    run_and_compare(w, cuda)
+
+
+def test_bf16_large_scores_exercise_rescaling(cuda):
+    # scale 1 with d = 128: scores of std ~11, so the running max moves often
+    w = wl.Workload("bf16_big_scores", 1, 2, 1000, 128, scale=1.0, seed=22)
+    run_and_compare(w, cuda)
+
+
+def test_mha_N2048_d64_full(cuda):
+    run_and_compare(wl.WORKLOADS["mha_N2048_d64"], cuda)
+
+
+def test_causal_N8192_d128_sampled(cuda):
+    run_and_compare(wl.WORKLOADS["causal_N8192_d128"], cuda, rows_per_head=48, heads=6)
+
+
+# ------------------------------------------------------------------------- block-sparse
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_blocksparse_small_full(cuda, d):
+    w = wl.Workload("bs_small", 2, 2, 1024, d, block_sparse=True, seed=31)
+    run_and_compare(w, cuda)
+
+
+def test_blocksparse_N16384_d64_sampled(cuda):
+    run_and_compare(wl.WORKLOADS["blocksparse_N16384_d64"], cuda, rows_per_head=32, heads=4)
+
+
+def test_all_ones_mask_equals_dense_bitwise(cuda):
+    w = wl.Workload("bs_ones", 1, 2, 512, 64, seed=32)
+    inp = wl.make_inputs(w)
+    q, k, v = (H.to_device(inp, n, cuda) for n in ("q", "k", "v"))
+    ones = torch.ones((4, 4), dtype=torch.uint8, device=cuda)
+    o1, l1 = fa.attention_forward(q, k, v, w.softmax_scale)
+    o2, l2 = fa.attention_forward(q, k, v, w.softmax_scale, block_mask=ones)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_identity_mask_is_per_tile_attention(cuda):
+    w = wl.Workload("bs_eye", 1, 1, 512, 128, seed=33)
+    inp = wl.make_inputs(w)
+    q, k, v = (H.to_device(inp, n, cuda) for n in ("q", "k", "v"))
+    eye = torch.eye(4, dtype=torch.uint8, device=cuda)
+    o, lse = fa.attention_forward(q, k, v, w.softmax_scale, block_mask=eye)
+    for t in range(4):
+        sl = slice(128 * t, 128 * t + 128)
+        ot, lt = fa.attention_forward(q[:, :, sl].contiguous(), k[:, :, sl].contiguous(),
+                                      v[:, :, sl].contiguous(), w.softmax_scale)
+        assert torch.equal(o[:, :, sl], ot) and torch.equal(lse[:, :, sl], lt)
+
+
+def test_empty_mask_rows_give_zero_and_neg_inf(cuda):
+    w = wl.Workload("bs_empty", 1, 1, 256, 64, seed=34)
+    inp = wl.make_inputs(w)
+    q, k, v = (H.to_device(inp, n, cuda) for n in ("q", "k", "v"))
+    m = torch.tensor([[0, 0], [1, 1]], dtype=torch.uint8, device=cuda)
+    o, lse = fa.attention_forward(q, k, v, w.softmax_scale, block_mask=m)
+    assert torch.all(o[:, :, :128] == 0) and torch.all(torch.isneginf(lse[:, :, :128]))
+    O_ref, lse_ref = orc.forward_head(inp.f64("q")[0, 0], inp.f64("k")[0, 0], inp.f64("v")[0, 0],
+                                      w.softmax_scale, block_mask=m.cpu().numpy())
+    H.compare_o(o[0, 0].float().cpu().numpy(), O_ref, bf16=True)
+    H.compare_lse(lse[0, 0].cpu().numpy(), lse_ref)
+
+
+def test_causal_first_row_is_v0(cuda):
+    w = wl.Workload("c_first", 1, 1, 300, 64, causal=True, seed=35)
+    inp = wl.make_inputs(w)
+    q, k, v = (H.to_device(inp, n, cuda) for n in ("q", "k", "v"))
+    o, _ = fa.attention_forward(q, k, v, w.softmax_scale, causal=True)
+    assert torch.equal(o[0, 0, 0], v[0, 0, 0])
+
+
+def test_outputs_do_not_touch_neighbours(cuda):
+    """Rows past N are never written (ragged tail): guard rows around the output stay intact."""
+    w = wl.Workload("guard", 1, 1, 200, 64, seed=36)
+    inp = wl.make_inputs(w)
+    q, k, v = (H.to_device(inp, n, cuda) for n in ("q", "k", "v"))
+    big = torch.full((1, 1, 400, 64), 7.0, dtype=torch.bfloat16, device=cuda)
+    lse_big = torch.full((1, 1, 400), 7.0, dtype=torch.float32, device=cuda)
+    o = big[:, :, :200]
+    lse = lse_big[:, :, :200]
+    fa.fa_fwd(q, k, v, o.contiguous() if not o.is_contiguous() else o, lse, w.softmax_scale)
+    torch.cuda.synchronize()
+    assert torch.all(big[:, :, 200:] == 7.0) and torch.all(lse_big[:, :, 200:] == 7.0)
