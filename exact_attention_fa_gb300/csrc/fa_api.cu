@@ -185,8 +185,8 @@ int fa_fwd_fp32(const float* q, const float* k, const float* v, float* o, float*
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   (void)d;
   if (B < 1 || H < 1 || N < 1) return 0;
-  const size_t rows = static_cast<size_t>(B) * H * N;
-  return (2 * rows * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  const size_t rows = static_cast<size_t>(B) * H * ((static_cast<size_t>(N) + 127) / 128) * 128;
+  return 2 * rows * sizeof(float);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
@@ -214,7 +214,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   p.dq = dq;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
-  const size_t rows = static_cast<size_t>(BH) * N;
+  const size_t rows = static_cast<size_t>(BH) * ((static_cast<size_t>(N) + 127) / 128) * 128;
   p.lse2 = static_cast<float*>(workspace);
   p.Dsum = static_cast<float*>(workspace) + rows;
   p.BH = BH;

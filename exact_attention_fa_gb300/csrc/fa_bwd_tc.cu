@@ -1,6 +1,498 @@
-// Backward (placeholder until the tcgen05 backward lands).
+// Backward by recomputation on the tcgen05 tensor cores.
+//
+// The forward keeps only O and the row statistic lse; the backward rebuilds S and P tile by tile
+// ("3 · FlashAttention", 3.4; "FlashAttention：在线 softmax 与 IO-aware 注意力", section 五) and
+// applies softmax calculus:
+//     P = exp(scale * Q K^T - lse),  dV = P^T dO,  dP = dO V^T,  D_i = sum_k dO_ik O_ik,
+//     dS = P * (dP - D),  dQ = scale * dS K,  dK = scale * dS^T Q.
+//
+// Kernel 1 (prep): per row, D_i and lse2_i = lse_i * log2(e) into the workspace (padded to whole
+// 128-row tiles: +inf / 0 on padding rows so that they contribute nothing), and dQ zeroed.
+//
+// Kernel 2 (main), one CTA per (128-key tile j, head), 14 warps:
+//   * warp 8 (one lane): TMA. K_j and V_j once; then per query tile i, Q_i, dO_i and the 128
+//     lse2 / D values of that tile into a two-stage ring;
+//   * warp 9 (one lane): MMAs. S^T = K Q_i^T and dP^T = V dO_i^T (keys on TMEM lanes, queries on
+//     columns); dV += P^T dO_i and dK += dS^T Q_i with P^T / dS^T read from TMEM; dQ_i = dS K with
+//     dS read from shared memory;
+//   * warps 0-7 (two warpgroups, one per half of the query columns): thread = key row. Computes
+//     P^T = exp2(S^T * scale * log2e - lse2) (causal / tail masked), writes it as bf16 over S^T,
+//     then dS^T = P^T * (dP^T - D) as bf16 over dP^T and, transposed by its layout, into the
+//     shared-memory operand of the dQ product; at the end stores dV and scale * dK;
+//   * warps 10-13: thread = query row; reads dQ_i from TMEM and adds scale * dQ_i into the fp32
+//     output with vector reductions.
+// TMEM columns: S^T [0,128), dP^T [128,256) (dQ_i reuses it after dS^T was consumed),
+// dV [256, 256+d), dK [256+d, 256+2d).
+#include <cuda_bf16.h>
+#include <math.h>
+
 #include "fa_internal.h"
+#include "fa_ptx.cuh"
 
 namespace fa {
-cudaError_t launch_bwd(const BwdParams&, int, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int BT = 128;  // keys per CTA tile = queries per inner tile
+constexpr int kComputeWarps = 8;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kDrainWarp0 = 10;
+constexpr int kThreads = 14 * 32;
+constexpr int kBoxBytes = 128 * 64 * 2;
+
+template <int D>
+struct BCfg {
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kStages = D == 128 ? 2 : 3;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTileBytes;
+  static constexpr int kOffDS = 2 * kTileBytes;           // 128 x 128 bf16, two 64-query boxes
+  static constexpr int kOffStage = kOffDS + 2 * kBoxBytes;
+  // per stage: Q_i, dO_i, lse2[128], D[128]
+  static constexpr int kStageQ = 0;
+  static constexpr int kStageDO = kTileBytes;
+  static constexpr int kStageLse = 2 * kTileBytes;
+  static constexpr int kStageD = 2 * kTileBytes + 512;
+  static constexpr int kStageBytes = 2 * kTileBytes + 1024;
+  static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+  static constexpr int kBarKV = 0;
+  static constexpr int kBarFull = 1;
+  static constexpr int kBarEmpty = 1 + kStages;
+  static constexpr int kBarS = 1 + 2 * kStages;
+  static constexpr int kBarDP = kBarS + 1;
+  static constexpr int kBarP = kBarS + 2;
+  static constexpr int kBarDS = kBarS + 3;
+  static constexpr int kBarDQFull = kBarS + 4;
+  static constexpr int kBarDQEmpty = kBarS + 5;
+  static constexpr int kBarAcc = kBarS + 6;
+  static constexpr int kBarDrain = kBarS + 7;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kOffTmemPtr = kOffBar + 8 * kNumBars;
+  static constexpr int kOffAbort = kOffTmemPtr + 4;
+  static constexpr int kSmemBytes = kOffAbort + 4;  // the base must be 1024-aligned (checked)
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+};
+
+__device__ __forceinline__ void tma_bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// CTA -> (head, key tile). Heads in L2-sized groups; inside a group the key tiles with the most
+// query tiles to visit (causal: the first ones) come first.
+__device__ __forceinline__ void decode_bwd(const BwdParams& p, int group, int& bh, int& j) {
+  const int per_group = group * p.n_tiles;
+  const int g = blockIdx.x / per_group;
+  const int within = blockIdx.x - g * per_group;
+  const int gsize = min(group, p.BH - g * group);
+  j = within / gsize;
+  bh = g * group + within % gsize;
+}
+
+// TMEM column holding the packed bf16 pair of queries (16k, 16k+1) of the P^T / dS^T operand:
+// the warpgroup owning query columns [64c, 64c+64) packs them into columns [64c, 64c+32).
+__device__ __forceinline__ uint32_t packed_col(int k) { return k < 4 ? 8u * k : 64u + 8u * (k - 4); }
+
+template <int D>
+__device__ void bwd_producer(const BwdParams& p, uint32_t sbase, const Ctl& ctl, int bh, int j,
+                             int i0, int npad) {
+  using C = BCfg<D>;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
+  tma_prefetch_desc(&p.tm_q);
+  tma_prefetch_desc(&p.tm_k);
+  tma_prefetch_desc(&p.tm_v);
+  tma_prefetch_desc(&p.tm_do);
+  mbar_arrive_expect_tx(bar(C::kBarKV), 2 * C::kTileBytes);
+  for (int b = 0; b < D / 64; ++b) {
+    tma_load_3d(sbase + C::kOffK + b * kBoxBytes, &p.tm_k, bar(C::kBarKV), b * 64, j * BT, bh);
+    tma_load_3d(sbase + C::kOffV + b * kBoxBytes, &p.tm_v, bar(C::kBarKV), b * 64, j * BT, bh);
+  }
+  int issued[C::kStages];
+#pragma unroll
+  for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
+  bool ok = true;
+  for (int i = i0, it = 0; i < p.n_tiles; ++i, ++it) {
+    const int st = it % C::kStages;
+    const int round = it / C::kStages;
+    if (!mbar_wait(bar(C::kBarEmpty + st), (round & 1) ^ 1, ctl)) { ok = false; break; }
+    const uint32_t sb = sbase + C::kOffStage + st * C::kStageBytes;
+    mbar_arrive_expect_tx(bar(C::kBarFull + st), 2 * C::kTileBytes + 1024);
+    for (int b = 0; b < D / 64; ++b) {
+      tma_load_3d(sb + C::kStageQ + b * kBoxBytes, &p.tm_q, bar(C::kBarFull + st), b * 64, i * BT, bh);
+      tma_load_3d(sb + C::kStageDO + b * kBoxBytes, &p.tm_do, bar(C::kBarFull + st), b * 64, i * BT, bh);
+    }
+    const size_t r0 = static_cast<size_t>(bh) * npad + static_cast<size_t>(i) * BT;
+    tma_bulk_g2s(sb + C::kStageLse, p.lse2 + r0, 512, bar(C::kBarFull + st));
+    tma_bulk_g2s(sb + C::kStageD, p.Dsum + r0, 512, bar(C::kBarFull + st));
+    issued[st] = round;
+  }
+  if (!ok) {
+    Ctl drain = ctl;
+    int zero = 0;
+    drain.abort_flag = &zero;
+    mbar_wait(bar(C::kBarKV), 0, drain);
+    for (int s = 0; s < C::kStages; ++s)
+      if (issued[s] >= 0) mbar_wait(bar(C::kBarFull + s), issued[s] & 1, drain);
+  }
+}
+
+template <int D>
+__device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const Ctl& ctl, int i0) {
+  using C = BCfg<D>;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
+  constexpr uint32_t kIdescT = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T: both K-major
+  constexpr uint32_t kIdescG = idesc_bf16(128, D, 0, 1);    // dV, dK: A in TMEM, B MN-major
+  constexpr uint32_t kIdescQ = idesc_bf16(128, D, 1, 1);    // dQ: A = dS MN-major, B = K MN-major
+
+  bool ok = mbar_wait(bar(C::kBarKV), 0, ctl);
+  tc_fence_after();
+  const uint32_t ka = sbase + C::kOffK, va = sbase + C::kOffV, dsa = sbase + C::kOffDS;
+  for (int i = i0, it = 0; ok && i < p.n_tiles; ++i, ++it) {
+    const int st = it % C::kStages;
+    const uint32_t sb = sbase + C::kOffStage + st * C::kStageBytes;
+    const uint32_t qa = sb + C::kStageQ, doa = sb + C::kStageDO;
+    if (!mbar_wait(bar(C::kBarFull + st), (it / C::kStages) & 1, ctl)) { ok = false; break; }
+    tc_fence_after();
+    // S^T = K Q_i^T
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      const uint32_t off = (k / 4) * kBoxBytes + (k % 4) * 32;
+      mma_ss(tmem + C::kColS, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
+             kIdescT, k > 0);
+    }
+    mma_commit(bar(C::kBarS));
+    // dP^T = V dO_i^T, into columns the previous dQ_i occupied until drained
+    if (it > 0) {
+      if (!mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+    }
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      const uint32_t off = (k / 4) * kBoxBytes + (k % 4) * 32;
+      mma_ss(tmem + C::kColDP, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(doa + off, 16, 1024),
+             kIdescT, k > 0);
+    }
+    mma_commit(bar(C::kBarDP));
+    // dV += P^T dO_i
+    if (!mbar_wait(bar(C::kBarP), it & 1, ctl)) { ok = false; break; }
+    tc_fence_after();
+#pragma unroll
+    for (int k = 0; k < BT / 16; ++k)
+      mma_ts(tmem + C::kColDV, tmem + C::kColS + packed_col(k),
+             sdesc_sw128(doa + k * 2048, kBoxBytes, 1024), kIdescG, (it > 0 || k > 0) ? 1u : 0u);
+    // dK += dS^T Q_i ; dQ_i = dS K
+    if (!mbar_wait(bar(C::kBarDS), it & 1, ctl)) { ok = false; break; }
+    tc_fence_after();
+#pragma unroll
+    for (int k = 0; k < BT / 16; ++k)
+      mma_ts(tmem + C::kColDK, tmem + C::kColDP + packed_col(k),
+             sdesc_sw128(qa + k * 2048, kBoxBytes, 1024), kIdescG, (it > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+    for (int k = 0; k < BT / 16; ++k)
+      mma_ss(tmem + C::kColDP, sdesc_sw128(dsa + k * 2048, kBoxBytes, 1024),
+             sdesc_sw128(ka + k * 2048, kBoxBytes, 1024), kIdescQ, k > 0);
+    mma_commit(bar(C::kBarDQFull));
+    mma_commit(bar(C::kBarEmpty + st));
+  }
+  if (ok) {
+    mma_commit(bar(C::kBarAcc));
+  } else {
+    Ctl drain = ctl;
+    int zero = 0;
+    drain.abort_flag = &zero;
+    mma_commit(bar(C::kBarDrain));
+    mbar_wait(bar(C::kBarDrain), 0, drain);
+  }
+}
+
+template <int D>
+__device__ void bwd_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, uint32_t tmem,
+                            const Ctl& ctl, int bh, int j, int i0) {
+  using C = BCfg<D>;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int half = warp / 4;  // query columns [64*half, 64*half + 64)
+  const int quad = warp % 4;
+  const int r = quad * 32 + lane;  // key row within the tile (TMEM lane)
+  const int key = j * BT + r;
+  const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+  const uint32_t tS = tmem + lane_off + C::kColS + 64 * half;
+  const uint32_t tDP = tmem + lane_off + C::kColDP + 64 * half;
+  const float sl2 = p.scale_log2;
+  uint8_t* ds_row = smem + C::kOffDS + half * kBoxBytes + r * 128;
+
+  bool ok = true;
+  for (int i = i0, it = 0; i < p.n_tiles; ++i, ++it) {
+    const int st = it % C::kStages;
+    const float* lse2 = reinterpret_cast<const float*>(smem + C::kOffStage + st * C::kStageBytes +
+                                                       C::kStageLse) + 64 * half;
+    const float* dsum = reinterpret_cast<const float*>(smem + C::kOffStage + st * C::kStageBytes +
+                                                       C::kStageD) + 64 * half;
+    if (!mbar_wait(bar(C::kBarFull + st), (it / C::kStages) & 1, ctl)) { ok = false; break; }
+    if (!mbar_wait(bar(C::kBarS), it & 1, ctl)) { ok = false; break; }
+    tc_fence_after();
+    // queries of this thread's columns: q = i*128 + 64*half + x; allowed iff key <= q (causal)
+    // and key < N
+    int lim;  // number of leading columns x whose P is forced to zero
+    if (key >= p.N) lim = 64;
+    else if (p.causal && i == j) lim = min(64, max(0, r - 64 * half));
+    else lim = 0;
+
+    float pv[64];
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+      uint32_t s[32];
+      tmem_ld32(tS + 32 * ch, s);
+      uint32_t pk[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int x0 = 32 * ch + 2 * u;
+        float p0 = ex2(fmaf(__uint_as_float(s[2 * u]), sl2, -lse2[x0]));
+        float p1 = ex2(fmaf(__uint_as_float(s[2 * u + 1]), sl2, -lse2[x0 + 1]));
+        p0 = x0 < lim ? 0.f : p0;
+        p1 = x0 + 1 < lim ? 0.f : p1;
+        pv[x0] = p0;
+        pv[x0 + 1] = p1;
+        pk[u] = pack_bf16(p0, p1);
+      }
+      tmem_st16(tS + 16 * ch, pk);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(bar(C::kBarP));
+
+    if (!mbar_wait(bar(C::kBarDP), it & 1, ctl)) { ok = false; break; }
+    tc_fence_after();
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+      uint32_t dp[32];
+      tmem_ld32(tDP + 32 * ch, dp);
+      uint32_t pk[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int x0 = 32 * ch + 2 * u;
+        const float d0 = pv[x0] * (__uint_as_float(dp[2 * u]) - dsum[x0]);
+        const float d1 = pv[x0 + 1] * (__uint_as_float(dp[2 * u + 1]) - dsum[x0 + 1]);
+        pk[u] = pack_bf16(d0, d1);
+      }
+      tmem_st16(tDP + 16 * ch, pk);
+      // dS (queries contiguous per key row) into the 128-byte-swizzled MN-major operand
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int chunk = (4 * ch + u) ^ (r & 7);
+        *reinterpret_cast<uint4*>(ds_row + chunk * 16) =
+            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      }
+    }
+    tmem_st_wait();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(bar(C::kBarDS));
+  }
+  if (!ok) return;
+
+  // epilogue: dV and scale * dK, this warpgroup's half of the d columns
+  if (!mbar_wait(bar(C::kBarAcc), 0, ctl)) return;
+  tc_fence_after();
+  constexpr int kHalf = D / 2;
+#pragma unroll 1
+  for (int which = 0; which < 2; ++which) {
+    const uint32_t col = (which ? C::kColDK : C::kColDV) + kHalf * half;
+    const float mul = which ? p.scale : 1.f;
+    __nv_bfloat16* out = (which ? p.dk : p.dv) + (static_cast<size_t>(bh) * p.N + key) * D + kHalf * half;
+#pragma unroll 1
+    for (int c = 0; c < kHalf; c += 32) {
+      uint32_t v[32];
+      tmem_ld32(tmem + lane_off + col + c, v);
+      if (key < p.N) {
+        uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint4 w;
+          w.x = pack_bf16(__uint_as_float(v[8 * u + 0]) * mul, __uint_as_float(v[8 * u + 1]) * mul);
+          w.y = pack_bf16(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul);
+          w.z = pack_bf16(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul);
+          w.w = pack_bf16(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul);
+          dst[u] = w;
+        }
+      }
+    }
+  }
+}
+
+template <int D>
+__device__ void bwd_drain(const BwdParams& p, uint32_t sbase, uint32_t tmem, const Ctl& ctl, int bh,
+                          int i0) {
+  using C = BCfg<D>;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int quad = warp % 4;
+  const int qr = quad * 32 + lane;  // query row within the tile (TMEM lane)
+  const uint32_t tQ = tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::kColDP;
+  for (int i = i0, it = 0; i < p.n_tiles; ++i, ++it) {
+    if (!mbar_wait(bar(C::kBarDQFull), it & 1, ctl)) return;
+    tc_fence_after();
+    const int q = i * BT + qr;
+    float4* dst = reinterpret_cast<float4*>(p.dq + (static_cast<size_t>(bh) * p.N + q) * D);
+#pragma unroll 1
+    for (int c = 0; c < D; c += 32) {
+      uint32_t v[32];
+      tmem_ld32(tQ + c, v);
+      if (q < p.N) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          atomicAdd(dst + c / 4 + u,
+                    make_float4(__uint_as_float(v[4 * u]) * p.scale, __uint_as_float(v[4 * u + 1]) * p.scale,
+                                __uint_as_float(v[4 * u + 2]) * p.scale, __uint_as_float(v[4 * u + 3]) * p.scale));
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(bar(C::kBarDQEmpty));
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_constant__ BwdParams p,
+                                                             int group, int npad) {
+  using C = BCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemPtr);
+  const Ctl ctl{abort_flag, p.err, p.timeout_ns};
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
+  if (sbase & 1023u) {  // swizzled operands need a 1 KB aligned base; report, never misread
+    if (threadIdx.x == 0) atomicOr(p.err, kErrSmemAlign);
+    return;
+  }
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  int bh, j;
+  decode_bwd(p, group, bh, j);
+  const int i0 = p.causal ? j : 0;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(C::kBarKV), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kBarFull + s), 1);
+      mbar_init(bar(C::kBarEmpty + s), 1);
+    }
+    mbar_init(bar(C::kBarS), 1);
+    mbar_init(bar(C::kBarDP), 1);
+    mbar_init(bar(C::kBarP), kComputeWarps * 32);
+    mbar_init(bar(C::kBarDS), kComputeWarps * 32);
+    mbar_init(bar(C::kBarDQFull), 1);
+    mbar_init(bar(C::kBarDQEmpty), 128);
+    mbar_init(bar(C::kBarAcc), 1);
+    mbar_init(bar(C::kBarDrain), 1);
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < kComputeWarps) {
+    bwd_compute<D>(p, sbase, smem, tmem, ctl, bh, j, i0);
+  } else if (warp == kLoadWarp) {
+    if (lane == 0) bwd_producer<D>(p, sbase, ctl, bh, j, i0, npad);
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) bwd_mma<D>(p, sbase, tmem, ctl, i0);
+    __syncwarp();
+  } else {
+    bwd_drain<D>(p, sbase, tmem, ctl, bh, i0);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// prep: D_i = sum_k dO_ik O_ik, lse2_i = lse_i * log2(e) (padding rows: D = 0, lse2 = +inf),
+// dQ rows zeroed. D / 8 threads per row, 8 elements each.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ BwdParams p, int npad) {
+  constexpr int kTpr = D / 8;
+  const long long total = static_cast<long long>(p.BH) * npad * kTpr;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const int lane = threadIdx.x % 32;
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t - lane < total;
+       t += stride) {
+    const bool valid = t < total;
+    const long long row = t / kTpr;
+    const int part = static_cast<int>(t % kTpr);
+    const int bh = static_cast<int>(row / npad);
+    const int q = static_cast<int>(row % npad);
+    float acc = 0.f;
+    if (valid && q < p.N) {
+      const size_t off = (static_cast<size_t>(bh) * p.N + q) * D + part * 8;
+      const uint4 a = *reinterpret_cast<const uint4*>(p.dO + off);
+      const uint4 b = *reinterpret_cast<const uint4*>(p.o + off);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 x = __bfloat1622float2(a2[u]);
+        const float2 y = __bfloat1622float2(b2[u]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+      float4* dq = reinterpret_cast<float4*>(p.dq + off);
+      dq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      dq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(~0u, acc, off);
+    if (valid && part == 0) {
+      const bool in = q < p.N;
+      p.Dsum[row] = in ? acc : 0.f;
+      p.lse2[row] = in ? p.lse[static_cast<size_t>(bh) * p.N + q] * 1.4426950408889634f : INFINITY;
+    }
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const BwdParams& p, int num_sms, cudaStream_t s) {
+  using C = BCfg<D>;
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int npad = p.n_tiles * BT;
+  bwd_prep_kernel<D><<<num_sms * 8, 256, 0, s>>>(p, npad);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long head_bytes = 4ll * p.N * D * 2;
+  long long g = (32ll << 20) / head_bytes;
+  const int group = static_cast<int>(g < 1 ? 1 : (g > p.BH ? p.BH : g));
+  const long long grid = static_cast<long long>(p.n_tiles) * p.BH;
+  if (grid > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+  bwd_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, s>>>(p, group, npad);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t s) {
+  if (p.d == 64) return launch_d<64>(p, num_sms, s);
+  if (p.d == 128) return launch_d<128>(p, num_sms, s);
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace fa

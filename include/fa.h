@@ -72,7 +72,8 @@ int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, flo
                        int H, int N, int d, float scale, const uint8_t* block_mask,
                        fa_stream_t stream);
 
-/* Bytes of device workspace fa_bwd needs: 2 * B*H*N fp32 (rounded up to 256 bytes). */
+/* Bytes of device workspace fa_bwd needs: two fp32 values per row of B*H*ceil(N/128)*128 rows
+ * (rows padded to whole 128-row tiles). */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
 /* Backward by recomputation ("3 · FlashAttention", 3.4; "FlashAttention：在线 softmax 与

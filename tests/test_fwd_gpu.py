@@ -16,7 +16,7 @@ from oracle import attention as orc
 pytestmark = pytest.mark.gpu
 
 
-def run_and_compare(w: wl.Workload, device, rows_per_head=None, heads=None):
+def run_and_compare(w: wl.Workload, device, rows_per_head=None, heads=None, relative_above_one=False):
     """Runs the forward of workload w on the GPU; compares every row (or sampled rows/heads)."""
     inp = wl.make_inputs(w)
     q, k, v = (H.to_device(inp, n, device) for n in ("q", "k", "v"))
@@ -42,7 +42,8 @@ def run_and_compare(w: wl.Workload, device, rows_per_head=None, heads=None):
                 [0, w.N - 1, min(w.N - 1, 127), min(w.N - 1, 128)]]))
         O_ref, lse_ref = orc.forward_head(qf[b, h], kf[b, h], vf[b, h], w.softmax_scale,
                                           causal=w.causal, block_mask=mask_np, rows=rows)
-        mx, _ = H.compare_o(o[b, h, rows], O_ref, bf16=(w.dtype == "bf16"))
+        mx, _ = H.compare_o(o[b, h, rows], O_ref, bf16=(w.dtype == "bf16"),
+                            relative_above_one=relative_above_one)
         H.compare_lse(lse[b, h, rows], lse_ref)
         worst = max(worst, mx)
     return worst, o, lse
@@ -75,9 +76,10 @@ def test_bf16_small(cuda, N, d, causal):
 
 
 def test_bf16_large_scores_exercise_rescaling(cuda):
-    # scale 1 with d = 128: scores of std ~11, so the running max moves often
+    # scale 1 with d = 128: scores of std ~11, so the running max moves often and the softmax is
+    # nearly one-hot (outputs as large as the values themselves, hence the relative bound)
     w = wl.Workload("bf16_big_scores", 1, 2, 1000, 128, scale=1.0, seed=22)
-    run_and_compare(w, cuda)
+    run_and_compare(w, cuda, relative_above_one=True)
 
 
 def test_mha_N2048_d64_full(cuda):
