@@ -44,7 +44,8 @@ def compare_o(got: np.ndarray, want: np.ndarray, bf16: bool, relative_above_one:
 def compare_lse(got: np.ndarray, want: np.ndarray, tol=LSE_MAX_ABS):
     got = got.astype(np.float64)
     both_inf = np.isneginf(got) & np.isneginf(want)
-    err = np.where(both_inf, 0.0, np.abs(got - want))
+    with np.errstate(invalid="ignore"):
+        err = np.where(both_inf, 0.0, np.abs(got - want))
     assert np.all(np.isfinite(err)), "lse: -inf mismatch"
     assert err.max() <= tol, f"lse max abs {err.max():.3e}"
     return float(err.max())

@@ -40,8 +40,12 @@ def run_bwd(w: wl.Workload, device, heads=None):
             want[n].append(g)
             have[n].append(got[n][b, h])
     errs = {}
+    # With a single allowed key per row dS is identically zero, so dQ and dK vanish; their error is
+    # then measured against 1% of the norm of dV (a gradient of the same problem and scale).
+    floor = 1e-2 * np.linalg.norm(np.stack(want["dv"]).ravel())
     for n in ("dq", "dk", "dv"):
-        errs[n] = H.rel_fro(np.stack(have[n]), np.stack(want[n]))
+        w_, h_ = np.stack(want[n]), np.stack(have[n])
+        errs[n] = float(np.linalg.norm((h_ - w_).ravel()) / max(np.linalg.norm(w_.ravel()), floor))
         assert errs[n] <= H.GRAD_REL_FRO, f"{n}: relative Frobenius error {errs[n]:.3e}"
     return errs
 
