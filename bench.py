@@ -1,0 +1,450 @@
+#!/usr/bin/env python
+"""Throughput of the exact-attention hot path on GB300 (one JSON line on stdout).
+
+A step is one pass of the whole path over one batch: the tensor-core forward (O, lse) and, for
+workloads with a backward, the recomputing backward (dQ, dK, dV) -- every launch goes through the
+C ABI of libfa_gb300.so. The default workload is multi-head attention B=4, H=16, N=2048, d=64,
+bf16, non-causal, forward + backward.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Metric: TFLOPS = algorithmic FLOPs / time, with 4*B*H*N^2*d for the forward (causal: half;
+block-sparse: active tiles only) and 2.5 times that for the backward (its five contractions).
+`value` is timed with CUDA events around the kernels only (inputs resident in HBM, L2 flushed
+between steps by writing a 512 MiB buffer); `e2e` is the same step through the public API from
+pinned host buffers, host<->device copies inside the timed region. Under torchrun every rank runs
+its own replica of the workload (independent heads: no collective on the data path) and `value`
+sums over ranks using the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle (the parity reference) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "mha_N2048_d64"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def bench_workload(name: str):
+    from exact_attention_fa_gb300 import workloads as wl
+    w = wl.WORKLOADS[name]
+    if name == DEFAULT_WORKLOAD:  # the default step is the whole path: forward + backward
+        w = w.with_(backward=True)
+    return w
+
+
+def flops(w, mask=None):
+    from exact_attention_fa_gb300 import workloads as wl
+    f = wl.flop_count(w, mask, "fwd")
+    return f, (2.5 * f if w.backward else 0.0)
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------------------- CPU
+
+def oracle_tasks(w, inp, heads):
+    mask = inp.raw("mask") if w.block_sparse else None
+    tasks = []
+    for idx in heads:
+        b, h = divmod(idx % (w.B * w.H), w.H)
+        do = inp.raw("do")[b, h] if w.backward else None
+        tasks.append((inp.raw("q")[b, h], inp.raw("k")[b, h], inp.raw("v")[b, h], do,
+                      w.softmax_scale, w.causal, mask))
+    return tasks
+
+
+def make_pool(cores):
+    import multiprocessing as mp
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"  # one BLAS thread per worker: `cores` threads in total
+    from oracle import cpu_baseline
+    pool = mp.get_context("spawn").Pool(cores)
+    pool.map(cpu_baseline.warm, range(cores))
+    return pool
+
+
+def time_oracle(pool, tasks):
+    from oracle import cpu_baseline
+    t0 = time.perf_counter()
+    pool.map(cpu_baseline.run_head, tasks, chunksize=1)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline_leg(w, inp, budget_s=20.0):
+    """The oracle on a bounded sample of the workload's heads, on all host cores."""
+    if w.dtype != "bf16":
+        return None
+    cores = host_cores()
+    pool = make_pool(cores)
+    try:
+        f_fwd, f_bwd = flops(w, inp.raw("mask") if w.block_sparse else None)
+        per_head = (f_fwd + f_bwd) / (w.B * w.H)
+        # one probe round of `cores` heads, then as many whole rounds as fit the budget
+        n = min(cores, w.B * w.H)
+        dt = time_oracle(pool, oracle_tasks(w, inp, range(n)))
+        rounds = max(0, min(int(budget_s / max(dt, 1e-3)) - 1, (w.B * w.H) // n - 1))
+        heads, total = n, dt
+        if rounds:
+            more = range(n, n + rounds * n)
+            total += time_oracle(pool, oracle_tasks(w, inp, more))
+            heads += len(more)
+    finally:
+        pool.terminate()
+    return {"value": per_head * heads / total / 1e12, "unit": "TFLOPS", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{heads} of {w.B * w.H} heads of {w.name}, fp64 numpy oracle "
+                      f"({'forward+backward' if w.backward else 'forward'}), one head per worker",
+            "seconds": round(total, 3)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = bench_workload(args.workload)
+    from exact_attention_fa_gb300 import workloads as wl
+    inp = wl.make_inputs(w, with_do=w.backward)
+    cores = host_cores()
+    n = min(cores, w.B * w.H)
+    f_fwd, f_bwd = flops(w, inp.raw("mask") if w.block_sparse else None)
+    per_head = (f_fwd + f_bwd) / (w.B * w.H)
+    pool = make_pool(cores)
+    times = []
+    try:
+        for i in range(args.warmup + args.steps):
+            dt = time_oracle(pool, oracle_tasks(w, inp, range(i * n, (i + 1) * n)))
+            if i >= args.warmup:
+                times.append(dt)
+    finally:
+        pool.terminate()
+    t = statistics.fmean(times)
+    value = per_head * n / t / 1e12
+    sample = (f"{n} heads of {w.name} per step (one per worker), fp64 numpy oracle, "
+              f"{'forward+backward' if w.backward else 'forward'}")
+    print(json.dumps({
+        "impl": "reference", "metric": metric_name(w), "value": value, "unit": "TFLOPS",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, args.gpus, note="oracle on host cores"),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def metric_name(w):
+    return "attention fwd/bwd TFLOPS (4·B·H·N²·d, causal halved)"
+
+
+def config_of(w, n_gpus, note=None):
+    c = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype,
+         "causal": w.causal, "block_sparse": w.block_sparse,
+         "step": "forward+backward" if w.backward else "forward",
+         "global_batch": w.B * n_gpus, "seq_len": w.N, "parallelism": f"replicas{n_gpus}",
+         "l2": "flushed between steps (512 MiB write)"}
+    if note:
+        c["note"] = note
+    return c
+
+
+# ----------------------------------------------------------------------------------------- GPU
+
+class ClockSampler:
+    def __init__(self, path):
+        self.path = path
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self, device_index):
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9 or parts[0] != str(device_index):
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for nm, val in zip(names[1:], parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = bench_workload(args.workload)
+    from exact_attention_fa_gb300 import workloads as wl
+
+    # host inputs first (and the oracle pool, if any, is spawned before CUDA is touched)
+    inp = wl.make_inputs(w, with_do=w.backward)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_leg(w, inp)
+
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import exact_attention_fa_gb300 as fa
+    fa.load()
+
+    def dev_tensor(name):
+        a = inp.raw(name)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    q, k, v = dev_tensor("q"), dev_tensor("k"), dev_tensor("v")
+    do = dev_tensor("do") if w.backward else None
+    mask = dev_tensor("mask") if w.block_sparse else None
+    scale = w.softmax_scale
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    if w.backward:
+        dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        dk, dv = torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8,
+                         device=dev)
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def fwd():
+        if w.dtype == "fp32":
+            fa.fa_fwd_fp32(q, k, v, o, lse, scale, w.causal)
+        elif w.block_sparse:
+            fa.fa_fwd_blocksparse(q, k, v, o, lse, scale, mask)
+        else:
+            fa.fa_fwd(q, k, v, o, lse, scale, w.causal)
+
+    def bwd():
+        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, w.causal, ws)
+
+    launches_per_step = (1 + (2 if w.backward else 0))
+    f_fwd, f_bwd = flops(w, inp.raw("mask") if w.block_sparse else None)
+
+    for _ in range(args.warmup):
+        flush_buf.zero_()
+        fwd()
+        if w.backward:
+            bwd()
+    fa.fa_check_device_error(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(os.path.join("/tmp", f"fa_clocks_{os.getpid()}.csv")) as clocks:
+        time.sleep(0.1)
+        t0 = time.perf_counter()
+        for i in range(K):
+            flush_buf.zero_()
+            ev[i][0].record()
+            fwd()
+            ev[i][1].record()
+            if w.backward:
+                bwd()
+            ev[i][2].record()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        wall = time.perf_counter() - t0
+        time.sleep(0.1)
+    fa.fa_check_device_error(dev)
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)] if w.backward else [0.0]
+    t_step = statistics.fmean(step_ms)
+    t_fwd = statistics.fmean(fwd_ms)
+    t_bwd = statistics.fmean(bwd_ms)
+    if world > 1:
+        tt = torch.tensor([t_step, t_fwd, t_bwd], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step, t_fwd, t_bwd = tt.tolist()
+
+    # ------------------------------------------------------------------ end to end, host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = {n: t.cpu().pin_memory() for n, t in (("q", q), ("k", k), ("v", v))}
+        if w.backward:
+            pin["do"] = do.cpu().pin_memory()
+        outs = {"o": o, "lse": lse}
+        if w.backward:
+            outs.update(dq=dq, dk=dk, dv=dv)
+        host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs.items()}
+        dev_in = {"q": q, "k": k, "v": v, "do": do}
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+        E = min(K, 100)
+        ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(E)]
+        for i in range(-2, E):
+            flush_buf.zero_()
+            if i >= 0:
+                ee[i][0].record()
+            for n, t in pin.items():
+                dev_in[n].copy_(t, non_blocking=True)
+            fwd()
+            if w.backward:
+                bwd()
+            for n, t in outs.items():
+                host_out[n].copy_(t, non_blocking=True)
+            if i >= 0:
+                ee[i][1].record()
+        torch.cuda.synchronize()
+        fa.fa_check_device_error(dev)
+        t_e2e = statistics.fmean(ee[i][0].elapsed_time(ee[i][1]) for i in range(E))
+        if world > 1:
+            tt = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            t_e2e = tt.item()
+        e2e = {"value": world * (f_fwd + f_bwd) / (t_e2e * 1e-3) / 1e12, "unit": "TFLOPS",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e,
+               "steps": E}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    # dominant kernel: the part of the step that takes longer
+    if w.backward and t_bwd >= t_fwd:
+        kname = f"bwd_tc_kernel<{w.d}> (+ bwd_prep_kernel<{w.d}> in the same call)"
+        kflops, kms = f_bwd, t_bwd
+    else:
+        kname = ("fwd_fp32_kernel" if w.dtype == "fp32" else "fwd_tc_kernel") + f"<{w.d}>"
+        kflops, kms = f_fwd, t_fwd
+    achieved = kflops / (kms * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    traffic = recorded_traffic(kname, w)
+    value = world * (f_fwd + f_bwd) / (t_step * 1e-3) / 1e12
+    line = {
+        "metric": metric_name(w), "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp32" if w.dtype == "fp32" else "bf16",
+        "data": "synthetic: i.i.d. N(0,1) inputs, seeded" + (", rounded to bf16" if w.dtype == "bf16" else ""),
+        "config": config_of(w, world),
+        "parts": {
+            "fwd": {"ms": t_fwd, "tflops": f_fwd / (t_fwd * 1e-3) / 1e12,
+                    "frac_of_bf16_peak": f_fwd / (t_fwd * 1e-3) / 1e12 / peak},
+            **({"bwd": {"ms": t_bwd, "tflops": f_bwd / (t_bwd * 1e-3) / 1e12,
+                        "frac_of_bf16_peak": f_bwd / (t_bwd * 1e-3) / 1e12 / peak}}
+               if w.backward else {}),
+        },
+        "roofline": {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_src} bf16 dense (burst) "
+                                    f"{'MEASURED_PEAKS.json' if peak_src == 'measured' else 'fallback'}",
+                     "traffic": traffic},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks.summary(local),
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def recorded_traffic(kname, w):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu summary, if one exists
+    for this kernel, workload and kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    from exact_attention_fa_gb300 import build
+    entry = rec.get(f"{w.name}:{kname.split(' ')[0]}")
+    if not entry or entry.get("source_digest") != build.source_digest():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -47,6 +47,11 @@ def _digest() -> str:
     return h.hexdigest()
 
 
+def source_digest() -> str:
+    """Digest of the kernel sources and build flags (identifies the kernels a profile was taken on)."""
+    return _digest()
+
+
 def _compile(src: str, verbose_ptxas: bool) -> str:
     obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
     cmd = [nvcc(), *NVCC_FLAGS, "-c", src, "-o", obj]
