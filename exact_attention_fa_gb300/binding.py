@@ -18,7 +18,9 @@ FA_OK = 0
 _STATUS = {
     1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA",
     5: "FA_ERR_DEVICE_TIMEOUT", 6: "FA_ERR_NO_DEVICE", 7: "FA_ERR_TOO_LARGE",
+    8: "FA_ERR_SCRATCH_LIMIT",
 }
+FA_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 # (name, restype, argtypes) of every symbol declared in include/fa.h
 _P = ctypes.c_void_p
@@ -30,6 +32,7 @@ SIGNATURES = [
     ("fa_fwd_blocksparse", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _P]),
     ("fa_bwd_workspace_bytes", ctypes.c_size_t, [_I, _I, _I, _I]),
     ("fa_bwd", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
+    ("fa_bwd_noalloc", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     ("fa_check_device_error", _I, [_P]),
     ("fa_status_string", ctypes.c_char_p, [_I]),
     ("fa_abi_version", _I, []),
@@ -141,6 +144,20 @@ def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool, workspac
     _check("fa_bwd", load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
                                    _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
                                    int(bool(causal)), _ptr(workspace), _stream(q)))
+
+
+def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool):
+    """fa_bwd for callers that cannot allocate: the library's static scratch replaces the
+    workspace (see include/fa.h for its size limit and sharing rules)."""
+    B, H, N, d = _bhnd(q, k, v, o, do, dk, dv)
+    _bhnd(dq, dtype=torch.float32)
+    if tuple(dq.shape) != tuple(q.shape):
+        raise ValueError("dq must have the shape of q")
+    _rows(lse, q.shape)
+    _check("fa_bwd_noalloc",
+           load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                                 _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                                 _stream(q)))
 
 
 def fa_check_device_error(device=None):

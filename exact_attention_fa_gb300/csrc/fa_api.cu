@@ -150,6 +150,8 @@ const char* fa_status_string(int status) {
     case FA_ERR_DEVICE_TIMEOUT: return "kernel gave up waiting on an on-chip barrier";
     case FA_ERR_NO_DEVICE: return "no current sm_103 CUDA device";
     case FA_ERR_TOO_LARGE: return "problem too large for the kernels' indexing";
+    case FA_ERR_SCRATCH_LIMIT:
+      return "problem needs more scratch than fa_bwd_noalloc's static buffer (4 MiB) holds";
     default: return "unknown status";
   }
 }

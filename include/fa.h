@@ -45,7 +45,8 @@ enum fa_status {
   FA_ERR_CUDA = 4,           /* a CUDA runtime or driver call failed (tensor map, launch)       */
   FA_ERR_DEVICE_TIMEOUT = 5, /* a kernel gave up waiting on an on-chip barrier                  */
   FA_ERR_NO_DEVICE = 6,      /* no current CUDA device, or it is not compute capability 10.3   */
-  FA_ERR_TOO_LARGE = 7       /* B*H*N or a grid dimension exceeds what the kernels index        */
+  FA_ERR_TOO_LARGE = 7,      /* B*H*N or a grid dimension exceeds what the kernels index        */
+  FA_ERR_SCRATCH_LIMIT = 8   /* fa_bwd_noalloc: the problem needs more than its static scratch  */
 };
 
 /* Forward, bf16 inputs and output, fp32 accumulation (tensor cores: tcgen05.mma, TMEM).
@@ -87,6 +88,26 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
            const float* lse, float* dq, void* dk, void* dv, int B, int H, int N, int d,
            float scale, int causal, void* workspace, fa_stream_t stream);
+
+/* Bytes of device scratch built into the library for fa_bwd_noalloc (per device). */
+#define FA_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* fa_bwd without a workspace argument, for callers that cannot allocate device memory (a plugin
+ * whose host gives it only its input and output buffers, a runtime that forbids cudaMalloc
+ * while it serves). The pages have no counterpart of this entry point.
+ * Same arguments, results and errors as fa_bwd, minus `workspace`: the scratch comes from a
+ * FA_NOALLOC_SCRATCH_BYTES array of device memory that every device holds from the moment the
+ * library's module is loaded on it until the process exits. Problems whose
+ * fa_bwd_workspace_bytes(B, H, N, d) exceeds that size are rejected with FA_ERR_SCRATCH_LIMIT
+ * before anything is enqueued (4 MiB covers B*H*ceil(N/128)*128 <= 524288 rows).
+ * Allocates nothing: no cudaMalloc/cudaFree or allocating library call. The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress, with that device current);
+ * make that first call before any stream capture. All calls on a device share the one array and
+ * it keeps the last call's contents (none needs clearing); calls whose kernels overlap on the GPU
+ * (other streams, other host threads) race on it and must be serialised by the caller. */
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                   const float* lse, float* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   float scale, int causal, fa_stream_t stream);
 
 /* Synchronises `stream`, then reads and clears the device error word of the current device.
  * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (a kernel gave up on a barrier; its outputs are invalid),
