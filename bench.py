@@ -173,6 +173,22 @@ def run_reference(args):
     }), flush=True)
 
 
+def aggregate_over_ranks(local_ms, world, device=None):
+    """Each timing's maximum over ranks: the slowest replica sets the job's time."""
+    if world == 1:
+        return list(local_ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(local_ms), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tflops(world, flops_per_rank, ms):
+    """Whole-job throughput: every replica processes flops_per_rank in the job time ms."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def metric_name(w):
     return "attention fwd/bwd TFLOPS (4·B·H·N²·d, causal halved)"
 
@@ -331,10 +347,7 @@ def run_ours(args):
     t_step = statistics.fmean(step_ms)
     t_fwd = statistics.fmean(fwd_ms)
     t_bwd = statistics.fmean(bwd_ms)
-    if world > 1:
-        tt = torch.tensor([t_step, t_fwd, t_bwd], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_step, t_fwd, t_bwd = tt.tolist()
+    t_step, t_fwd, t_bwd = aggregate_over_ranks([t_step, t_fwd, t_bwd], world, dev)
 
     # ------------------------------------------------------------------ end to end, host buffers
     e2e = None
@@ -367,11 +380,8 @@ def run_ours(args):
         torch.cuda.synchronize()
         fa.fa_check_device_error(dev)
         t_e2e = statistics.fmean(ee[i][0].elapsed_time(ee[i][1]) for i in range(E))
-        if world > 1:
-            tt = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            t_e2e = tt.item()
-        e2e = {"value": world * (f_fwd + f_bwd) / (t_e2e * 1e-3) / 1e12, "unit": "TFLOPS",
+        t_e2e = aggregate_over_ranks([t_e2e], world, dev)[0]
+        e2e = {"value": job_tflops(world, f_fwd + f_bwd, t_e2e), "unit": "TFLOPS",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e,
                "steps": E}
 
@@ -391,7 +401,7 @@ def run_ours(args):
     achieved = kflops / (kms * 1e-3) / 1e12
     peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     traffic = recorded_traffic(kname, w)
-    value = world * (f_fwd + f_bwd) / (t_step * 1e-3) / 1e12
+    value = job_tflops(world, f_fwd + f_bwd, t_step)
     line = {
         "metric": metric_name(w), "value": value, "unit": "TFLOPS", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True,
