@@ -8,7 +8,7 @@
 
 #include <mutex>
 
-#include "../../include/fa.h"
+#include "fa.h"
 #include "fa_internal.h"
 
 namespace {

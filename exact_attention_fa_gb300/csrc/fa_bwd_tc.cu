@@ -36,7 +36,6 @@ constexpr int BT = 128;  // keys per CTA tile = queries per inner tile
 constexpr int kComputeWarps = 8;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kDrainWarp0 = 10;
 constexpr int kThreads = 14 * 32;
 constexpr int kBoxBytes = 128 * 64 * 2;
 
@@ -71,6 +70,9 @@ struct BCfg {
   static constexpr int kOffAbort = kOffTmemPtr + 4;
   static constexpr int kSmemBytes = kOffAbort + 4;  // the base must be 1024-aligned (checked)
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  // d = 64 has room for dQ_i in its own columns; at d = 128 it reuses the dP^T columns.
+  static constexpr bool kDQAliasesDP = D == 128;
+  static constexpr uint32_t kColDQ = kDQAliasesDP ? kColDP : 256 + 2 * D;
 };
 
 __device__ __forceinline__ void tma_bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
@@ -150,31 +152,45 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
 
   bool ok = mbar_wait(bar(C::kBarKV), 0, ctl);
   tc_fence_after();
-  const uint32_t ka = sbase + C::kOffK, va = sbase + C::kOffV, dsa = sbase + C::kOffDS;
-  for (int i = i0, it = 0; ok && i < p.n_tiles; ++i, ++it) {
-    const int st = it % C::kStages;
-    const uint32_t sb = sbase + C::kOffStage + st * C::kStageBytes;
-    const uint32_t qa = sb + C::kStageQ, doa = sb + C::kStageDO;
-    if (!mbar_wait(bar(C::kBarFull + st), (it / C::kStages) & 1, ctl)) { ok = false; break; }
-    tc_fence_after();
-    // S^T = K Q_i^T
+  // Descriptor halves precomputed once; each MMA only adds a constant K-step offset.
+  constexpr uint32_t kHi = sdesc_hi_sw128(1024);
+  const uint32_t k_km = sdesc_lo(sbase + C::kOffK, 16);          // K as A of S^T (K-major)
+  const uint32_t v_km = sdesc_lo(sbase + C::kOffV, 16);          // V as A of dP^T (K-major)
+  const uint32_t k_mn = sdesc_lo(sbase + C::kOffK, kBoxBytes);   // K as B of dQ (MN-major)
+  const uint32_t ds_mn = sdesc_lo(sbase + C::kOffDS, kBoxBytes); // dS as A of dQ (MN-major)
+  const uint32_t st_km = sdesc_lo(sbase + C::kOffStage, 16);     // Q_i / dO_i, K-major
+  const uint32_t st_mn = sdesc_lo(sbase + C::kOffStage, kBoxBytes);  // Q_i / dO_i, MN-major
+  constexpr uint32_t kStageStep = C::kStageBytes >> 4;
+  constexpr uint32_t kDOOff = C::kStageDO >> 4;
+  const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColDQ;
+  const uint32_t tDV = tmem + C::kColDV, tDK = tmem + C::kColDK;
+  auto issue_s = [&](int it) {  // S^T = K Q_i^T
+    const uint32_t q_km = st_km + (it % C::kStages) * kStageStep;
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
-      const uint32_t off = (k / 4) * kBoxBytes + (k % 4) * 32;
-      mma_ss(tmem + C::kColS, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
-             kIdescT, k > 0);
+      const uint32_t off = ((k / 4) * kBoxBytes + (k % 4) * 32) >> 4;
+      mma_ss2(tS, k_km + off, q_km + off, kHi, kIdescT, k > 0 ? 1u : 0u);
     }
     mma_commit(bar(C::kBarS));
-    // dP^T = V dO_i^T, into columns the previous dQ_i occupied until drained
-    if (it > 0) {
+  };
+  if (ok && i0 < p.n_tiles) {
+    ok = mbar_wait(bar(C::kBarFull + 0), 0, ctl);
+    tc_fence_after();
+    if (ok) issue_s(0);
+  }
+  for (int i = i0, it = 0; ok && i < p.n_tiles; ++i, ++it) {
+    const int st = it % C::kStages;
+    const uint32_t q_mn = st_mn + st * kStageStep;
+    const uint32_t do_km = st_km + st * kStageStep + kDOOff, do_mn = q_mn + kDOOff;
+    // dP^T = V dO_i^T (when dQ shares these columns, only after the previous dQ_i was drained)
+    if (C::kDQAliasesDP && it > 0) {
       if (!mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
     }
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
-      const uint32_t off = (k / 4) * kBoxBytes + (k % 4) * 32;
-      mma_ss(tmem + C::kColDP, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(doa + off, 16, 1024),
-             kIdescT, k > 0);
+      const uint32_t off = ((k / 4) * kBoxBytes + (k % 4) * 32) >> 4;
+      mma_ss2(tDP, v_km + off, do_km + off, kHi, kIdescT, k > 0 ? 1u : 0u);
     }
     mma_commit(bar(C::kBarDP));
     // dV += P^T dO_i
@@ -182,19 +198,31 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
     tc_fence_after();
 #pragma unroll
     for (int k = 0; k < BT / 16; ++k)
-      mma_ts(tmem + C::kColDV, tmem + C::kColS + packed_col(k),
-             sdesc_sw128(doa + k * 2048, kBoxBytes, 1024), kIdescG, (it > 0 || k > 0) ? 1u : 0u);
+      mma_ts2(tDV, tS + packed_col(k), do_mn + ((k * 2048) >> 4), kHi, kIdescG,
+              (it > 0 || k > 0) ? 1u : 0u);
+    // S^T of the next query tile overwrites P^T: the tensor core runs MMAs in issue order, so
+    // the dV product above has read P^T first; the compute warps overlap it with dK, dQ below.
+    if (i + 1 < p.n_tiles) {
+      const int nx = it + 1;
+      if (!mbar_wait(bar(C::kBarFull + nx % C::kStages), (nx / C::kStages) & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+      issue_s(nx);
+    }
     // dK += dS^T Q_i ; dQ_i = dS K
     if (!mbar_wait(bar(C::kBarDS), it & 1, ctl)) { ok = false; break; }
     tc_fence_after();
 #pragma unroll
     for (int k = 0; k < BT / 16; ++k)
-      mma_ts(tmem + C::kColDK, tmem + C::kColDP + packed_col(k),
-             sdesc_sw128(qa + k * 2048, kBoxBytes, 1024), kIdescG, (it > 0 || k > 0) ? 1u : 0u);
+      mma_ts2(tDK, tDP + packed_col(k), q_mn + ((k * 2048) >> 4), kHi, kIdescG,
+              (it > 0 || k > 0) ? 1u : 0u);
+    if (!C::kDQAliasesDP && it > 0) {
+      if (!mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+    }
 #pragma unroll
     for (int k = 0; k < BT / 16; ++k)
-      mma_ss(tmem + C::kColDP, sdesc_sw128(dsa + k * 2048, kBoxBytes, 1024),
-             sdesc_sw128(ka + k * 2048, kBoxBytes, 1024), kIdescQ, k > 0);
+      mma_ss2(tDQ, ds_mn + ((k * 2048) >> 4), k_mn + ((k * 2048) >> 4), kHi, kIdescQ,
+              k > 0 ? 1u : 0u);
     mma_commit(bar(C::kBarDQFull));
     mma_commit(bar(C::kBarEmpty + st));
   }
@@ -332,7 +360,7 @@ __device__ void bwd_drain(const BwdParams& p, uint32_t sbase, uint32_t tmem, con
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int quad = warp % 4;
   const int qr = quad * 32 + lane;  // query row within the tile (TMEM lane)
-  const uint32_t tQ = tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::kColDP;
+  const uint32_t tQ = tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::kColDQ;
   for (int i = i0, it = 0; i < p.n_tiles; ++i, ++it) {
     if (!mbar_wait(bar(C::kBarDQFull), it & 1, ctl)) return;
     tc_fence_after();

@@ -35,6 +35,7 @@ constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
 constexpr int kBoxBytes = 128 * 64 * 2;  // one TMA box: 128 rows x 64 bf16 (128 B rows)
+constexpr float kRescaleSlack = 8.f;     // log2 units: P stays <= 256
 
 template <int D>
 struct Cfg {
@@ -138,22 +139,27 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
   constexpr uint32_t kIdescQK = idesc_bf16(128, BN, 0, 0);  // A = Q (K-major), B = K (K-major)
   constexpr uint32_t kIdescPV = idesc_bf16(128, D, 0, 1);   // A = P (TMEM), B = V (MN-major)
 
+  // Descriptor halves precomputed once; each MMA only adds a constant K-step offset.
+  constexpr uint32_t kHi = sdesc_hi_sw128(1024);
+  const uint32_t q_lo0 = sdesc_lo(sbase + C::kOffQ, 16);
+  const uint32_t kv_lo0 = sdesc_lo(sbase + C::kOffKV, 16);          // K tiles (K-major)
+  const uint32_t v_lo0 = sdesc_lo(sbase + C::kOffKV, kBoxBytes);    // V tiles (MN-major)
+  constexpr uint32_t kStageStep = C::kTileBytes >> 4;
   auto issue_s = [&](int t, int stage) {
-    const uint32_t qa = sbase + C::kOffQ + t * C::kTileBytes;
-    const uint32_t ka = sbase + C::kOffKV + stage * C::kTileBytes;
+    const uint32_t a = q_lo0 + t * kStageStep, b = kv_lo0 + stage * kStageStep;
+    const uint32_t d = tmem + C::col_s(t);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
-      const uint32_t off = (k / 4) * kBoxBytes + (k % 4) * 32;
-      mma_ss(tmem + C::col_s(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-             kIdescQK, k > 0);
+      const uint32_t off = ((k / 4) * kBoxBytes + (k % 4) * 32) >> 4;
+      mma_ss2(d, a + off, b + off, kHi, kIdescQK, k > 0 ? 1u : 0u);
     }
   };
   auto issue_pv = [&](int t, int stage, bool acc) {
-    const uint32_t va = sbase + C::kOffKV + stage * C::kTileBytes;
+    const uint32_t b = v_lo0 + stage * kStageStep;
+    const uint32_t d = tmem + C::col_o(t), pa = tmem + C::col_s(t);
 #pragma unroll
     for (int k = 0; k < BN / 16; ++k)
-      mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + k * 8,
-             sdesc_sw128(va + k * 2048, kBoxBytes, 1024), kIdescPV, (acc || k > 0) ? 1u : 0u);
+      mma_ts2(d, pa + k * 8, b + ((k * 2048) >> 4), kHi, kIdescPV, (acc || k > 0) ? 1u : 0u);
   };
 
   bool ok = mbar_wait(bar(C::kBarQ), 0, ctl);
@@ -251,10 +257,7 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
     tc_fence_after();
 
     uint32_t s[128];
-    tmem_ld32(tS + 0, s + 0);
-    tmem_ld32(tS + 32, s + 32);
-    tmem_ld32(tS + 64, s + 64);
-    tmem_ld32(tS + 96, s + 96);
+    tmem_ld128(tS, s);
 
     const int key0 = j * BN;
     const int lim = (p.mode == kCausal && j == qt) ? min(p.N, row + 1) : p.N;
@@ -265,45 +268,62 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
     }
     float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < 128; c += 4) {
-      mx0 = fmaxf(mx0, __uint_as_float(s[c]));
-      mx1 = fmaxf(mx1, __uint_as_float(s[c + 1]));
-      mx2 = fmaxf(mx2, __uint_as_float(s[c + 2]));
-      mx3 = fmaxf(mx3, __uint_as_float(s[c + 3]));
+    for (int c = 0; c < 128; c += 8) {
+      mx0 = max3(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+      mx1 = max3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+      mx2 = max3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
+      mx3 = max3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
     }
-    const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-    const float m_new = fmaxf(m, mx * sl2);
-    const float m_use = m_new == -INFINITY ? 0.f : m_new;
-    const float alpha = ex2(m - m_use);
+    const float mx = max3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
 
-    // Rescale this row of O only when its max moved (the exact skip: alpha would be 1).
-    if (any && __any_sync(~0u, m_new != m)) {
+    // Conditional rescaling (the FA4 idea of "3 · FlashAttention", 3.5): the reference max m
+    // only moves when this tile's max exceeds it by more than kRescaleSlack (log2 units), so
+    // P <= 2^kRescaleSlack and O, l are rescaled rarely. O = a / l is exact for any reference.
+    if (__any_sync(~0u, mx > m + kRescaleSlack)) {
+      const float m_new = fmaxf(m, mx);
+      const float alpha = ex2(m - m_new);  // 0 when nothing was accumulated (m = -inf)
+      if (any) {
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
-        uint32_t o[32];
-        tmem_ld32(tO + c, o);
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c, o);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st32(tO + c, o);
+          for (int i = 0; i < 32; i += 2) {
+            const unsigned long long v = f2_mul(
+                f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), f2_pack(alpha, alpha));
+            float lo, hi;
+            f2_unpack(v, lo, hi);
+            o[i] = __float_as_uint(lo);
+            o[i + 1] = __float_as_uint(hi);
+          }
+          tmem_st32(tO + c, o);
+        }
       }
+      l *= alpha;
+      m = m_new;
     }
-
-    float rs0 = 0.f, rs1 = 0.f;
+    const float m_use = m == -INFINITY ? 0.f : m;
+    const unsigned long long k2 = f2_pack(sl2, sl2);
+    const unsigned long long nm2 = f2_pack(-m_use, -m_use);
+    unsigned long long rs = f2_pack(0.f, 0.f);
 #pragma unroll
     for (int c = 0; c < 128; c += 32) {
       uint32_t pk[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float p0 = ex2(fmaf(__uint_as_float(s[c + 2 * i]), sl2, -m_use));
-        const float p1 = ex2(fmaf(__uint_as_float(s[c + 2 * i + 1]), sl2, -m_use));
-        rs0 += p0;
-        rs1 += p1;
+        const unsigned long long x = f2_fma(
+            f2_pack(__uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1])), k2, nm2);
+        float x0, x1;
+        f2_unpack(x, x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        rs = f2_add(rs, f2_pack(p0, p1));
         pk[i] = pack_bf16(p0, p1);
       }
       tmem_st16(tS + c / 2, pk);
     }
-    l = l * alpha + (rs0 + rs1);
-    m = m_new;
+    float rs0, rs1;
+    f2_unpack(rs, rs0, rs1);
+    l += rs0 + rs1;
     any = true;
     tmem_st_wait();
     tc_fence_before();

@@ -14,7 +14,7 @@
 
 #include <mutex>
 
-#include "../../include/fa.h"
+#include "fa.h"
 
 namespace {
 
