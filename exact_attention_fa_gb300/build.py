@@ -22,6 +22,8 @@ INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills", "-I", INCLUDE] + ARCH
+# Extra compile definitions (e.g. for tuning experiments), space separated.
+NVCC_FLAGS += os.environ.get("FA_NVCC_EXTRA", "").split()
 
 
 def nvcc() -> str:

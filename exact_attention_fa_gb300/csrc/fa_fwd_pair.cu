@@ -1,0 +1,464 @@
+// bf16 forward on the 5th-generation tensor cores (tcgen05.mma, accumulators in tensor memory).
+//
+// The method is the tiled online-softmax attention of "FlashAttention：メモリ効率的なアテンション計算"
+// (sections "オンライン softmax" and "タイル化") in the FlashAttention-2 order of
+// "출력을 누적해 메모리 이동을 줄이는 FlashAttention": per query tile, stream the key/value tiles, keep a
+// running row max m, running sum l and an unnormalised accumulator O rescaled by exp(m - m_new),
+// divide by l once at the end. Neither S nor P ever leaves the SM.
+//
+// GB300 mapping (one CTA per SM, 10 warps; used for dense / causal d = 128):
+//   * a CTA owns two 128-row query tiles (t = 0, 1) of one (b, h), so the tensor core works on one
+//     tile's QK^T / PV while the other tile's softmax runs on the CUDA cores, and each K/V tile
+//     streamed from L2 serves 256 query rows;
+//   * warp 8 (one lane) streams K_j, V_j with TMA into a ring of 128-byte-swizzled shared-memory
+//     stages guarded by full/empty mbarriers, keys one tile ahead of values; Q is loaded once;
+//   * warp 9 (one lane) issues the MMAs: S_t = Q_t K_j^T (both operands in shared memory, fp32
+//     result in TMEM) and O_t += P_t V_j (P_t read from TMEM, V_j from shared memory);
+//   * warps 0-3 / 4-7 are the softmax warpgroups of tile 0 / 1: thread r owns query row r (TMEM
+//     lane r). It loads its 128 scores, applies the scale (log2(e) folded in, exp2 on the SFU),
+//     the causal / tail mask, updates m and l, rescales its O row only when the reference max
+//     moves (conditional rescaling), writes P as bf16 into the columns of S (TMEM), and finally
+//     normalises O and writes O and lse.
+//   * causal / block-sparse: key tiles a query tile does not need are never loaded nor multiplied
+//     ("3 · FlashAttention", question on the causal mask; "拡張: Block-Sparse FlashAttention").
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256, 256+d), O_1 [256+d, 256+2d).
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int BM = 128;  // query rows per tile
+constexpr int BN = 128;  // keys per tile
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kBoxBytes = 128 * 64 * 2;  // one TMA box: 128 rows x 64 bf16 (128 B rows)
+constexpr float kRescaleSlack = 8.f;     // log2 units: P stays <= 256
+
+template <int D>
+struct Cfg {
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kStages = D == 128 ? 4 : 8;  // K/V ring (K and V tiles alternate)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = 2 * kTileBytes;
+  static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
+  // barriers: Q, full[S], empty[S], s_full[2], p_full[2], o_full[2], drain
+  static constexpr int kBarQ = 0;
+  static constexpr int kBarFull = 1;
+  static constexpr int kBarEmpty = 1 + kStages;
+  static constexpr int kBarS = 1 + 2 * kStages;
+  static constexpr int kBarP = kBarS + 2;
+  static constexpr int kBarO = kBarP + 2;
+  static constexpr int kBarDrain = kBarO + 2;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kOffTmemPtr = kOffBar + 8 * kNumBars;
+  static constexpr int kOffAbort = kOffTmemPtr + 4;
+  static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1 KB
+  __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
+  __device__ static constexpr uint32_t col_o(int t) { return t ? 256u + D : 256u; }
+};
+
+__device__ __forceinline__ bool tile_active(const FwdParams& p, int qt, int j) {
+  if (qt * BM >= p.N) return false;
+  if (p.mode == kCausal) return j <= qt;
+  if (p.mode == kBlockSparse) return __ldg(p.block_mask + static_cast<size_t>(qt) * p.n_tiles + j) != 0;
+  return true;
+}
+
+// next key tile >= j needed by either query tile, or n_tiles
+__device__ __forceinline__ int next_union(const FwdParams& p, int qt0, int qt1, int j) {
+  for (; j < p.n_tiles; ++j)
+    if (tile_active(p, qt0, j) || tile_active(p, qt1, j)) return j;
+  return p.n_tiles;
+}
+
+// CTA -> (head, query-tile pair). Heads are taken in groups small enough for their K/V to stay
+// in L2; inside a group the pairs with the most key tiles (causal: the last ones) come first.
+__device__ __forceinline__ void decode_work(const FwdParams& p, int& bh, int& pair) {
+  const int n_pairs = (p.n_tiles + 1) / 2;
+  const int per_group = p.heads_per_group * n_pairs;
+  const int g = blockIdx.x / per_group;
+  const int within = blockIdx.x - g * per_group;
+  const int gsize = min(p.heads_per_group, p.BH - g * p.heads_per_group);
+  pair = n_pairs - 1 - within / gsize;
+  bh = g * p.heads_per_group + within % gsize;
+}
+
+// ---------------------------------------------------------------------------------------------
+template <int D>
+__device__ void producer(const FwdParams& p, uint32_t sbase, const Ctl& ctl, int bh, int qt0,
+                         int qt1) {
+  using C = Cfg<D>;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
+  tma_prefetch_desc(&p.tm_q);
+  tma_prefetch_desc(&p.tm_k);
+  tma_prefetch_desc(&p.tm_v);
+
+  mbar_arrive_expect_tx(bar(C::kBarQ), 2 * C::kTileBytes);
+  for (int t = 0; t < 2; ++t)
+    for (int b = 0; b < D / 64; ++b)
+      tma_load_3d(sbase + C::kOffQ + t * C::kTileBytes + b * kBoxBytes, &p.tm_q, bar(C::kBarQ),
+                  b * 64, (t ? qt1 : qt0) * BM, bh);
+
+  int issued[C::kStages];
+#pragma unroll
+  for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
+  // Ring order: K of the first tile, then per tile K of the next tile ahead of V of this one,
+  // so that keys (needed first, by S) run one tile ahead of values (needed last, by PV).
+  int pos = 0;
+  bool ok = true;
+  auto load = [&](const void* map, int j) {
+    const int s = pos % C::kStages;
+    const int round = pos / C::kStages;
+    if (!mbar_wait(bar(C::kBarEmpty + s), (round & 1) ^ 1, ctl)) return false;
+    mbar_arrive_expect_tx(bar(C::kBarFull + s), C::kTileBytes);
+    for (int b = 0; b < D / 64; ++b)
+      tma_load_3d(sbase + C::kOffKV + s * C::kTileBytes + b * kBoxBytes, map, bar(C::kBarFull + s),
+                  b * 64, j * BN, bh);
+    issued[s] = round;
+    ++pos;
+    return true;
+  };
+  int j = next_union(p, qt0, qt1, 0);
+  if (j < p.n_tiles) ok = load(&p.tm_k, j);
+  while (ok && j < p.n_tiles) {
+    const int jn = next_union(p, qt0, qt1, j + 1);
+    if (jn < p.n_tiles && !(ok = load(&p.tm_k, jn))) break;
+    if (!(ok = load(&p.tm_v, j))) break;
+    j = jn;
+  }
+  if (!ok) {
+    // Give the copies already in flight a bounded time to land before the CTA exits.
+    Ctl drain = ctl;
+    int zero = 0;
+    drain.abort_flag = &zero;
+    mbar_wait(bar(C::kBarQ), 0, drain);
+    for (int s = 0; s < C::kStages; ++s)
+      if (issued[s] >= 0) mbar_wait(bar(C::kBarFull + s), issued[s] & 1, drain);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+template <int D>
+__device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, const Ctl& ctl,
+                           int qt0, int qt1) {
+  using C = Cfg<D>;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
+  constexpr uint32_t kIdescQK = idesc_bf16(128, BN, 0, 0);  // A = Q (K-major), B = K (K-major)
+  constexpr uint32_t kIdescPV = idesc_bf16(128, D, 0, 1);   // A = P (TMEM), B = V (MN-major)
+
+  // Descriptors precomputed once (Q of both tiles per K-step, first K and V stage); a stage
+  // is a constant offset away, so each MMA costs the issuing thread one add.
+  constexpr uint32_t kHi = sdesc_hi_sw128(1024);
+  constexpr uint64_t kStageStep = C::kTileBytes >> 4;
+  uint64_t qd[2][D / 16];
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k)
+      qd[t][k] = sdesc64(
+          sdesc_lo(sbase + C::kOffQ + t * C::kTileBytes + (k / 4) * kBoxBytes + (k % 4) * 32, 16), kHi);
+  const uint64_t kd0 = sdesc64(sdesc_lo(sbase + C::kOffKV, 16), kHi);
+  const uint64_t vd0 = sdesc64(sdesc_lo(sbase + C::kOffKV, kBoxBytes), kHi);
+  auto issue_s = [&](int t, int stage) {
+    if constexpr (D == 128)
+      mma_qk_d128(tmem + C::col_s(t), qd[t], kd0 + stage * kStageStep, kIdescQK);
+    else
+      mma_qk_d64(tmem + C::col_s(t), qd[t], kd0 + stage * kStageStep, kIdescQK);
+  };
+  auto issue_pv = [&](int t, int stage, bool acc) {
+    mma_pv_k128(tmem + C::col_o(t), tmem + C::col_s(t), vd0 + stage * kStageStep, kIdescPV,
+                acc ? 1u : 0u);
+  };
+
+  bool ok = mbar_wait(bar(C::kBarQ), 0, ctl);
+  tc_fence_after();
+  uint32_t pphase[2] = {0, 0};
+  bool acc[2] = {false, false};
+  // Ring positions in the producer's order: K(u0), then per union tile u_i: K(u_{i+1}), V(u_i).
+  auto wait_full = [&](int ps) {
+    return mbar_wait(bar(C::kBarFull + ps % C::kStages), (ps / C::kStages) & 1, ctl);
+  };
+  int j = next_union(p, qt0, qt1, 0);
+  int i = 0;  // index of j among the union tiles
+  if (ok && j < p.n_tiles) {
+    ok = wait_full(0);
+    tc_fence_after();
+    if (ok) {
+      if (tile_active(p, qt0, j)) { issue_s(0, 0); mma_commit(bar(C::kBarS + 0)); }
+      if (tile_active(p, qt1, j)) { issue_s(1, 0); mma_commit(bar(C::kBarS + 1)); }
+      mma_commit(bar(C::kBarEmpty + 0));
+    }
+  }
+  while (ok && j < p.n_tiles) {
+    const bool a0 = tile_active(p, qt0, j), a1 = tile_active(p, qt1, j);
+    const int jn = next_union(p, qt0, qt1, j + 1);
+    const bool has_next = jn < p.n_tiles;
+    const int kpos = 2 * i + 1;                      // K(u_{i+1})
+    const int vpos = has_next ? 2 * i + 2 : 2 * i + 1;  // V(u_i)
+    const int sv = vpos % C::kStages, skn = kpos % C::kStages;
+    if (!wait_full(vpos)) { ok = false; break; }
+    tc_fence_after();
+    const bool n0 = has_next && tile_active(p, qt0, jn);
+    const bool n1 = has_next && tile_active(p, qt1, jn);
+
+    if (a0) {
+      if (!mbar_wait(bar(C::kBarP + 0), pphase[0], ctl)) { ok = false; break; }
+      pphase[0] ^= 1;
+      tc_fence_after();
+      issue_pv(0, sv, acc[0]);
+      acc[0] = true;
+    }
+    if (has_next) {
+      if (!wait_full(kpos)) { ok = false; break; }
+      tc_fence_after();
+    }
+    // S_0 of the next tile overwrites P_0 of this one: the tensor core runs MMAs in issue order,
+    // so the PV above has read P_0 before this write lands.
+    if (n0) { issue_s(0, skn); mma_commit(bar(C::kBarS + 0)); }
+    if (a1) {
+      if (!mbar_wait(bar(C::kBarP + 1), pphase[1], ctl)) { ok = false; break; }
+      pphase[1] ^= 1;
+      tc_fence_after();
+      issue_pv(1, sv, acc[1]);
+      acc[1] = true;
+    }
+    if (n1) { issue_s(1, skn); mma_commit(bar(C::kBarS + 1)); }
+    if (has_next) mma_commit(bar(C::kBarEmpty + skn));
+    mma_commit(bar(C::kBarEmpty + sv));
+    ++i;
+    j = jn;
+  }
+  if (ok) {
+    mma_commit(bar(C::kBarO + 0));
+    mma_commit(bar(C::kBarO + 1));
+  } else {
+    // Let the MMAs already issued finish before TMEM is released.
+    Ctl drain = ctl;
+    int zero = 0;
+    drain.abort_flag = &zero;
+    mma_commit(bar(C::kBarDrain));
+    mbar_wait(bar(C::kBarDrain), 0, drain);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+template <int D>
+__device__ void softmax_wg(const FwdParams& p, uint32_t sbase, uint32_t tmem, const Ctl& ctl,
+                           int bh, int qt0, int qt1) {
+  using C = Cfg<D>;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int t = warp / 4;
+  const int quad = warp % 4;
+  const int r = quad * 32 + lane;
+  const int qt = t ? qt1 : qt0;
+  const int row = qt * BM + r;
+  const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+  const uint32_t tS = tmem + lane_off + C::col_s(t);
+  const uint32_t tO = tmem + lane_off + C::col_o(t);
+  const float sl2 = p.scale_log2;
+
+  float m = -INFINITY, l = 0.f;
+  bool any = false;
+  uint32_t sphase = 0;
+  bool ok = true;
+  for (int j = 0; j < p.n_tiles; ++j) {
+    if (!tile_active(p, qt, j)) continue;
+    if (!mbar_wait(bar(C::kBarS + t), sphase, ctl)) { ok = false; break; }
+    sphase ^= 1;
+    tc_fence_after();
+
+    uint32_t s[128];
+    tmem_ld128(tS, s);
+
+    const int key0 = j * BN;
+    const int lim = (p.mode == kCausal && j == qt) ? min(p.N, row + 1) : p.N;
+    if (key0 + BN > lim) {
+#pragma unroll
+      for (int c = 0; c < 128; ++c)
+        if (key0 + c >= lim) s[c] = __float_as_uint(-INFINITY);
+    }
+    float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 128; c += 8) {
+      mx0 = max3(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+      mx1 = max3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+      mx2 = max3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
+      mx3 = max3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
+    }
+    const float mx = max3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
+
+    // Conditional rescaling (the FA4 idea of "3 · FlashAttention", 3.5): the reference max m
+    // only moves when this tile's max exceeds it by more than kRescaleSlack (log2 units), so
+    // P <= 2^kRescaleSlack and O, l are rescaled rarely. O = a / l is exact for any reference.
+    if (__any_sync(~0u, mx > m + kRescaleSlack)) {
+      const float m_new = fmaxf(m, mx);
+      const float alpha = ex2(m - m_new);  // 0 when nothing was accumulated (m = -inf)
+      if (any) {
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c, o);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const unsigned long long v = f2_mul(
+                f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), f2_pack(alpha, alpha));
+            float lo, hi;
+            f2_unpack(v, lo, hi);
+            o[i] = __float_as_uint(lo);
+            o[i + 1] = __float_as_uint(hi);
+          }
+          tmem_st32(tO + c, o);
+        }
+      }
+      l *= alpha;
+      m = m_new;
+    }
+    const float m_use = m == -INFINITY ? 0.f : m;
+    const unsigned long long k2 = f2_pack(sl2, sl2);
+    const unsigned long long nm2 = f2_pack(-m_use, -m_use);
+    unsigned long long rs = f2_pack(0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < 128; c += 32) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const unsigned long long x = f2_fma(
+            f2_pack(__uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1])), k2, nm2);
+        float x0, x1;
+        f2_unpack(x, x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        rs = f2_add(rs, f2_pack(p0, p1));
+        pk[i] = pack_bf16(p0, p1);
+      }
+      tmem_st16(tS + c / 2, pk);
+    }
+    float rs0, rs1;
+    f2_unpack(rs, rs0, rs1);
+    l += rs0 + rs1;
+    any = true;
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(bar(C::kBarP + t));
+  }
+
+  if (!ok) return;
+  const size_t grow = static_cast<size_t>(bh) * p.N + row;
+  if (any) {
+    if (!mbar_wait(bar(C::kBarO + t), 0, ctl)) return;
+    tc_fence_after();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+    for (int c = 0; c < D; c += 32) {
+      uint32_t o[32];
+      tmem_ld32(tO + c, o);
+      if (row < p.N) {
+        uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D + c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 w;
+          w.x = pack_bf16(__uint_as_float(o[8 * i + 0]) * inv, __uint_as_float(o[8 * i + 1]) * inv);
+          w.y = pack_bf16(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv);
+          w.z = pack_bf16(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv);
+          w.w = pack_bf16(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv);
+          dst[i] = w;
+        }
+      }
+    }
+    if (row < p.N)
+      p.lse[grow] = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+  } else if (row < p.N) {
+    uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D);
+    for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+    p.lse[grow] = -INFINITY;
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) fwd_pair_kernel(const __grid_constant__ FwdParams p) {
+  using C = Cfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemPtr);
+  const Ctl ctl{abort_flag, p.err, p.timeout_ns};
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  int bh, pair;
+  decode_work(p, bh, pair);
+  const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(C::kBarQ), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kBarFull + s), 1);
+      mbar_init(bar(C::kBarEmpty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::kBarS + t), 1);
+      mbar_init(bar(C::kBarP + t), 128);
+      mbar_init(bar(C::kBarO + t), 1);
+    }
+    mbar_init(bar(C::kBarDrain), 1);
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kLoadWarp) {
+    if (lane == 0) producer<D>(p, sbase, ctl, bh, qt0, qt1);
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) mma_issuer<D>(p, sbase, tmem, ctl, qt0, qt1);
+    __syncwarp();
+  } else {
+    softmax_wg<D>(p, sbase, tmem, ctl, bh, qt0, qt1);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch(const FwdParams& p, cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        fwd_pair_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const unsigned grid = static_cast<unsigned>((p.n_tiles + 1) / 2) * static_cast<unsigned>(p.BH);
+  fwd_pair_kernel<D><<<grid, kThreads, Cfg<D>::kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_pair(const FwdParams& p, int d, cudaStream_t s) {
+  if (d == 64) return launch<64>(p, s);
+  if (d == 128) return launch<128>(p, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -6,20 +6,22 @@
 // running row max m, running sum l and an unnormalised accumulator O rescaled by exp(m - m_new),
 // divide by l once at the end. Neither S nor P ever leaves the SM.
 //
-// GB300 mapping (one CTA per SM, 10 warps):
-//   * a CTA owns two 128-row query tiles (t = 0, 1) of one (b, h), so the tensor core works on one
-//     tile's QK^T / PV while the other tile's softmax runs on the CUDA cores;
-//   * warp 8 (one lane) streams K_j, V_j with TMA into a ring of 128-byte-swizzled shared-memory
-//     stages guarded by full/empty mbarriers; Q is loaded once;
-//   * warp 9 (one lane) issues the MMAs: S_t = Q_t K_j^T (both operands in shared memory, fp32
-//     result in TMEM) and O_t += P_t V_j (P_t read from TMEM, V_j from shared memory);
-//   * warps 0-3 / 4-7 are the softmax warpgroups of tile 0 / 1: thread r owns query row r (TMEM
-//     lane r). It loads its 128 scores, applies the scale (log2(e) folded in, exp2 on the SFU),
-//     the causal / tail mask, updates m and l, rescales its O row only if m changed, writes P as
-//     bf16 into the columns of S (TMEM), and finally normalises O and writes O and lse.
+// GB300 mapping (one CTA per SM, 6 warps, one 128-row query tile of one (b, h) per CTA):
+//   * warp 5 (one lane) streams K_j, V_j with TMA into a ring of 128-byte-swizzled shared-memory
+//     stages guarded by full/empty mbarriers, keys two tiles ahead of values; Q is loaded once;
+//   * warp 4 (one lane) issues every tcgen05.mma. Issue blocks while the tensor pipe is busy, so
+//     this warp does nothing else. S = Q K_j^T goes to one of two S buffers in TMEM, so the scores
+//     of tile j + 1 are computed while the softmax works on tile j; O += P_j V_j reads P_j from
+//     the S buffer it was written into (P aliased over S), after which that buffer takes
+//     S_{j+2};
+//   * warps 0-3 are the softmax warpgroup: thread r owns query row r (TMEM lane r). Per key tile
+//     it loads its 128 scores, applies the scale (log2(e) folded in, exp2 on the SFU) and the
+//     causal / tail mask, updates m and l, rescales its O row only when the reference max moves
+//     (conditional rescaling), and writes P as bf16 over the S columns. At the end it writes
+//     O / l and lse.
 //   * causal / block-sparse: key tiles a query tile does not need are never loaded nor multiplied
 //     ("3 · FlashAttention", question on the causal mask; "拡張: Block-Sparse FlashAttention").
-// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256, 256+d), O_1 [256+d, 256+2d).
+// TMEM columns: O [0, d), S buffers [128, 256) and [256, 384).
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -31,93 +33,103 @@ namespace {
 
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per tile
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kMmaWarp = 4;
+constexpr int kLoadWarp = 5;
+constexpr int kThreads = 192;
 constexpr int kBoxBytes = 128 * 64 * 2;  // one TMA box: 128 rows x 64 bf16 (128 B rows)
 constexpr float kRescaleSlack = 8.f;     // log2 units: P stays <= 256
 
 template <int D>
 struct Cfg {
   static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kStages = D == 128 ? 4 : 8;  // K/V ring (K and V tiles alternate)
+  static constexpr int kStages = D == 128 ? 6 : 12;  // K/V ring
   static constexpr int kOffQ = 0;
-  static constexpr int kOffKV = 2 * kTileBytes;
+  static constexpr int kOffKV = kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-  // barriers: Q, full[S], empty[S], s_full[2], p_full[2], o_full[2], drain
+  // barriers: Q, full[S], empty[S], s_full[2], p_full[2], pv_done, o_full, drain
   static constexpr int kBarQ = 0;
   static constexpr int kBarFull = 1;
   static constexpr int kBarEmpty = 1 + kStages;
   static constexpr int kBarS = 1 + 2 * kStages;
   static constexpr int kBarP = kBarS + 2;
-  static constexpr int kBarO = kBarP + 2;
-  static constexpr int kBarDrain = kBarO + 2;
+  static constexpr int kBarPV = kBarP + 2;
+  static constexpr int kBarO = kBarPV + 1;
+  static constexpr int kBarDrain = kBarO + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffTmemPtr = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemPtr + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1 KB
-  __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
-  __device__ static constexpr uint32_t col_o(int t) { return t ? 256u + D : 256u; }
+  static constexpr uint32_t kColO = 0;
+  __device__ static constexpr uint32_t col_s(int b) { return 128u + 128u * b; }
 };
 
 __device__ __forceinline__ bool tile_active(const FwdParams& p, int qt, int j) {
-  if (qt * BM >= p.N) return false;
   if (p.mode == kCausal) return j <= qt;
   if (p.mode == kBlockSparse) return __ldg(p.block_mask + static_cast<size_t>(qt) * p.n_tiles + j) != 0;
   return true;
 }
 
-// next key tile >= j needed by either query tile, or n_tiles
-__device__ __forceinline__ int next_union(const FwdParams& p, int qt0, int qt1, int j) {
+// next key tile >= j this query tile needs, or n_tiles
+__device__ __forceinline__ int next_tile(const FwdParams& p, int qt, int j) {
   for (; j < p.n_tiles; ++j)
-    if (tile_active(p, qt0, j) || tile_active(p, qt1, j)) return j;
+    if (tile_active(p, qt, j)) return j;
   return p.n_tiles;
 }
 
-// CTA -> (head, query-tile pair). Heads are taken in groups small enough for their K/V to stay
-// in L2; inside a group the pairs with the most key tiles (causal: the last ones) come first.
-__device__ __forceinline__ void decode_work(const FwdParams& p, int& bh, int& pair) {
-  const int per_group = p.heads_per_group * p.n_pairs;
+// CTA -> (head, query tile). Heads are taken in groups small enough for their K/V to stay in
+// L2; inside a group the query tiles with the most key tiles (causal: the last ones) come first.
+__device__ __forceinline__ void decode_work(const FwdParams& p, int& bh, int& qt) {
+  const int per_group = p.heads_per_group * p.n_tiles;
   const int g = blockIdx.x / per_group;
   const int within = blockIdx.x - g * per_group;
   const int gsize = min(p.heads_per_group, p.BH - g * p.heads_per_group);
-  pair = p.n_pairs - 1 - within / gsize;
+  qt = p.n_tiles - 1 - within / gsize;
   bh = g * p.heads_per_group + within % gsize;
 }
 
+// Ring order shared by the producer and the MMA warp: K(u0), K(u1), then for each needed tile
+// u_i: K(u_{i+2}) (if it exists), V(u_i).
+
 // ---------------------------------------------------------------------------------------------
 template <int D>
-__device__ void producer(const FwdParams& p, uint32_t sbase, const Ctl& ctl, int bh, int qt0,
-                         int qt1) {
+__device__ void producer(const FwdParams& p, uint32_t sbase, const Ctl& ctl, int bh, int qt) {
   using C = Cfg<D>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
   tma_prefetch_desc(&p.tm_q);
   tma_prefetch_desc(&p.tm_k);
   tma_prefetch_desc(&p.tm_v);
 
-  mbar_arrive_expect_tx(bar(C::kBarQ), 2 * C::kTileBytes);
-  for (int t = 0; t < 2; ++t)
-    for (int b = 0; b < D / 64; ++b)
-      tma_load_3d(sbase + C::kOffQ + t * C::kTileBytes + b * kBoxBytes, &p.tm_q, bar(C::kBarQ),
-                  b * 64, (t ? qt1 : qt0) * BM, bh);
+  mbar_arrive_expect_tx(bar(C::kBarQ), C::kTileBytes);
+  for (int b = 0; b < D / 64; ++b)
+    tma_load_3d(sbase + C::kOffQ + b * kBoxBytes, &p.tm_q, bar(C::kBarQ), b * 64, qt * BM, bh);
 
   int issued[C::kStages];
 #pragma unroll
   for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
-  int it = 0;
+  int pos = 0;
   bool ok = true;
-  for (int j = next_union(p, qt0, qt1, 0); ok && j < p.n_tiles; j = next_union(p, qt0, qt1, j + 1)) {
-    for (int kv = 0; kv < 2; ++kv, ++it) {
-      const int s = it % C::kStages;
-      const int round = it / C::kStages;
-      if (!mbar_wait(bar(C::kBarEmpty + s), (round & 1) ^ 1, ctl)) { ok = false; break; }
-      mbar_arrive_expect_tx(bar(C::kBarFull + s), C::kTileBytes);
-      const void* map = kv ? static_cast<const void*>(&p.tm_v) : static_cast<const void*>(&p.tm_k);
-      for (int b = 0; b < D / 64; ++b)
-        tma_load_3d(sbase + C::kOffKV + s * C::kTileBytes + b * kBoxBytes, map,
-                    bar(C::kBarFull + s), b * 64, j * BN, bh);
-      issued[s] = round;
-    }
+  auto load = [&](const void* map, int j) {
+    const int s = pos % C::kStages;
+    const int round = pos / C::kStages;
+    if (!mbar_wait(bar(C::kBarEmpty + s), (round & 1) ^ 1, ctl)) return false;
+    mbar_arrive_expect_tx(bar(C::kBarFull + s), C::kTileBytes);
+    for (int b = 0; b < D / 64; ++b)
+      tma_load_3d(sbase + C::kOffKV + s * C::kTileBytes + b * kBoxBytes, map, bar(C::kBarFull + s),
+                  b * 64, j * BN, bh);
+    issued[s] = round;
+    ++pos;
+    return true;
+  };
+  int j = next_tile(p, qt, 0);
+  int j1 = j < p.n_tiles ? next_tile(p, qt, j + 1) : p.n_tiles;
+  if (j < p.n_tiles) ok = load(&p.tm_k, j);
+  if (ok && j1 < p.n_tiles) ok = load(&p.tm_k, j1);
+  while (ok && j < p.n_tiles) {
+    const int j2 = j1 < p.n_tiles ? next_tile(p, qt, j1 + 1) : p.n_tiles;
+    if (j2 < p.n_tiles && !(ok = load(&p.tm_k, j2))) break;
+    if (!(ok = load(&p.tm_v, j))) break;
+    j = j1;
+    j1 = j2;
   }
   if (!ok) {
     // Give the copies already in flight a bounded time to land before the CTA exits.
@@ -133,92 +145,73 @@ __device__ void producer(const FwdParams& p, uint32_t sbase, const Ctl& ctl, int
 // ---------------------------------------------------------------------------------------------
 template <int D>
 __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, const Ctl& ctl,
-                           int qt0, int qt1) {
+                           int qt) {
   using C = Cfg<D>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
   constexpr uint32_t kIdescQK = idesc_bf16(128, BN, 0, 0);  // A = Q (K-major), B = K (K-major)
   constexpr uint32_t kIdescPV = idesc_bf16(128, D, 0, 1);   // A = P (TMEM), B = V (MN-major)
-
-  // Descriptor halves precomputed once; each MMA only adds a constant K-step offset.
   constexpr uint32_t kHi = sdesc_hi_sw128(1024);
-  const uint32_t q_lo0 = sdesc_lo(sbase + C::kOffQ, 16);
-  const uint32_t kv_lo0 = sdesc_lo(sbase + C::kOffKV, 16);          // K tiles (K-major)
-  const uint32_t v_lo0 = sdesc_lo(sbase + C::kOffKV, kBoxBytes);    // V tiles (MN-major)
-  constexpr uint32_t kStageStep = C::kTileBytes >> 4;
-  auto issue_s = [&](int t, int stage) {
-    const uint32_t a = q_lo0 + t * kStageStep, b = kv_lo0 + stage * kStageStep;
-    const uint32_t d = tmem + C::col_s(t);
+  constexpr uint64_t kStageStep = C::kTileBytes >> 4;
+  // Descriptors precomputed once: Q for each K-step, the first stage of K (K-major) and V
+  // (MN-major); a stage is a constant offset away.
+  uint64_t qd[D / 16];
 #pragma unroll
-    for (int k = 0; k < D / 16; ++k) {
-      const uint32_t off = ((k / 4) * kBoxBytes + (k % 4) * 32) >> 4;
-      mma_ss2(d, a + off, b + off, kHi, kIdescQK, k > 0 ? 1u : 0u);
-    }
+  for (int k = 0; k < D / 16; ++k)
+    qd[k] = sdesc64(sdesc_lo(sbase + C::kOffQ + (k / 4) * kBoxBytes + (k % 4) * 32, 16), kHi);
+  const uint64_t kd0 = sdesc64(sdesc_lo(sbase + C::kOffKV, 16), kHi);
+  const uint64_t vd0 = sdesc64(sdesc_lo(sbase + C::kOffKV, kBoxBytes), kHi);
+  auto issue_s = [&](int stage, int buf) {
+    if constexpr (D == 128)
+      mma_qk_d128(tmem + C::col_s(buf), qd, kd0 + stage * kStageStep, kIdescQK);
+    else
+      mma_qk_d64(tmem + C::col_s(buf), qd, kd0 + stage * kStageStep, kIdescQK);
+    mma_commit(bar(C::kBarS + buf));
   };
-  auto issue_pv = [&](int t, int stage, bool acc) {
-    const uint32_t b = v_lo0 + stage * kStageStep;
-    const uint32_t d = tmem + C::col_o(t), pa = tmem + C::col_s(t);
-#pragma unroll
-    for (int k = 0; k < BN / 16; ++k)
-      mma_ts2(d, pa + k * 8, b + ((k * 2048) >> 4), kHi, kIdescPV, (acc || k > 0) ? 1u : 0u);
+  auto wait_full = [&](int ps) {
+    return mbar_wait(bar(C::kBarFull + ps % C::kStages), (ps / C::kStages) & 1, ctl);
   };
+  auto release = [&](int ps) { mma_commit(bar(C::kBarEmpty + ps % C::kStages)); };
 
   bool ok = mbar_wait(bar(C::kBarQ), 0, ctl);
-  tc_fence_after();
-  uint32_t pphase[2] = {0, 0};
-  bool acc[2] = {false, false};
-  int it = 0;  // ring position of the current tile's K (V is at it + 1)
-  int j = next_union(p, qt0, qt1, 0);
-  if (ok && j < p.n_tiles) {
-    ok = mbar_wait(bar(C::kBarFull + 0), 0, ctl);
+  int j = next_tile(p, qt, 0);
+  int j1 = j < p.n_tiles ? next_tile(p, qt, j + 1) : p.n_tiles;
+  int pos = 0;
+  for (int b = 0; b < 2 && ok; ++b) {  // S of the first two tiles
+    if ((b ? j1 : j) >= p.n_tiles) break;
+    if (!(ok = wait_full(pos))) break;
     tc_fence_after();
-    if (ok) {
-      if (tile_active(p, qt0, j)) { issue_s(0, 0); mma_commit(bar(C::kBarS + 0)); }
-      if (tile_active(p, qt1, j)) { issue_s(1, 0); mma_commit(bar(C::kBarS + 1)); }
-      mma_commit(bar(C::kBarEmpty + 0));
-    }
+    issue_s(pos % C::kStages, b);
+    release(pos);
+    ++pos;
   }
-  while (ok && j < p.n_tiles) {
-    const bool a0 = tile_active(p, qt0, j), a1 = tile_active(p, qt1, j);
-    const int sv = (it + 1) % C::kStages;
-    if (!mbar_wait(bar(C::kBarFull + sv), ((it + 1) / C::kStages) & 1, ctl)) { ok = false; break; }
+  uint32_t pph[2] = {0, 0};
+  for (int i = 0; ok && j < p.n_tiles; ++i) {
+    const int buf = i & 1;
+    const int j2 = j1 < p.n_tiles ? next_tile(p, qt, j1 + 1) : p.n_tiles;
+    const int kpos = j2 < p.n_tiles ? pos++ : -1;  // K(u_{i+2})
+    const int vpos = pos++;                         // V(u_i)
+    // O += P_i V_i once the softmax has written P_i over S buffer `buf`
+    if (!mbar_wait(bar(C::kBarP + buf), pph[buf], ctl)) { ok = false; break; }
+    pph[buf] ^= 1;
+    if (!wait_full(vpos)) { ok = false; break; }
     tc_fence_after();
-    const int jn = next_union(p, qt0, qt1, j + 1);
-    const bool has_next = jn < p.n_tiles;
-    const bool n0 = has_next && tile_active(p, qt0, jn);
-    const bool n1 = has_next && tile_active(p, qt1, jn);
-    const int itn = it + 2;
-    const int skn = itn % C::kStages;
-
-    if (a0) {
-      if (!mbar_wait(bar(C::kBarP + 0), pphase[0], ctl)) { ok = false; break; }
-      pphase[0] ^= 1;
+    mma_pv_k128(tmem + C::kColO, tmem + C::col_s(buf), vd0 + (vpos % C::kStages) * kStageStep,
+                kIdescPV, i > 0 ? 1u : 0u);
+    mma_commit(bar(C::kBarPV));
+    release(vpos);
+    // S of the tile after next into the same buffer: the PV above reads P from it first (one
+    // thread's MMAs run in issue order).
+    if (kpos >= 0) {
+      if (!wait_full(kpos)) { ok = false; break; }
       tc_fence_after();
-      issue_pv(0, sv, acc[0]);
-      acc[0] = true;
+      issue_s(kpos % C::kStages, buf);
+      release(kpos);
     }
-    if (has_next) {
-      if (!mbar_wait(bar(C::kBarFull + skn), (itn / C::kStages) & 1, ctl)) { ok = false; break; }
-      tc_fence_after();
-    }
-    // S_0 of the next tile overwrites P_0 of this one: the tensor core runs MMAs in issue order,
-    // so the PV above has read P_0 before this write lands.
-    if (n0) { issue_s(0, skn); mma_commit(bar(C::kBarS + 0)); }
-    if (a1) {
-      if (!mbar_wait(bar(C::kBarP + 1), pphase[1], ctl)) { ok = false; break; }
-      pphase[1] ^= 1;
-      tc_fence_after();
-      issue_pv(1, sv, acc[1]);
-      acc[1] = true;
-    }
-    if (n1) { issue_s(1, skn); mma_commit(bar(C::kBarS + 1)); }
-    if (has_next) mma_commit(bar(C::kBarEmpty + skn));
-    mma_commit(bar(C::kBarEmpty + sv));
-    it = itn;
-    j = jn;
+    j = j1;
+    j1 = j2;
   }
   if (ok) {
-    mma_commit(bar(C::kBarO + 0));
-    mma_commit(bar(C::kBarO + 1));
+    mma_commit(bar(C::kBarO));
   } else {
     // Let the MMAs already issued finish before TMEM is released.
     Ctl drain = ctl;
@@ -232,30 +225,26 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
 // ---------------------------------------------------------------------------------------------
 template <int D>
 __device__ void softmax_wg(const FwdParams& p, uint32_t sbase, uint32_t tmem, const Ctl& ctl,
-                           int bh, int qt0, int qt1) {
+                           int bh, int qt) {
   using C = Cfg<D>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int t = warp / 4;
-  const int quad = warp % 4;
-  const int r = quad * 32 + lane;
-  const int qt = t ? qt1 : qt0;
+  const int r = warp * 32 + lane;
   const int row = qt * BM + r;
-  const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-  const uint32_t tS = tmem + lane_off + C::col_s(t);
-  const uint32_t tO = tmem + lane_off + C::col_o(t);
+  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t tO = tmem + lane_off + C::kColO;
   const float sl2 = p.scale_log2;
 
   float m = -INFINITY, l = 0.f;
-  bool any = false;
-  uint32_t sphase = 0;
+  int i = 0;  // tiles processed
+  uint32_t sph[2] = {0, 0};
   bool ok = true;
-  for (int j = 0; j < p.n_tiles; ++j) {
-    if (!tile_active(p, qt, j)) continue;
-    if (!mbar_wait(bar(C::kBarS + t), sphase, ctl)) { ok = false; break; }
-    sphase ^= 1;
+  for (int j = next_tile(p, qt, 0); j < p.n_tiles; j = next_tile(p, qt, j + 1), ++i) {
+    const int buf = i & 1;
+    const uint32_t tS = tmem + lane_off + C::col_s(buf);
+    if (!mbar_wait(bar(C::kBarS + buf), sph[buf], ctl)) { ok = false; break; }
+    sph[buf] ^= 1;
     tc_fence_after();
-
     uint32_t s[128];
     tmem_ld128(tS, s);
 
@@ -282,19 +271,24 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
     if (__any_sync(~0u, mx > m + kRescaleSlack)) {
       const float m_new = fmaxf(m, mx);
       const float alpha = ex2(m - m_new);  // 0 when nothing was accumulated (m = -inf)
-      if (any) {
+      if (i > 0) {
+        // O must hold all i PV products. S of this tile was issued after PV_{i-2}, so at least
+        // i - 1 have completed and the parity of completion i is unambiguous.
+        bool good = mbar_wait(bar(C::kBarPV), (i - 1) & 1, ctl);
+        if (__any_sync(~0u, !good)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
           uint32_t o[32];
           tmem_ld32(tO + c, o);
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
+          for (int e = 0; e < 32; e += 2) {
             const unsigned long long v = f2_mul(
-                f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), f2_pack(alpha, alpha));
+                f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), f2_pack(alpha, alpha));
             float lo, hi;
             f2_unpack(v, lo, hi);
-            o[i] = __float_as_uint(lo);
-            o[i + 1] = __float_as_uint(hi);
+            o[e] = __float_as_uint(lo);
+            o[e + 1] = __float_as_uint(hi);
           }
           tmem_st32(tO + c, o);
         }
@@ -310,30 +304,29 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
     for (int c = 0; c < 128; c += 32) {
       uint32_t pk[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int e = 0; e < 16; ++e) {
         const unsigned long long x = f2_fma(
-            f2_pack(__uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1])), k2, nm2);
+            f2_pack(__uint_as_float(s[c + 2 * e]), __uint_as_float(s[c + 2 * e + 1])), k2, nm2);
         float x0, x1;
         f2_unpack(x, x0, x1);
         const float p0 = ex2(x0), p1 = ex2(x1);
         rs = f2_add(rs, f2_pack(p0, p1));
-        pk[i] = pack_bf16(p0, p1);
+        pk[e] = pack_bf16(p0, p1);
       }
       tmem_st16(tS + c / 2, pk);
     }
     float rs0, rs1;
     f2_unpack(rs, rs0, rs1);
     l += rs0 + rs1;
-    any = true;
     tmem_st_wait();
     tc_fence_before();
-    mbar_arrive(bar(C::kBarP + t));
+    mbar_arrive(bar(C::kBarP + buf));
   }
 
   if (!ok) return;
   const size_t grow = static_cast<size_t>(bh) * p.N + row;
-  if (any) {
-    if (!mbar_wait(bar(C::kBarO + t), 0, ctl)) return;
+  if (i > 0) {
+    if (!mbar_wait(bar(C::kBarO), 0, ctl)) return;
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
@@ -343,13 +336,13 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
       if (row < p.N) {
         uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D + c);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int e = 0; e < 4; ++e) {
           uint4 w;
-          w.x = pack_bf16(__uint_as_float(o[8 * i + 0]) * inv, __uint_as_float(o[8 * i + 1]) * inv);
-          w.y = pack_bf16(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv);
-          w.z = pack_bf16(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv);
-          w.w = pack_bf16(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv);
-          dst[i] = w;
+          w.x = pack_bf16(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
+          w.y = pack_bf16(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
+          w.z = pack_bf16(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
+          w.w = pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
+          dst[e] = w;
         }
       }
     }
@@ -357,7 +350,7 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
       p.lse[grow] = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
   } else if (row < p.N) {
     uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D);
-    for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+    for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
     p.lse[grow] = -INFINITY;
   }
 }
@@ -376,9 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  int bh, pair;
-  decode_work(p, bh, pair);
-  const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
+  int bh, qt;
+  decode_work(p, bh, qt);
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -387,11 +379,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
       mbar_init(bar(C::kBarFull + s), 1);
       mbar_init(bar(C::kBarEmpty + s), 1);
     }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(bar(C::kBarS + t), 1);
-      mbar_init(bar(C::kBarP + t), 128);
-      mbar_init(bar(C::kBarO + t), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(C::kBarS + b), 1);
+      mbar_init(bar(C::kBarP + b), 128);
     }
+    mbar_init(bar(C::kBarPV), 1);
+    mbar_init(bar(C::kBarO), 1);
     mbar_init(bar(C::kBarDrain), 1);
     fence_barrier_init();
   }
@@ -405,13 +398,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
   const uint32_t tmem = *tmem_slot;
 
   if (warp == kLoadWarp) {
-    if (lane == 0) producer<D>(p, sbase, ctl, bh, qt0, qt1);
+    if (lane == 0) producer<D>(p, sbase, ctl, bh, qt);
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_issuer<D>(p, sbase, tmem, ctl, qt0, qt1);
+    if (lane == 0) mma_issuer<D>(p, sbase, tmem, ctl, qt);
     __syncwarp();
   } else {
-    softmax_wg<D>(p, sbase, tmem, ctl, bh, qt0, qt1);
+    softmax_wg<D>(p, sbase, tmem, ctl, bh, qt);
   }
 
   tc_fence_before();
@@ -431,7 +424,7 @@ cudaError_t launch(const FwdParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const unsigned grid = static_cast<unsigned>(p.n_pairs) * static_cast<unsigned>(p.BH);
+  const unsigned grid = static_cast<unsigned>(p.n_tiles) * static_cast<unsigned>(p.BH);
   fwd_tc_kernel<D><<<grid, kThreads, Cfg<D>::kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }

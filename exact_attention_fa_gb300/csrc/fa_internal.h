@@ -21,8 +21,7 @@ struct FwdParams {
   float* lse;
   const uint8_t* block_mask;  // [n_tiles][n_tiles] or null
   int BH, N;
-  int n_tiles;                // ceil(N / 128)
-  int n_pairs;                // ceil(n_tiles / 2): a CTA owns two 128-row query tiles
+  int n_tiles;                // ceil(N / 128): query tiles = key tiles = block-mask tiles
   int heads_per_group;        // CTA order: groups of heads whose K/V fit in L2
   int mode;                   // MaskMode
   float scale_log2;           // scale * log2(e)
@@ -64,7 +63,8 @@ struct BwdParams {
 };
 
 // Launchers; return a cudaError_t (cudaSuccess on success).
-cudaError_t launch_fwd_tc(const FwdParams& p, int d, int num_sms, cudaStream_t s);
+cudaError_t launch_fwd_tc(const FwdParams& p, int d, int num_sms, cudaStream_t s);    // 1 tile/CTA
+cudaError_t launch_fwd_pair(const FwdParams& p, int d, cudaStream_t s);               // 2 tiles/CTA
 cudaError_t launch_fwd_fp32(const Fp32FwdParams& p, cudaStream_t s);
 cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t s);
 

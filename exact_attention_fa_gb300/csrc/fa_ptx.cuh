@@ -69,14 +69,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that lets the thread sleep in hardware (up to `ns`) until the phase completes, so that
+// waiting warps do not take issue slots from the working warps of their SM sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits until the phase with the given parity of the barrier has completed. Bounded: gives up
 // (returning false, raising kErrTimeout and the CTA abort flag) after ctl.timeout_ns of wall
 // time, or as soon as another warp of the CTA has aborted.
+// After the first failed test, waiting threads sleep in hardware (up to this many ns per try,
+// woken early when the phase completes) instead of spinning; 0 disables the sleep.
+#ifndef FA_WAIT_SLEEP_NS
+#define FA_WAIT_SLEEP_NS 200000
+#endif
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Ctl& ctl) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (FA_WAIT_SLEEP_NS ? mbar_try_wait_sleep(bar, parity, FA_WAIT_SLEEP_NS)
+                         : mbar_try_wait(bar, parity))
+      return true;
     if (*ctl.abort_flag) return false;
     if (globaltimer() - t0 > ctl.timeout_ns) {
       raise_error(ctl, kErrTimeout);
@@ -270,6 +291,62 @@ __device__ __forceinline__ void mma_ts2(uint32_t d_tmem, uint32_t a_tmem, uint32
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %5, p;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(accumulate), "r"(idesc)
       : "memory");
+}
+
+// Lean issue of a whole 128 x 128 (x K) product for the MMA warp, which shares its SM
+// sub-partition with busy warps: every MMA is one 64-bit add and the tcgen05.mma itself.
+// a[k]: precomputed A descriptors per K-step; b: B descriptor of step 0, K-major 128-byte swizzle
+// with 64-column boxes 16 KB apart (steps at +0, +2, +4, +6 then +1024.. in 16-byte units).
+__device__ __forceinline__ void mma_qk_d128(uint32_t d_tmem, const uint64_t (&a)[8], uint64_t b,
+                                            uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .b64 tb;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %10, 0;\n\t"
+      "add.s64 tb, %9, 2;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %2, tb, %10, 1;\n\t"
+      "add.s64 tb, %9, 4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %3, tb, %10, 1;\n\t"
+      "add.s64 tb, %9, 6;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %4, tb, %10, 1;\n\t"
+      "add.s64 tb, %9, 1024;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %5, tb, %10, 1;\n\t"
+      "add.s64 tb, %9, 1026;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %6, tb, %10, 1;\n\t"
+      "add.s64 tb, %9, 1028;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %7, tb, %10, 1;\n\t"
+      "add.s64 tb, %9, 1030;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %8, tb, %10, 1;\n\t"
+      "}\n" ::"r"(d_tmem),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]),
+      "l"(b), "r"(idesc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_qk_d64(uint32_t d_tmem, const uint64_t (&a)[4], uint64_t b,
+                                           uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .b64 tb;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %6, 0;\n\t"
+      "add.s64 tb, %5, 2;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %2, tb, %6, 1;\n\t"
+      "add.s64 tb, %5, 4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %3, tb, %6, 1;\n\t"
+      "add.s64 tb, %5, 6;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %4, tb, %6, 1;\n\t"
+      "}\n" ::"r"(d_tmem),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b), "r"(idesc)
+      : "memory");
+}
+// O (+)= P V over 128 keys: A = P in TMEM (8 columns per K-step), B = V MN-major (16 rows = 2 KB
+// per K-step, i.e. +128 in 16-byte units).
+__device__ __forceinline__ void mma_pv_k128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 tb;\n\t.reg .b32 ta;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.s32 ta, %1, 8;\n\tadd.s64 tb, %2, 128;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 16;\n\tadd.s64 tb, %2, 256;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 24;\n\tadd.s64 tb, %2, 384;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 32;\n\tadd.s64 tb, %2, 512;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 40;\n\tadd.s64 tb, %2, 640;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 48;\n\tadd.s64 tb, %2, 768;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 56;\n\tadd.s64 tb, %2, 896;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__host__ __device__ constexpr uint64_t sdesc64(uint32_t lo, uint32_t hi) {
+  return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32 D, dense.
