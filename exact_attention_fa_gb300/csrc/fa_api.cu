@@ -96,6 +96,20 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int BH, int N, int d, i
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view [B*H][N][d] of an fp32 tensor, box 32 x 64 x 1 (128-byte rows), 128-byte swizzle.
+bool encode_f32_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                                 static_cast<cuuint64_t>(N) * d * 4};
+  const cuuint32_t box[3] = {32, 64, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int to_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
 int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -216,7 +230,8 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   fa::BwdParams p{};
   const int BH = B * H;
   if (!encode_bf16_map(&p.tm_q, q, BH, N, d) || !encode_bf16_map(&p.tm_k, k, BH, N, d) ||
-      !encode_bf16_map(&p.tm_v, v, BH, N, d) || !encode_bf16_map(&p.tm_do, dO, BH, N, d))
+      !encode_bf16_map(&p.tm_v, v, BH, N, d) || !encode_bf16_map(&p.tm_do, dO, BH, N, d) ||
+      !encode_f32_map(&p.tm_dq, dq, BH, N, d))
     return FA_ERR_CUDA;
   p.o = static_cast<const __nv_bfloat16*>(o);
   p.dO = static_cast<const __nv_bfloat16*>(dO);

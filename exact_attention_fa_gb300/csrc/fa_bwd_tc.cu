@@ -36,6 +36,7 @@ constexpr int BT = 128;  // keys per CTA tile = queries per inner tile
 constexpr int kComputeWarps = 8;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kDrainWarp0 = 10;
 constexpr int kThreads = 14 * 32;
 constexpr int kBoxBytes = 128 * 64 * 2;
 
@@ -53,6 +54,9 @@ struct BCfg {
   static constexpr int kStageLse = 2 * kTileBytes;
   static constexpr int kStageD = 2 * kTileBytes + 512;
   static constexpr int kStageBytes = 2 * kTileBytes + 1024;
+  // dQ_i is staged for the bulk reductions (128-byte-swizzled fp32 boxes of 64 rows x 32
+  // columns) in the ring stage that held Q_i and dO_i: exactly 128 x d x 4 bytes, dead once dQ_i
+  // is computed. The drain hands the stage back to the producer after the TMA has read it.
   static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
   static constexpr int kBarKV = 0;
   static constexpr int kBarFull = 1;
@@ -223,8 +227,7 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
     for (int k = 0; k < BT / 16; ++k)
       mma_ss2(tDQ, ds_mn + ((k * 2048) >> 4), k_mn + ((k * 2048) >> 4), kHi, kIdescQ,
               k > 0 ? 1u : 0u);
-    mma_commit(bar(C::kBarDQFull));
-    mma_commit(bar(C::kBarEmpty + st));
+    mma_commit(bar(C::kBarDQFull));  // (the drain releases stage st after staging dQ_i in it)
   }
   if (ok) {
     mma_commit(bar(C::kBarAcc));
@@ -352,35 +355,55 @@ __device__ void bwd_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, u
   }
 }
 
+// dQ_i (TMEM, thread = query row) -> scale -> swizzled fp32 staging tile in shared memory ->
+// bulk tensor reduction into the fp32 output (coalesced adds at L2, done by the TMA unit). The
+// TMEM columns are handed back as soon as they are read, the ring stage once the TMA has read it.
 template <int D>
-__device__ void bwd_drain(const BwdParams& p, uint32_t sbase, uint32_t tmem, const Ctl& ctl, int bh,
-                          int i0) {
+__device__ void bwd_drain(const BwdParams& p, uint32_t sbase, uint8_t* smem, uint32_t tmem,
+                          const Ctl& ctl, int bh, int i0) {
   using C = BCfg<D>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int quad = warp % 4;
   const int qr = quad * 32 + lane;  // query row within the tile (TMEM lane)
+  const bool issuer = warp == kDrainWarp0 && lane == 0;
   const uint32_t tQ = tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::kColDQ;
+  constexpr uint32_t kBox = 64 * 128;       // one TMA box: 64 rows x 128 B
+  constexpr uint32_t kColBox = 128 * 128;   // 32 columns of the 128 rows
   for (int i = i0, it = 0; i < p.n_tiles; ++i, ++it) {
-    if (!mbar_wait(bar(C::kBarDQFull), it & 1, ctl)) return;
+    const int st = it % C::kStages;
+    const bool bad = !mbar_wait(bar(C::kBarDQFull), it & 1, ctl);
+    if (bar_red_or(1, 128, bad)) return;
     tc_fence_after();
-    const int q = i * BT + qr;
-    float4* dst = reinterpret_cast<float4*>(p.dq + (static_cast<size_t>(bh) * p.N + q) * D);
+    uint8_t* row = smem + C::kOffStage + st * C::kStageBytes + qr * 128;
 #pragma unroll 1
     for (int c = 0; c < D; c += 32) {
       uint32_t v[32];
       tmem_ld32(tQ + c, v);
-      if (q < p.N) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          atomicAdd(dst + c / 4 + u,
-                    make_float4(__uint_as_float(v[4 * u]) * p.scale, __uint_as_float(v[4 * u + 1]) * p.scale,
-                                __uint_as_float(v[4 * u + 2]) * p.scale, __uint_as_float(v[4 * u + 3]) * p.scale));
+      if (c + 32 == D) {  // every column read: the MMA warp may reuse them
+        tc_fence_before();
+        mbar_arrive(bar(C::kBarDQEmpty));
       }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<float4*>(row + (c / 32) * kColBox + ((u ^ (qr & 7)) << 4)) =
+            make_float4(__uint_as_float(v[4 * u]) * p.scale, __uint_as_float(v[4 * u + 1]) * p.scale,
+                        __uint_as_float(v[4 * u + 2]) * p.scale,
+                        __uint_as_float(v[4 * u + 3]) * p.scale);
     }
-    tc_fence_before();
-    mbar_arrive(bar(C::kBarDQEmpty));
+    fence_proxy_async_smem();
+    bar_sync(1, 128);
+    if (issuer) {
+      const uint32_t src = sbase + C::kOffStage + st * C::kStageBytes;
+      for (int b = 0; b < D / 32; ++b)
+        for (int rb = 0; rb < 2; ++rb)
+          tma_reduce_add_3d(&p.tm_dq, src + b * kColBox + rb * kBox, 32 * b, i * BT + rb * 64, bh);
+      bulk_commit();
+      bulk_wait_read_all();
+      mbar_arrive(bar(C::kBarEmpty + st));  // the producer may load the next Q, dO here
+    }
   }
+  if (issuer) bulk_wait_all();  // the reductions complete before the kernel ends
 }
 
 template <int D>
@@ -437,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     if (lane == 0) bwd_mma<D>(p, sbase, tmem, ctl, i0);
     __syncwarp();
   } else {
-    bwd_drain<D>(p, sbase, tmem, ctl, bh, i0);
+    bwd_drain<D>(p, sbase, smem, tmem, ctl, bh, i0);
   }
 
   tc_fence_before();

@@ -45,6 +45,7 @@ struct BwdParams {
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   CUtensorMap tm_do;
+  CUtensorMap tm_dq;  // fp32 [B*H][N][d], box 32 x 64 x 1, 128-byte swizzle (bulk reductions)
   const __nv_bfloat16* o;
   const __nv_bfloat16* dO;
   const float* lse;

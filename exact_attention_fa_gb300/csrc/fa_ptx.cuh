@@ -121,6 +121,45 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint3
       : "memory");
 }
 
+// Bulk tensor reduction shared -> global: adds a swizzled fp32 shared-memory box into the tensor
+// (element-wise, performed at L2), tracked by the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_reduce_add_3d(const void* map, uint32_t src, int c0, int c1,
+                                                  int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until the shared memory of every committed bulk operation has been read.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until every committed bulk operation has completed (its global writes are done).
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Named barrier over `count` threads that also ORs a predicate across them: every participant
+// gets the same answer, so a group can leave a loop together (never stranding a barrier).
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred pin, pout;\n\t"
+      "setp.ne.b32 pin, %1, 0;\n\t"
+      "bar.red.or.pred pout, %2, %3, pin;\n\t"
+      "selp.u32 %0, 1, 0, pout;\n\t}\n"
+      : "=r"(out)
+      : "r"(v ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return out != 0;
+}
+__device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Makes generic-proxy shared-memory writes of this thread visible to the async proxy (TMA,
 // tensor cores).
 __device__ __forceinline__ void fence_proxy_async_smem() {
