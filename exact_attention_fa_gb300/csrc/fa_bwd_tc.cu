@@ -273,6 +273,10 @@ __device__ void bwd_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, u
     else if (p.causal && i == j) lim = min(64, max(0, r - 64 * half));
     else lim = 0;
 
+    // P^T = exp2(S^T * scale * log2e - lse2): row statistics read four at a time, arithmetic on
+    // packed fp32 pairs.
+    const float4* lse4 = reinterpret_cast<const float4*>(lse2);
+    const unsigned long long k2 = f2_pack(sl2, sl2);
     float pv[64];
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
@@ -280,15 +284,25 @@ __device__ void bwd_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, u
       tmem_ld32(tS + 32 * ch, s);
       uint32_t pk[16];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int x0 = 32 * ch + 2 * u;
-        float p0 = ex2(fmaf(__uint_as_float(s[2 * u]), sl2, -lse2[x0]));
-        float p1 = ex2(fmaf(__uint_as_float(s[2 * u + 1]), sl2, -lse2[x0 + 1]));
+      for (int u = 0; u < 8; ++u) {
+        const float4 L = lse4[8 * ch + u];
+        const int x0 = 32 * ch + 4 * u;
+        float a0, a1, a2, a3;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * u]), __uint_as_float(s[4 * u + 1])), k2,
+                         f2_pack(-L.x, -L.y)), a0, a1);
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * u + 2]), __uint_as_float(s[4 * u + 3])), k2,
+                         f2_pack(-L.z, -L.w)), a2, a3);
+        float p0 = ex2(a0), p1 = ex2(a1), p2 = ex2(a2), p3 = ex2(a3);
         p0 = x0 < lim ? 0.f : p0;
         p1 = x0 + 1 < lim ? 0.f : p1;
+        p2 = x0 + 2 < lim ? 0.f : p2;
+        p3 = x0 + 3 < lim ? 0.f : p3;
         pv[x0] = p0;
         pv[x0 + 1] = p1;
-        pk[u] = pack_bf16(p0, p1);
+        pv[x0 + 2] = p2;
+        pv[x0 + 3] = p3;
+        pk[2 * u] = pack_bf16(p0, p1);
+        pk[2 * u + 1] = pack_bf16(p2, p3);
       }
       tmem_st16(tS + 16 * ch, pk);
     }
@@ -298,17 +312,25 @@ __device__ void bwd_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, u
 
     if (!mbar_wait(bar(C::kBarDP), it & 1, ctl)) { ok = false; break; }
     tc_fence_after();
+    const float4* d4 = reinterpret_cast<const float4*>(dsum);
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
       uint32_t dp[32];
       tmem_ld32(tDP + 32 * ch, dp);
       uint32_t pk[16];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int x0 = 32 * ch + 2 * u;
-        const float d0 = pv[x0] * (__uint_as_float(dp[2 * u]) - dsum[x0]);
-        const float d1 = pv[x0 + 1] * (__uint_as_float(dp[2 * u + 1]) - dsum[x0 + 1]);
-        pk[u] = pack_bf16(d0, d1);
+      for (int u = 0; u < 8; ++u) {  // dS = P * (dP - D)
+        const float4 Dv = d4[8 * ch + u];
+        const int x0 = 32 * ch + 4 * u;
+        float d0, d1, d2, d3;
+        f2_unpack(f2_mul(f2_pack(pv[x0], pv[x0 + 1]),
+                         f2_add(f2_pack(__uint_as_float(dp[4 * u]), __uint_as_float(dp[4 * u + 1])),
+                                f2_pack(-Dv.x, -Dv.y))), d0, d1);
+        f2_unpack(f2_mul(f2_pack(pv[x0 + 2], pv[x0 + 3]),
+                         f2_add(f2_pack(__uint_as_float(dp[4 * u + 2]), __uint_as_float(dp[4 * u + 3])),
+                                f2_pack(-Dv.z, -Dv.w))), d2, d3);
+        pk[2 * u] = pack_bf16(d0, d1);
+        pk[2 * u + 1] = pack_bf16(d2, d3);
       }
       tmem_st16(tDP + 16 * ch, pk);
       // dS (queries contiguous per key row) into the 128-byte-swizzled MN-major operand
