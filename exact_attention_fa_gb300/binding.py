@@ -33,6 +33,7 @@ SIGNATURES = [
     ("fa_bwd_workspace_bytes", ctypes.c_size_t, [_I, _I, _I, _I]),
     ("fa_bwd", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
     ("fa_bwd_noalloc", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    ("fa_selftest_wait_timeout", _I, [ctypes.c_uint, _P]),
     ("fa_check_device_error", _I, [_P]),
     ("fa_status_string", ctypes.c_char_p, [_I]),
     ("fa_abi_version", _I, []),
@@ -158,6 +159,13 @@ def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool):
            load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
                                  _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
                                  _stream(q)))
+
+
+def fa_selftest_wait_timeout(timeout_us: int = 20000, device=None):
+    """Runs the library's bounded-wait self-test kernel (a wait that can only time out)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    s = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    _check("fa_selftest_wait_timeout", load().fa_selftest_wait_timeout(int(timeout_us), s))
 
 
 def fa_check_device_error(device=None):

@@ -10,6 +10,7 @@
 
 #include "fa.h"
 #include "fa_internal.h"
+#include "fa_ptx.cuh"
 
 namespace {
 
@@ -111,6 +112,20 @@ bool encode_f32_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
 }
 
 int to_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+// One thread waits, with the kernels' bounded wait, on a barrier nobody arrives at.
+__global__ void selftest_wait_kernel(unsigned* err, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    fa::mbar_init(fa::smem_u32(&bar), 1);
+    fa::fence_barrier_init();
+  }
+  __syncthreads();
+  const fa::Ctl ctl{&abort_flag, err, timeout_ns};
+  if (threadIdx.x == 0) fa::mbar_wait(fa::smem_u32(&bar), 0, ctl);
+}
 
 int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
              int N, int d, float scale, int mode, const uint8_t* block_mask, fa_stream_t stream) {
@@ -252,6 +267,16 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   p.err = ds->err;
   p.timeout_ns = kWaitTimeoutNs;
   return to_status(fa::launch_bwd(p, ds->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fa_selftest_wait_timeout(unsigned timeout_us, fa_stream_t stream) {
+  if (timeout_us < 1 || timeout_us > 10000000u) return FA_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  const int st = device_state(&ds);
+  if (st != FA_OK) return st;
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      ds->err, static_cast<unsigned long long>(timeout_us) * 1000ull);
+  return to_status(cudaGetLastError());
 }
 
 int fa_check_device_error(fa_stream_t stream) {

@@ -109,6 +109,13 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    const float* lse, float* dq, void* dk, void* dv, int B, int H, int N, int d,
                    float scale, int causal, fa_stream_t stream);
 
+/* Diagnostic, with no counterpart on the pages: launches one CTA whose thread waits on an
+ * on-chip barrier that nothing ever arrives at, bounded by timeout_us (1 .. 10^7 microseconds).
+ * The wait gives up, records FA_ERR_DEVICE_TIMEOUT in the device error word and the kernel
+ * returns: a stuck pipeline surfaces as a status (via fa_check_device_error), not as a hang,
+ * and the CUDA context stays usable. */
+int fa_selftest_wait_timeout(unsigned timeout_us, fa_stream_t stream);
+
 /* Synchronises `stream`, then reads and clears the device error word of the current device.
  * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (a kernel gave up on a barrier; its outputs are invalid),
  * or FA_ERR_CUDA if the synchronisation itself failed. */

@@ -102,3 +102,8 @@ def test_no_device_here_is_reported_not_crashed(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert lib.fa_fwd(fake(), fake(), fake(), fake(), fake(), 1, 1, 128, 64, 0.125, 0, None) == 6
+
+
+def test_selftest_validation(lib):
+    assert lib.fa_selftest_wait_timeout(0, None) == 1
+    assert lib.fa_selftest_wait_timeout(20000001, None) == 1
