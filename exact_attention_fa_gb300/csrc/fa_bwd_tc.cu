@@ -9,20 +9,22 @@
 // Kernel 1 (prep): per row, D_i and lse2_i = lse_i * log2(e) into the workspace (padded to whole
 // 128-row tiles: +inf / 0 on padding rows so that they contribute nothing), and dQ zeroed.
 //
-// Kernel 2 (main), one CTA per (128-key tile j, head), 14 warps:
+// Kernel 2 (main), one CTA per (128-key tile j, head), 16 warps:
 //   * warp 8 (one lane): TMA. K_j and V_j once; then per query tile i, Q_i, dO_i and the 128
-//     lse2 / D values of that tile into a two-stage ring;
+//     lse2 / D values of that tile into a ring of stages;
 //   * warp 9 (one lane): MMAs. S^T = K Q_i^T and dP^T = V dO_i^T (keys on TMEM lanes, queries on
-//     columns); dV += P^T dO_i and dK += dS^T Q_i with P^T / dS^T read from TMEM; dQ_i = dS K with
-//     dS read from shared memory;
+//     columns); dV += P^T dO_i and dK += dS^T Q_i with P^T / dS^T read from TMEM; dQ_i from dS in
+//     shared memory (d = 128: dQ_i^T = K^T dS^T, d on lanes; d = 64: dQ_i = dS K, queries on lanes);
 //   * warps 0-7 (two warpgroups, one per half of the query columns): thread = key row. Computes
 //     P^T = exp2(S^T * scale * log2e - lse2) (causal / tail masked), writes it as bf16 over S^T,
 //     then dS^T = P^T * (dP^T - D) as bf16 over dP^T and, transposed by its layout, into the
 //     shared-memory operand of the dQ product; at the end stores dV and scale * dK;
-//   * warps 10-13: thread = query row; reads dQ_i from TMEM and adds scale * dQ_i into the fp32
-//     output with vector reductions.
-// TMEM columns: S^T [0,128), dP^T [128,256) (dQ_i reuses it after dS^T was consumed),
-// dV [256, 256+d), dK [256+d, 256+2d).
+//   * warps 12-15: read dQ_i from TMEM and add scale * dQ_i into the fp32 output. d = 128: one
+//     thread per column of dQ issues coalesced fp32 reductions from registers; d = 64: the tile is
+//     staged in the ring stage and added by TMA bulk reductions. Warps 10-11 only complete the
+//     producer / MMA warpgroup, which hands registers to the drain warpgroup.
+// TMEM columns: S^T [0,128), dP^T [128,256) (at d = 128 dQ_i^T reuses it after dS^T was consumed),
+// dV [256, 256+d), dK [256+d, 256+2d) (d = 64: dQ_i at [384, 448)).
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -36,8 +38,24 @@ constexpr int BT = 128;  // keys per CTA tile = queries per inner tile
 constexpr int kComputeWarps = 8;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kDrainWarp0 = 10;
-constexpr int kThreads = 14 * 32;
+constexpr int kDrainWarp0 = 12;  // warps 12-15; warps 10 and 11 only complete the warpgroup
+constexpr int kThreads = 16 * 32;
+// Registers per thread after the warpgroups re-balance the 128 each is launched with: the
+// producer / MMA warpgroup gives some up, the dQ drain holds a whole 128-column row of dQ^T; the
+// compute warpgroups keep 128. The sum must stay within the launch's 512 x 128.
+constexpr int kRegsLoadMma = 104;
+constexpr int kRegsDrain = 144;
+static_assert(2 * 128 * 128 + 128 * kRegsLoadMma + 128 * kRegsDrain <= 65536,
+              "register split exceeds the launch's register file share");
+
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 constexpr int kBoxBytes = 128 * 64 * 2;
 
 template <int D>
@@ -77,6 +95,11 @@ struct BCfg {
   // d = 64 has room for dQ_i in its own columns; at d = 128 it reuses the dP^T columns.
   static constexpr bool kDQAliasesDP = D == 128;
   static constexpr uint32_t kColDQ = kDQAliasesDP ? kColDP : 256 + 2 * D;
+  // d = 128 computes dQ_i^T = K^T dS^T (d on TMEM lanes, queries on columns): a warp then holds
+  // 32 consecutive d of one query row, so the drain adds it into the fp32 output with coalesced
+  // reductions straight from registers, and the ring stage is free as soon as the MMAs are done.
+  // d = 64 computes dQ_i (queries on lanes) and reduces it through the stage with the TMA.
+  static constexpr bool kDQTransposed = D == 128;
 };
 
 __device__ __forceinline__ void tma_bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
@@ -153,6 +176,7 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
   constexpr uint32_t kIdescT = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T: both K-major
   constexpr uint32_t kIdescG = idesc_bf16(128, D, 0, 1);    // dV, dK: A in TMEM, B MN-major
   constexpr uint32_t kIdescQ = idesc_bf16(128, D, 1, 1);    // dQ: A = dS MN-major, B = K MN-major
+  constexpr uint32_t kIdescQT = idesc_bf16(D, 128, 1, 1);   // dQ^T: A = K MN-major, B = dS MN-major
 
   bool ok = mbar_wait(bar(C::kBarKV), 0, ctl);
   tc_fence_after();
@@ -223,11 +247,20 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
       if (!mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
     }
+    if (C::kDQTransposed) {
 #pragma unroll
-    for (int k = 0; k < BT / 16; ++k)
-      mma_ss2(tDQ, ds_mn + ((k * 2048) >> 4), k_mn + ((k * 2048) >> 4), kHi, kIdescQ,
-              k > 0 ? 1u : 0u);
-    mma_commit(bar(C::kBarDQFull));  // (the drain releases stage st after staging dQ_i in it)
+      for (int k = 0; k < BT / 16; ++k)
+        mma_ss2(tDQ, k_mn + ((k * 2048) >> 4), ds_mn + ((k * 2048) >> 4), kHi, kIdescQT,
+                k > 0 ? 1u : 0u);
+      mma_commit(bar(C::kBarDQFull));
+      mma_commit(bar(C::kBarEmpty + st));  // Q_i, dO_i (and its lse2, D rows) are no longer read
+    } else {
+#pragma unroll
+      for (int k = 0; k < BT / 16; ++k)
+        mma_ss2(tDQ, ds_mn + ((k * 2048) >> 4), k_mn + ((k * 2048) >> 4), kHi, kIdescQ,
+                k > 0 ? 1u : 0u);
+      mma_commit(bar(C::kBarDQFull));  // (the drain releases stage st after staging dQ_i in it)
+    }
   }
   if (ok) {
     mma_commit(bar(C::kBarAcc));
@@ -428,6 +461,44 @@ __device__ void bwd_drain(const BwdParams& p, uint32_t sbase, uint8_t* smem, uin
   if (issuer) bulk_wait_all();  // the reductions complete before the kernel ends
 }
 
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
+// dQ_i^T (TMEM, thread = column d of dQ, 128 query columns) -> scale -> fp32 reductions: for each
+// query a warp adds 32 consecutive floats (128 bytes, one coalesced request). The TMEM columns are
+// handed back right after the single load, before the reductions are issued.
+template <int D>
+__device__ void bwd_drain_transposed(const BwdParams& p, uint32_t sbase, uint32_t tmem,
+                                     const Ctl& ctl, int bh, int i0) {
+  using C = BCfg<D>;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int quad = warp % 4;
+  const int dcol = quad * 32 + lane;  // column of dQ (TMEM lane)
+  const uint32_t tQ = tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::kColDQ;
+  const float scale = p.scale;
+  for (int i = i0, it = 0; i < p.n_tiles; ++i, ++it) {
+    const bool bad = !mbar_wait(bar(C::kBarDQFull), it & 1, ctl);
+    if (bar_red_or(1, 128, bad)) return;
+    tc_fence_after();
+    uint32_t v[128];
+    tmem_ld64x2(tQ, v);
+    tc_fence_before();
+    mbar_arrive(bar(C::kBarDQEmpty));
+    float* dst = p.dq + (static_cast<size_t>(bh) * p.N + static_cast<size_t>(i) * BT) * D + dcol;
+    const int nvalid = min(BT, p.N - i * BT);
+    if (nvalid == BT) {
+#pragma unroll
+      for (int q = 0; q < BT; ++q) red_add_f32(dst + q * D, __uint_as_float(v[q]) * scale);
+    } else {
+#pragma unroll
+      for (int q = 0; q < BT; ++q)
+        if (q < nvalid) red_add_f32(dst + q * D, __uint_as_float(v[q]) * scale);
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_constant__ BwdParams p,
                                                              int group, int npad) {
@@ -475,14 +546,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 
   if (warp < kComputeWarps) {
     bwd_compute<D>(p, sbase, smem, tmem, ctl, bh, j, i0);
-  } else if (warp == kLoadWarp) {
-    if (lane == 0) bwd_producer<D>(p, sbase, ctl, bh, j, i0, npad);
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) bwd_mma<D>(p, sbase, tmem, ctl, i0);
+  } else if (warp < kDrainWarp0) {
+    regs_dec<kRegsLoadMma>();
+    if (warp == kLoadWarp) {
+      if (lane == 0) bwd_producer<D>(p, sbase, ctl, bh, j, i0, npad);
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) bwd_mma<D>(p, sbase, tmem, ctl, i0);
+    }
     __syncwarp();
   } else {
-    bwd_drain<D>(p, sbase, smem, tmem, ctl, bh, i0);
+    regs_inc<kRegsDrain>();
+    if (C::kDQTransposed)
+      bwd_drain_transposed<D>(p, sbase, tmem, ctl, bh, i0);
+    else
+      bwd_drain<D>(p, sbase, smem, tmem, ctl, bh, i0);
   }
 
   tc_fence_before();
