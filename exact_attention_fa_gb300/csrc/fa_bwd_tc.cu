@@ -178,7 +178,7 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
   constexpr uint32_t kIdescQ = idesc_bf16(128, D, 1, 1);    // dQ: A = dS MN-major, B = K MN-major
   constexpr uint32_t kIdescQT = idesc_bf16(D, 128, 1, 1);   // dQ^T: A = K MN-major, B = dS MN-major
 
-  bool ok = mbar_wait(bar(C::kBarKV), 0, ctl);
+  bool ok = mbar_wait_poll_warp(bar(C::kBarKV), 0, ctl);
   tc_fence_after();
   // Descriptor halves precomputed once; each MMA only adds a constant K-step offset.
   constexpr uint32_t kHi = sdesc_hi_sw128(1024);
@@ -202,7 +202,7 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
     mma_commit(bar(C::kBarS));
   };
   if (ok && i0 < p.n_tiles) {
-    ok = mbar_wait(bar(C::kBarFull + 0), 0, ctl);
+    ok = mbar_wait_poll_warp(bar(C::kBarFull + 0), 0, ctl);
     tc_fence_after();
     if (ok) issue_s(0);
   }
@@ -212,7 +212,7 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
     const uint32_t do_km = st_km + st * kStageStep + kDOOff, do_mn = q_mn + kDOOff;
     // dP^T = V dO_i^T (when dQ shares these columns, only after the previous dQ_i was drained)
     if (C::kDQAliasesDP && it > 0) {
-      if (!mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, ctl)) { ok = false; break; }
+      if (!mbar_wait_poll_warp(bar(C::kBarDQEmpty), (it - 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
     }
 #pragma unroll
@@ -222,7 +222,7 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
     }
     mma_commit(bar(C::kBarDP));
     // dV += P^T dO_i
-    if (!mbar_wait(bar(C::kBarP), it & 1, ctl)) { ok = false; break; }
+    if (!mbar_wait_poll_warp(bar(C::kBarP), it & 1, ctl)) { ok = false; break; }
     tc_fence_after();
 #pragma unroll
     for (int k = 0; k < BT / 16; ++k)
@@ -232,19 +232,19 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
     // the dV product above has read P^T first; the compute warps overlap it with dK, dQ below.
     if (i + 1 < p.n_tiles) {
       const int nx = it + 1;
-      if (!mbar_wait(bar(C::kBarFull + nx % C::kStages), (nx / C::kStages) & 1, ctl)) { ok = false; break; }
+      if (!mbar_wait_poll_warp(bar(C::kBarFull + nx % C::kStages), (nx / C::kStages) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       issue_s(nx);
     }
     // dK += dS^T Q_i ; dQ_i = dS K
-    if (!mbar_wait(bar(C::kBarDS), it & 1, ctl)) { ok = false; break; }
+    if (!mbar_wait_poll_warp(bar(C::kBarDS), it & 1, ctl)) { ok = false; break; }
     tc_fence_after();
 #pragma unroll
     for (int k = 0; k < BT / 16; ++k)
       mma_ts2(tDK, tDP + packed_col(k), q_mn + ((k * 2048) >> 4), kHi, kIdescG,
               (it > 0 || k > 0) ? 1u : 0u);
     if (!C::kDQAliasesDP && it > 0) {
-      if (!mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, ctl)) { ok = false; break; }
+      if (!mbar_wait_poll_warp(bar(C::kBarDQEmpty), (it - 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
     }
     if (C::kDQTransposed) {
@@ -269,7 +269,7 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
     int zero = 0;
     drain.abort_flag = &zero;
     mma_commit(bar(C::kBarDrain));
-    mbar_wait(bar(C::kBarDrain), 0, drain);
+    mbar_wait_poll_warp(bar(C::kBarDrain), 0, drain);
   }
 }
 
@@ -551,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     if (warp == kLoadWarp) {
       if (lane == 0) bwd_producer<D>(p, sbase, ctl, bh, j, i0, npad);
     } else if (warp == kMmaWarp) {
-      if (lane == 0) bwd_mma<D>(p, sbase, tmem, ctl, i0);
+      bwd_mma<D>(p, sbase, tmem, ctl, i0);  // whole warp: one elected lane issues
     }
     __syncwarp();
   } else {

@@ -175,13 +175,13 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
                 acc ? 1u : 0u);
   };
 
-  bool ok = mbar_wait(bar(C::kBarQ), 0, ctl);
+  bool ok = mbar_wait_warp(bar(C::kBarQ), 0, ctl);
   tc_fence_after();
   uint32_t pphase[2] = {0, 0};
   bool acc[2] = {false, false};
   // Ring positions in the producer's order: K(u0), then per union tile u_i: K(u_{i+1}), V(u_i).
   auto wait_full = [&](int ps) {
-    return mbar_wait(bar(C::kBarFull + ps % C::kStages), (ps / C::kStages) & 1, ctl);
+    return mbar_wait_warp(bar(C::kBarFull + ps % C::kStages), (ps / C::kStages) & 1, ctl);
   };
   int j = next_union(p, qt0, qt1, 0);
   int i = 0;  // index of j among the union tiles
@@ -207,7 +207,7 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
     const bool n1 = has_next && tile_active(p, qt1, jn);
 
     if (a0) {
-      if (!mbar_wait(bar(C::kBarP + 0), pphase[0], ctl)) { ok = false; break; }
+      if (!mbar_wait_warp(bar(C::kBarP + 0), pphase[0], ctl)) { ok = false; break; }
       pphase[0] ^= 1;
       tc_fence_after();
       issue_pv(0, sv, acc[0]);
@@ -221,7 +221,7 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
     // so the PV above has read P_0 before this write lands.
     if (n0) { issue_s(0, skn); mma_commit(bar(C::kBarS + 0)); }
     if (a1) {
-      if (!mbar_wait(bar(C::kBarP + 1), pphase[1], ctl)) { ok = false; break; }
+      if (!mbar_wait_warp(bar(C::kBarP + 1), pphase[1], ctl)) { ok = false; break; }
       pphase[1] ^= 1;
       tc_fence_after();
       issue_pv(1, sv, acc[1]);
@@ -242,7 +242,7 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
     int zero = 0;
     drain.abort_flag = &zero;
     mma_commit(bar(C::kBarDrain));
-    mbar_wait(bar(C::kBarDrain), 0, drain);
+    mbar_wait_warp(bar(C::kBarDrain), 0, drain);
   }
 }
 
@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_pair_kernel(const __grid_cons
     if (lane == 0) producer<D>(p, sbase, ctl, bh, qt0, qt1);
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_issuer<D>(p, sbase, tmem, ctl, qt0, qt1);
+    mma_issuer<D>(p, sbase, tmem, ctl, qt0, qt1);  // whole warp: one elected lane issues
     __syncwarp();
   } else {
     softmax_wg<D>(p, sbase, tmem, ctl, bh, qt0, qt1);

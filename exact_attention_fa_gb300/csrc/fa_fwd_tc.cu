@@ -168,11 +168,11 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
     mma_commit(bar(C::kBarS + buf));
   };
   auto wait_full = [&](int ps) {
-    return mbar_wait(bar(C::kBarFull + ps % C::kStages), (ps / C::kStages) & 1, ctl);
+    return mbar_wait_warp(bar(C::kBarFull + ps % C::kStages), (ps / C::kStages) & 1, ctl);
   };
   auto release = [&](int ps) { mma_commit(bar(C::kBarEmpty + ps % C::kStages)); };
 
-  bool ok = mbar_wait(bar(C::kBarQ), 0, ctl);
+  bool ok = mbar_wait_warp(bar(C::kBarQ), 0, ctl);
   int j = next_tile(p, qt, 0);
   int j1 = j < p.n_tiles ? next_tile(p, qt, j + 1) : p.n_tiles;
   int pos = 0;
@@ -191,7 +191,7 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
     const int kpos = j2 < p.n_tiles ? pos++ : -1;  // K(u_{i+2})
     const int vpos = pos++;                         // V(u_i)
     // O += P_i V_i once the softmax has written P_i over S buffer `buf`
-    if (!mbar_wait(bar(C::kBarP + buf), pph[buf], ctl)) { ok = false; break; }
+    if (!mbar_wait_warp(bar(C::kBarP + buf), pph[buf], ctl)) { ok = false; break; }
     pph[buf] ^= 1;
     if (!wait_full(vpos)) { ok = false; break; }
     tc_fence_after();
@@ -218,7 +218,7 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
     int zero = 0;
     drain.abort_flag = &zero;
     mma_commit(bar(C::kBarDrain));
-    mbar_wait(bar(C::kBarDrain), 0, drain);
+    mbar_wait_warp(bar(C::kBarDrain), 0, drain);
   }
 }
 
@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (lane == 0) producer<D>(p, sbase, ctl, bh, qt);
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_issuer<D>(p, sbase, tmem, ctl, qt);
+    mma_issuer<D>(p, sbase, tmem, ctl, qt);  // whole warp: one elected lane issues
     __syncwarp();
   } else {
     softmax_wg<D>(p, sbase, tmem, ctl, bh, qt);

@@ -106,6 +106,44 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const C
   }
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// The same bounded wait by polling, never suspending: for the single thread that issues MMAs, which
+// must resume within a few cycles of the phase completing to keep the tensor pipe fed (a thread
+// suspended in try_wait takes a few hundred cycles to resume).
+__device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity, const Ctl& ctl) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((n & 63u) == 0) {
+      if (*ctl.abort_flag) return false;
+      if (globaltimer() - t0 > ctl.timeout_ns) {
+        raise_error(ctl, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Waits of the converged MMA-issuing warp: every lane waits and all lanes take the same outcome.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const Ctl& ctl) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl));
+}
+__device__ __forceinline__ bool mbar_wait_poll_warp(uint32_t bar, uint32_t parity, const Ctl& ctl) {
+  return __all_sync(0xffffffffu, mbar_wait_poll(bar, parity, ctl));
+}
+
 // ------------------------------------------------------------------------------------------
 // TMA (bulk tensor copies global -> shared, completion counted in bytes on an mbarrier)
 // ------------------------------------------------------------------------------------------
@@ -188,13 +226,18 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// MMA and commit helpers are executed by a whole converged warp: each asm block elects one lane
+// (elect.sync, the same lane every time) to issue the tcgen05 instructions. Issued this way the
+// descriptors stay warp-uniform; issuing from a one-lane branch instead was measured ~3x slower
+// per MMA when busy warps share the SM sub-partition.
+//
 // D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate. `accumulate` = 0 overwrites D.
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -202,17 +245,18 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// Arrives (once) on the mbarrier when every tcgen05 operation issued so far by this thread has
-// completed.
+// Arrives (once) on the mbarrier when every tcgen05 operation issued so far by the elected lane
+// has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
       : "memory");
 }
 
@@ -336,21 +380,21 @@ __host__ __device__ constexpr uint32_t sdesc_hi_sw128(uint32_t sbo) {
 __device__ __forceinline__ void mma_ss2(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
                                         uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
       "setp.ne.b32 p, %5, 0;\n\t"
       "mov.b64 da, {%1, %3};\n\t"
       "mov.b64 db, {%2, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}\n" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}\n" ::"r"(d_tmem),
       "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void mma_ts2(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
                                         uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "mov.b64 db, {%2, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %5, p;\n\t}\n" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %5, p;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(accumulate), "r"(idesc)
       : "memory");
 }
@@ -362,15 +406,15 @@ __device__ __forceinline__ void mma_ts2(uint32_t d_tmem, uint32_t a_tmem, uint32
 __device__ __forceinline__ void mma_qk_d128(uint32_t d_tmem, const uint64_t (&a)[8], uint64_t b,
                                             uint32_t idesc) {
   asm volatile(
-      "{\n\t.reg .b64 tb;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %10, 0;\n\t"
-      "add.s64 tb, %9, 2;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %2, tb, %10, 1;\n\t"
-      "add.s64 tb, %9, 4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %3, tb, %10, 1;\n\t"
-      "add.s64 tb, %9, 6;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %4, tb, %10, 1;\n\t"
-      "add.s64 tb, %9, 1024;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %5, tb, %10, 1;\n\t"
-      "add.s64 tb, %9, 1026;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %6, tb, %10, 1;\n\t"
-      "add.s64 tb, %9, 1028;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %7, tb, %10, 1;\n\t"
-      "add.s64 tb, %9, 1030;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %8, tb, %10, 1;\n\t"
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .b64 tb;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %10, 0;\n\t"
+      "add.s64 tb, %9, 2;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, tb, %10, 1;\n\t"
+      "add.s64 tb, %9, 4;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, tb, %10, 1;\n\t"
+      "add.s64 tb, %9, 6;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, tb, %10, 1;\n\t"
+      "add.s64 tb, %9, 1024;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, tb, %10, 1;\n\t"
+      "add.s64 tb, %9, 1026;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, tb, %10, 1;\n\t"
+      "add.s64 tb, %9, 1028;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, tb, %10, 1;\n\t"
+      "add.s64 tb, %9, 1030;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], %8, tb, %10, 1;\n\t"
       "}\n" ::"r"(d_tmem),
       "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]),
       "l"(b), "r"(idesc)
@@ -379,11 +423,11 @@ __device__ __forceinline__ void mma_qk_d128(uint32_t d_tmem, const uint64_t (&a)
 __device__ __forceinline__ void mma_qk_d64(uint32_t d_tmem, const uint64_t (&a)[4], uint64_t b,
                                            uint32_t idesc) {
   asm volatile(
-      "{\n\t.reg .b64 tb;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %6, 0;\n\t"
-      "add.s64 tb, %5, 2;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %2, tb, %6, 1;\n\t"
-      "add.s64 tb, %5, 4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %3, tb, %6, 1;\n\t"
-      "add.s64 tb, %5, 6;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %4, tb, %6, 1;\n\t"
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .b64 tb;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %6, 0;\n\t"
+      "add.s64 tb, %5, 2;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, tb, %6, 1;\n\t"
+      "add.s64 tb, %5, 4;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, tb, %6, 1;\n\t"
+      "add.s64 tb, %5, 6;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, tb, %6, 1;\n\t"
       "}\n" ::"r"(d_tmem),
       "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b), "r"(idesc)
       : "memory");
@@ -393,16 +437,16 @@ __device__ __forceinline__ void mma_qk_d64(uint32_t d_tmem, const uint64_t (&a)[
 __device__ __forceinline__ void mma_pv_k128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 tb;\n\t.reg .b32 ta;\n\t"
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .pred p;\n\t.reg .b64 tb;\n\t.reg .b32 ta;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
-      "add.s32 ta, %1, 8;\n\tadd.s64 tb, %2, 128;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
-      "add.s32 ta, %1, 16;\n\tadd.s64 tb, %2, 256;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
-      "add.s32 ta, %1, 24;\n\tadd.s64 tb, %2, 384;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
-      "add.s32 ta, %1, 32;\n\tadd.s64 tb, %2, 512;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
-      "add.s32 ta, %1, 40;\n\tadd.s64 tb, %2, 640;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
-      "add.s32 ta, %1, 48;\n\tadd.s64 tb, %2, 768;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
-      "add.s32 ta, %1, 56;\n\tadd.s64 tb, %2, 896;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.s32 ta, %1, 8;\n\tadd.s64 tb, %2, 128;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 16;\n\tadd.s64 tb, %2, 256;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 24;\n\tadd.s64 tb, %2, 384;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 32;\n\tadd.s64 tb, %2, 512;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 40;\n\tadd.s64 tb, %2, 640;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 48;\n\tadd.s64 tb, %2, 768;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 56;\n\tadd.s64 tb, %2, 896;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
       "}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
