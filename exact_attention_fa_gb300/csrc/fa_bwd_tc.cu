@@ -105,8 +105,9 @@ struct BCfg {
 __device__ __forceinline__ void tma_bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                              uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      "\n\t}" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
@@ -147,7 +148,7 @@ __device__ void bwd_producer(const BwdParams& p, uint32_t sbase, const Ctl& ctl,
   for (int i = i0, it = 0; i < p.n_tiles; ++i, ++it) {
     const int st = it % C::kStages;
     const int round = it / C::kStages;
-    if (!mbar_wait(bar(C::kBarEmpty + st), (round & 1) ^ 1, ctl)) { ok = false; break; }
+    if (!mbar_wait_warp(bar(C::kBarEmpty + st), (round & 1) ^ 1, ctl)) { ok = false; break; }
     const uint32_t sb = sbase + C::kOffStage + st * C::kStageBytes;
     mbar_arrive_expect_tx(bar(C::kBarFull + st), 2 * C::kTileBytes + 1024);
     for (int b = 0; b < D / 64; ++b) {
@@ -163,9 +164,9 @@ __device__ void bwd_producer(const BwdParams& p, uint32_t sbase, const Ctl& ctl,
     Ctl drain = ctl;
     int zero = 0;
     drain.abort_flag = &zero;
-    mbar_wait(bar(C::kBarKV), 0, drain);
+    mbar_wait_warp(bar(C::kBarKV), 0, drain);
     for (int s = 0; s < C::kStages; ++s)
-      if (issued[s] >= 0) mbar_wait(bar(C::kBarFull + s), issued[s] & 1, drain);
+      if (issued[s] >= 0) mbar_wait_warp(bar(C::kBarFull + s), issued[s] & 1, drain);
   }
 }
 
@@ -549,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   } else if (warp < kDrainWarp0) {
     regs_dec<kRegsLoadMma>();
     if (warp == kLoadWarp) {
-      if (lane == 0) bwd_producer<D>(p, sbase, ctl, bh, j, i0, npad);
+      bwd_producer<D>(p, sbase, ctl, bh, j, i0, npad);  // whole warp: one elected lane issues
     } else if (warp == kMmaWarp) {
       bwd_mma<D>(p, sbase, tmem, ctl, i0);  // whole warp: one elected lane issues
     }

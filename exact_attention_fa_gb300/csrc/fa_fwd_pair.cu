@@ -114,7 +114,7 @@ __device__ void producer(const FwdParams& p, uint32_t sbase, const Ctl& ctl, int
   auto load = [&](const void* map, int j) {
     const int s = pos % C::kStages;
     const int round = pos / C::kStages;
-    if (!mbar_wait(bar(C::kBarEmpty + s), (round & 1) ^ 1, ctl)) return false;
+    if (!mbar_wait_warp(bar(C::kBarEmpty + s), (round & 1) ^ 1, ctl)) return false;
     mbar_arrive_expect_tx(bar(C::kBarFull + s), C::kTileBytes);
     for (int b = 0; b < D / 64; ++b)
       tma_load_3d(sbase + C::kOffKV + s * C::kTileBytes + b * kBoxBytes, map, bar(C::kBarFull + s),
@@ -136,9 +136,9 @@ __device__ void producer(const FwdParams& p, uint32_t sbase, const Ctl& ctl, int
     Ctl drain = ctl;
     int zero = 0;
     drain.abort_flag = &zero;
-    mbar_wait(bar(C::kBarQ), 0, drain);
+    mbar_wait_warp(bar(C::kBarQ), 0, drain);
     for (int s = 0; s < C::kStages; ++s)
-      if (issued[s] >= 0) mbar_wait(bar(C::kBarFull + s), issued[s] & 1, drain);
+      if (issued[s] >= 0) mbar_wait_warp(bar(C::kBarFull + s), issued[s] & 1, drain);
   }
 }
 
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_pair_kernel(const __grid_cons
   const uint32_t tmem = *tmem_slot;
 
   if (warp == kLoadWarp) {
-    if (lane == 0) producer<D>(p, sbase, ctl, bh, qt0, qt1);
+    producer<D>(p, sbase, ctl, bh, qt0, qt1);  // whole warp: one elected lane issues
     __syncwarp();
   } else if (warp == kMmaWarp) {
     mma_issuer<D>(p, sbase, tmem, ctl, qt0, qt1);  // whole warp: one elected lane issues
