@@ -161,13 +161,14 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (static_cast<long long>(p.n_tiles) * BH > 0x7fffffffll) return FA_ERR_TOO_LARGE;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   // Two kernels: two 128-row query tiles per CTA (ping-pong between them; K/V streamed once for
-  // 256 rows) or one query tile per CTA with double-buffered scores. Measured on GB300: the pair
-  // kernel is faster for dense / causal d = 128 (1036 vs 954 TFLOPS, causal N = 8192), the
-  // single-tile kernel for d = 64 and for block-sparse masks (441 vs 367 TFLOPS at 25% density).
+  // 256 rows) or one query tile per CTA with double-buffered scores. Measured on GB300 (TFLOPS,
+  // pair / single): d = 128 causal N = 8192 1253 / 1283, dense N = 8192 1344 / 1372; d = 64 causal
+  // N = 8192 810 / 719, dense N = 2048 629 / 596; block-sparse d = 64 at 25% density 453 / 583
+  // (the pair kernel visits the union of both tiles' key tiles).
 #ifndef FA_FWD_POLICY
 #define FA_FWD_POLICY 0  // 0: by shape as above; 1: always pair; 2: always single
 #endif
-  const bool pair = FA_FWD_POLICY == 1 || (FA_FWD_POLICY == 0 && d == 128 && mode != fa::kBlockSparse);
+  const bool pair = FA_FWD_POLICY == 1 || (FA_FWD_POLICY == 0 && d == 64 && mode != fa::kBlockSparse);
   return to_status(pair ? fa::launch_fwd_pair(p, d, cs) : fa::launch_fwd_tc(p, d, ds->num_sms, cs));
 }
 

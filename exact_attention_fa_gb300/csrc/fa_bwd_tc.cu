@@ -10,9 +10,9 @@
 // 128-row tiles: +inf / 0 on padding rows so that they contribute nothing), and dQ zeroed.
 //
 // Kernel 2 (main), one CTA per (128-key tile j, head), 16 warps:
-//   * warp 8 (one lane): TMA. K_j and V_j once; then per query tile i, Q_i, dO_i and the 128
+//   * warp 8 (one elected lane): TMA. K_j and V_j once; then per query tile i, Q_i, dO_i and the 128
 //     lse2 / D values of that tile into a ring of stages;
-//   * warp 9 (one lane): MMAs. S^T = K Q_i^T and dP^T = V dO_i^T (keys on TMEM lanes, queries on
+//   * warp 9 (one elected lane): MMAs. S^T = K Q_i^T and dP^T = V dO_i^T (keys on TMEM lanes, queries on
 //     columns); dV += P^T dO_i and dK += dS^T Q_i with P^T / dS^T read from TMEM; dQ_i from dS in
 //     shared memory (d = 128: dQ_i^T = K^T dS^T, d on lanes; d = 64: dQ_i = dS K, queries on lanes);
 //   * warps 0-7 (two warpgroups, one per half of the query columns): thread = key row. Computes

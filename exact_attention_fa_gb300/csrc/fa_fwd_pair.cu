@@ -6,13 +6,13 @@
 // running row max m, running sum l and an unnormalised accumulator O rescaled by exp(m - m_new),
 // divide by l once at the end. Neither S nor P ever leaves the SM.
 //
-// GB300 mapping (one CTA per SM, 10 warps; used for dense / causal d = 128):
+// GB300 mapping (one CTA per SM, 10 warps; used for dense / causal d = 64):
 //   * a CTA owns two 128-row query tiles (t = 0, 1) of one (b, h), so the tensor core works on one
 //     tile's QK^T / PV while the other tile's softmax runs on the CUDA cores, and each K/V tile
 //     streamed from L2 serves 256 query rows;
-//   * warp 8 (one lane) streams K_j, V_j with TMA into a ring of 128-byte-swizzled shared-memory
+//   * warp 8 (one elected lane) streams K_j, V_j with TMA into a ring of 128-byte-swizzled shared-memory
 //     stages guarded by full/empty mbarriers, keys one tile ahead of values; Q is loaded once;
-//   * warp 9 (one lane) issues the MMAs: S_t = Q_t K_j^T (both operands in shared memory, fp32
+//   * warp 9 (one elected lane) issues the MMAs: S_t = Q_t K_j^T (both operands in shared memory, fp32
 //     result in TMEM) and O_t += P_t V_j (P_t read from TMEM, V_j from shared memory);
 //   * warps 0-3 / 4-7 are the softmax warpgroups of tile 0 / 1: thread r owns query row r (TMEM
 //     lane r). It loads its 128 scores, applies the scale (log2(e) folded in, exp2 on the SFU),

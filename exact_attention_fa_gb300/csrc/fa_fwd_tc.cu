@@ -6,11 +6,13 @@
 // running row max m, running sum l and an unnormalised accumulator O rescaled by exp(m - m_new),
 // divide by l once at the end. Neither S nor P ever leaves the SM.
 //
-// GB300 mapping (one CTA per SM, 6 warps, one 128-row query tile of one (b, h) per CTA):
-//   * warp 5 (one lane) streams K_j, V_j with TMA into a ring of 128-byte-swizzled shared-memory
-//     stages guarded by full/empty mbarriers, keys two tiles ahead of values; Q is loaded once;
-//   * warp 4 (one lane) issues every tcgen05.mma. Issue blocks while the tensor pipe is busy, so
-//     this warp does nothing else. S = Q K_j^T goes to one of two S buffers in TMEM, so the scores
+// GB300 mapping (one CTA per SM, 6 warps, one 128-row query tile of one (b, h) per CTA; used for
+// d = 128 and for block-sparse masks):
+//   * warp 5 (one elected lane) streams K_j, V_j with TMA into a ring of 128-byte-swizzled
+//     shared-memory stages guarded by full/empty mbarriers, keys two tiles ahead of values; Q is
+//     loaded once;
+//   * warp 4 (one elected lane) issues every tcgen05.mma. Issue blocks while the tensor pipe is
+//     busy, so this warp does nothing else. S = Q K_j^T goes to one of two S buffers in TMEM, so the scores
 //     of tile j + 1 are computed while the softmax works on tile j; O += P_j V_j reads P_j from
 //     the S buffer it was written into (P aliased over S), after which that buffer takes
 //     S_{j+2};
