@@ -462,6 +462,17 @@ __device__ void bwd_drain(const BwdParams& p, uint32_t sbase, uint8_t* smem, uin
   if (issuer) bulk_wait_all();  // the reductions complete before the kernel ends
 }
 
+// The drain paces its reductions: after every FA_RED_PACE_GROUP of them the warp sleeps
+// FA_RED_PACE_NS. Issued back to back they fill the SM's memory-instruction queue faster than the
+// L2 takes them (~25 B/cycle per SM), and the compute warps' shared / tensor-memory accesses then
+// wait behind them (their dS phase was measured 2.9x slower). 150 ns per 16 keeps a warp's 128
+// reductions within ~1.2 us, well inside one query-tile iteration; 300 ns was already too slow.
+#ifndef FA_RED_PACE_NS
+#define FA_RED_PACE_NS 150
+#endif
+#ifndef FA_RED_PACE_GROUP
+#define FA_RED_PACE_GROUP 16
+#endif
 __device__ __forceinline__ void red_add_f32(float* addr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
@@ -491,7 +502,12 @@ __device__ void bwd_drain_transposed(const BwdParams& p, uint32_t sbase, uint32_
     const int nvalid = min(BT, p.N - i * BT);
     if (nvalid == BT) {
 #pragma unroll
-      for (int q = 0; q < BT; ++q) red_add_f32(dst + q * D, __uint_as_float(v[q]) * scale);
+      for (int q = 0; q < BT; ++q) {
+        red_add_f32(dst + q * D, __uint_as_float(v[q]) * scale);
+#if FA_RED_PACE_NS > 0
+        if ((q % FA_RED_PACE_GROUP) == FA_RED_PACE_GROUP - 1) __nanosleep(FA_RED_PACE_NS);
+#endif
+      }
     } else {
 #pragma unroll
       for (int q = 0; q < BT; ++q)
