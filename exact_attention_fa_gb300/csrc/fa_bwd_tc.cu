@@ -28,6 +28,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -40,13 +42,10 @@ constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kDrainWarp0 = 12;  // warps 12-15; warps 10 and 11 only complete the warpgroup
 constexpr int kThreads = 16 * 32;
-// Registers per thread after the warpgroups re-balance the 128 each is launched with: the
-// producer / MMA warpgroup gives some up, the dQ drain holds a whole 128-column row of dQ^T; the
-// compute warpgroups keep 128. The sum must stay within the launch's 512 x 128.
-constexpr int kRegsLoadMma = 104;
-constexpr int kRegsDrain = 144;
-static_assert(2 * 128 * 128 + 128 * kRegsLoadMma + 128 * kRegsDrain <= 65536,
-              "register split exceeds the launch's register file share");
+// Registers per thread after the warpgroups re-balance the 128 each is launched with (per head
+// dimension, in BCfg): the producer / MMA warpgroup gives some up; at d = 128 the dQ drain holds a
+// whole 128-column row of dQ^T, at d = 64 it only stages 32 columns at a time and the compute
+// warpgroups take the difference.
 
 template <int N>
 __device__ __forceinline__ void regs_inc() {
@@ -72,10 +71,15 @@ struct BCfg {
   static constexpr int kStageLse = 2 * kTileBytes;
   static constexpr int kStageD = 2 * kTileBytes + 512;
   static constexpr int kStageBytes = 2 * kTileBytes + 1024;
-  // dQ_i is staged for the bulk reductions (128-byte-swizzled fp32 boxes of 64 rows x 32
-  // columns) in the ring stage that held Q_i and dO_i: exactly 128 x d x 4 bytes, dead once dQ_i
-  // is computed. The drain hands the stage back to the producer after the TMA has read it.
-  static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+  // d = 128 computes dQ_i^T = K^T dS^T (d on TMEM lanes, queries on columns): a warp then holds
+  // 32 consecutive d of one query row, so the drain adds it into the fp32 output with coalesced
+  // reductions straight from registers. d = 64 computes dQ_i (queries on lanes) and stages it
+  // (128-byte-swizzled fp32 boxes of 64 rows x 32 columns, 32 KB) in its own buffer for TMA bulk
+  // reductions. Either way the ring stage is free as soon as the MMAs have read Q_i and dO_i.
+  static constexpr bool kDQTransposed = D == 128;
+  static constexpr int kOffDQStage = kOffStage + kStages * kStageBytes;
+  static constexpr int kDQStageBytes = kDQTransposed ? 0 : 128 * D * 4;
+  static constexpr int kOffBar = kOffDQStage + kDQStageBytes;
   static constexpr int kBarKV = 0;
   static constexpr int kBarFull = 1;
   static constexpr int kBarEmpty = 1 + kStages;
@@ -95,11 +99,11 @@ struct BCfg {
   // d = 64 has room for dQ_i in its own columns; at d = 128 it reuses the dP^T columns.
   static constexpr bool kDQAliasesDP = D == 128;
   static constexpr uint32_t kColDQ = kDQAliasesDP ? kColDP : 256 + 2 * D;
-  // d = 128 computes dQ_i^T = K^T dS^T (d on TMEM lanes, queries on columns): a warp then holds
-  // 32 consecutive d of one query row, so the drain adds it into the fp32 output with coalesced
-  // reductions straight from registers, and the ring stage is free as soon as the MMAs are done.
-  // d = 64 computes dQ_i (queries on lanes) and reduces it through the stage with the TMA.
-  static constexpr bool kDQTransposed = D == 128;
+  static constexpr int kRegsCompute = D == 128 ? 128 : 152;
+  static constexpr int kRegsLoadMma = D == 128 ? 104 : 96;
+  static constexpr int kRegsDrain = D == 128 ? 144 : 96;
+  static_assert(2 * 128 * kRegsCompute + 128 * kRegsLoadMma + 128 * kRegsDrain <= 65536,
+                "register split exceeds the launch's 512 x 128 registers");
 };
 
 __device__ __forceinline__ void tma_bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
@@ -260,7 +264,8 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
       for (int k = 0; k < BT / 16; ++k)
         mma_ss2(tDQ, ds_mn + ((k * 2048) >> 4), k_mn + ((k * 2048) >> 4), kHi, kIdescQ,
                 k > 0 ? 1u : 0u);
-      mma_commit(bar(C::kBarDQFull));  // (the drain releases stage st after staging dQ_i in it)
+      mma_commit(bar(C::kBarDQFull));
+      mma_commit(bar(C::kBarEmpty + st));
     }
   }
   if (ok) {
@@ -307,38 +312,51 @@ __device__ void bwd_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, u
     else if (p.causal && i == j) lim = min(64, max(0, r - 64 * half));
     else lim = 0;
 
-    // P^T = exp2(S^T * scale * log2e - lse2): row statistics read four at a time, arithmetic on
-    // packed fp32 pairs.
+    // P^T = exp2(S^T * scale * log2e - lse2) in two 32-column chunks: row statistics read four at
+    // a time, arithmetic on packed fp32 pairs. At d = 64 the mask (diagonal tile, padding keys) is
+    // applied only by warps that have masked entries.
     const float4* lse4 = reinterpret_cast<const float4*>(lse2);
     const unsigned long long k2 = f2_pack(sl2, sl2);
     float pv[64];
+    auto p_phase = [&](auto masked) {
 #pragma unroll
-    for (int ch = 0; ch < 2; ++ch) {
-      uint32_t s[32];
-      tmem_ld32(tS + 32 * ch, s);
-      uint32_t pk[16];
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t s[32];
+        tmem_ld32(tS + 32 * ch, s);
+        uint32_t pk[16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float4 L = lse4[8 * ch + u];
-        const int x0 = 32 * ch + 4 * u;
-        float a0, a1, a2, a3;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * u]), __uint_as_float(s[4 * u + 1])), k2,
-                         f2_pack(-L.x, -L.y)), a0, a1);
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * u + 2]), __uint_as_float(s[4 * u + 3])), k2,
-                         f2_pack(-L.z, -L.w)), a2, a3);
-        float p0 = ex2(a0), p1 = ex2(a1), p2 = ex2(a2), p3 = ex2(a3);
-        p0 = x0 < lim ? 0.f : p0;
-        p1 = x0 + 1 < lim ? 0.f : p1;
-        p2 = x0 + 2 < lim ? 0.f : p2;
-        p3 = x0 + 3 < lim ? 0.f : p3;
-        pv[x0] = p0;
-        pv[x0 + 1] = p1;
-        pv[x0 + 2] = p2;
-        pv[x0 + 3] = p3;
-        pk[2 * u] = pack_bf16(p0, p1);
-        pk[2 * u + 1] = pack_bf16(p2, p3);
+        for (int u = 0; u < 8; ++u) {
+          const float4 L = lse4[8 * ch + u];
+          const int x0 = 32 * ch + 4 * u;
+          float a0, a1, a2, a3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * u]), __uint_as_float(s[4 * u + 1])), k2,
+                           f2_pack(-L.x, -L.y)), a0, a1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * u + 2]), __uint_as_float(s[4 * u + 3])), k2,
+                           f2_pack(-L.z, -L.w)), a2, a3);
+          float p0 = ex2(a0), p1 = ex2(a1), p2 = ex2(a2), p3 = ex2(a3);
+          if constexpr (decltype(masked)::value) {
+            p0 = x0 < lim ? 0.f : p0;
+            p1 = x0 + 1 < lim ? 0.f : p1;
+            p2 = x0 + 2 < lim ? 0.f : p2;
+            p3 = x0 + 3 < lim ? 0.f : p3;
+          }
+          pv[x0] = p0;
+          pv[x0 + 1] = p1;
+          pv[x0 + 2] = p2;
+          pv[x0 + 3] = p3;
+          pk[2 * u] = pack_bf16(p0, p1);
+          pk[2 * u + 1] = pack_bf16(p2, p3);
+        }
+        tmem_st16(tS + 16 * ch, pk);
       }
-      tmem_st16(tS + 16 * ch, pk);
+    };
+    if constexpr (D == 64) {
+      if (__any_sync(0xffffffffu, lim > 0))
+        p_phase(std::true_type{});
+      else
+        p_phase(std::false_type{});
+    } else {
+      p_phase(std::true_type{});  // a single code path measured faster at d = 128
     }
     tmem_st_wait();
     tc_fence_before();
@@ -413,7 +431,7 @@ __device__ void bwd_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, u
 
 // dQ_i (TMEM, thread = query row) -> scale -> swizzled fp32 staging tile in shared memory ->
 // bulk tensor reduction into the fp32 output (coalesced adds at L2, done by the TMA unit). The
-// TMEM columns are handed back as soon as they are read, the ring stage once the TMA has read it.
+// TMEM columns are handed back as soon as they are read, the staging tile once the TMA has read it.
 template <int D>
 __device__ void bwd_drain(const BwdParams& p, uint32_t sbase, uint8_t* smem, uint32_t tmem,
                           const Ctl& ctl, int bh, int i0) {
@@ -427,11 +445,10 @@ __device__ void bwd_drain(const BwdParams& p, uint32_t sbase, uint8_t* smem, uin
   constexpr uint32_t kBox = 64 * 128;       // one TMA box: 64 rows x 128 B
   constexpr uint32_t kColBox = 128 * 128;   // 32 columns of the 128 rows
   for (int i = i0, it = 0; i < p.n_tiles; ++i, ++it) {
-    const int st = it % C::kStages;
     const bool bad = !mbar_wait(bar(C::kBarDQFull), it & 1, ctl);
     if (bar_red_or(1, 128, bad)) return;
     tc_fence_after();
-    uint8_t* row = smem + C::kOffStage + st * C::kStageBytes + qr * 128;
+    uint8_t* row = smem + C::kOffDQStage + qr * 128;
 #pragma unroll 1
     for (int c = 0; c < D; c += 32) {
       uint32_t v[32];
@@ -450,13 +467,13 @@ __device__ void bwd_drain(const BwdParams& p, uint32_t sbase, uint8_t* smem, uin
     fence_proxy_async_smem();
     bar_sync(1, 128);
     if (issuer) {
-      const uint32_t src = sbase + C::kOffStage + st * C::kStageBytes;
+      const uint32_t src = sbase + C::kOffDQStage;
       for (int b = 0; b < D / 32; ++b)
         for (int rb = 0; rb < 2; ++rb)
           tma_reduce_add_3d(&p.tm_dq, src + b * kColBox + rb * kBox, 32 * b, i * BT + rb * 64, bh);
       bulk_commit();
-      bulk_wait_read_all();
-      mbar_arrive(bar(C::kBarEmpty + st));  // the producer may load the next Q, dO here
+      bulk_wait_read_all();  // the staging buffer may be rewritten once every drain thread is past
+                             // the barrier at the top of the next iteration
     }
   }
   if (issuer) bulk_wait_all();  // the reductions complete before the kernel ends
@@ -530,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     if (threadIdx.x == 0) atomicOr(p.err, kErrSmemAlign);
     return;
   }
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int warp = threadIdx.x / 32;
   int bh, j;
   decode_bwd(p, group, bh, j);
   const int i0 = p.causal ? j : 0;
@@ -562,9 +579,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   const uint32_t tmem = *tmem_slot;
 
   if (warp < kComputeWarps) {
+    if constexpr (C::kRegsCompute > 128) regs_inc<C::kRegsCompute>();
     bwd_compute<D>(p, sbase, smem, tmem, ctl, bh, j, i0);
   } else if (warp < kDrainWarp0) {
-    regs_dec<kRegsLoadMma>();
+    regs_dec<C::kRegsLoadMma>();
     if (warp == kLoadWarp) {
       bwd_producer<D>(p, sbase, ctl, bh, j, i0, npad);  // whole warp: one elected lane issues
     } else if (warp == kMmaWarp) {
@@ -572,7 +590,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     }
     __syncwarp();
   } else {
-    regs_inc<kRegsDrain>();
+    if constexpr (C::kRegsDrain > 128)
+      regs_inc<C::kRegsDrain>();
+    else
+      regs_dec<C::kRegsDrain>();
     if (C::kDQTransposed)
       bwd_drain_transposed<D>(p, sbase, tmem, ctl, bh, i0);
     else

@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_pair_kernel(const __grid_cons
   const Ctl ctl{abort_flag, p.err, p.timeout_ns};
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
 
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int warp = threadIdx.x / 32;
   int bh, pair;
   decode_work(p, bh, pair);
   const int qt0 = 2 * pair, qt1 = 2 * pair + 1;

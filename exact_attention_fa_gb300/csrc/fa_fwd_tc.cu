@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
   const Ctl ctl{abort_flag, p.err, p.timeout_ns};
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
 
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int warp = threadIdx.x / 32;
   int bh, qt;
   decode_work(p, bh, qt);
 
