@@ -62,18 +62,38 @@ struct Cfg {
   __device__ static constexpr uint32_t col_o(int t) { return t ? 256u + D : 256u; }
 };
 
-__device__ __forceinline__ bool tile_active(const FwdParams& p, int qt, int j) {
-  if (qt * BM >= p.N) return false;
-  if (p.mode == kCausal) return j <= qt;
-  if (p.mode == kBlockSparse) return __ldg(p.block_mask + static_cast<size_t>(qt) * p.n_tiles + j) != 0;
-  return true;
-}
+// Key tiles visited by the two query tiles of a CTA, resolved once per role: dense and causal
+// query tiles need key tiles [0, last_t] (last_t = -1 past the end of the sequence); block-sparse
+// ones additionally look up the tile mask. Kept in registers so that the per-tile bookkeeping of
+// the MMA and producer warps stays a few integer compares.
+struct TilePlan {
+  const uint8_t* mask0;  // block-sparse: mask rows of the two query tiles, else null
+  const uint8_t* mask1;
+  int last0, last1, n_tiles;
+  __device__ __forceinline__ bool active(int t, int j) const {
+    const int last = t ? last1 : last0;
+    const uint8_t* m = t ? mask1 : mask0;
+    return j <= last && (m == nullptr || __ldg(m + j) != 0);
+  }
+  // next key tile >= j needed by either query tile, or n_tiles
+  __device__ __forceinline__ int next(int j) const {
+    if (mask0 == nullptr) return j <= max(last0, last1) ? j : n_tiles;
+    for (; j < n_tiles; ++j)
+      if (active(0, j) || active(1, j)) return j;
+    return n_tiles;
+  }
+};
 
-// next key tile >= j needed by either query tile, or n_tiles
-__device__ __forceinline__ int next_union(const FwdParams& p, int qt0, int qt1, int j) {
-  for (; j < p.n_tiles; ++j)
-    if (tile_active(p, qt0, j) || tile_active(p, qt1, j)) return j;
-  return p.n_tiles;
+__device__ __forceinline__ TilePlan make_plan(const FwdParams& p, int qt0, int qt1) {
+  TilePlan t;
+  t.n_tiles = p.n_tiles;
+  const bool sparse = p.mode == kBlockSparse;
+  auto last = [&](int qt) { return qt * BM >= p.N ? -1 : (p.mode == kCausal ? qt : p.n_tiles - 1); };
+  t.last0 = last(qt0);
+  t.last1 = last(qt1);
+  t.mask0 = sparse ? p.block_mask + static_cast<size_t>(qt0) * p.n_tiles : nullptr;
+  t.mask1 = sparse ? p.block_mask + static_cast<size_t>(qt1) * p.n_tiles : nullptr;
+  return t;
 }
 
 // CTA -> (head, query-tile pair). Heads are taken in groups small enough for their K/V to stay
@@ -123,10 +143,11 @@ __device__ void producer(const FwdParams& p, uint32_t sbase, const Ctl& ctl, int
     ++pos;
     return true;
   };
-  int j = next_union(p, qt0, qt1, 0);
+  const TilePlan plan = make_plan(p, qt0, qt1);
+  int j = plan.next(0);
   if (j < p.n_tiles) ok = load(&p.tm_k, j);
   while (ok && j < p.n_tiles) {
-    const int jn = next_union(p, qt0, qt1, j + 1);
+    const int jn = plan.next(j + 1);
     if (jn < p.n_tiles && !(ok = load(&p.tm_k, jn))) break;
     if (!(ok = load(&p.tm_v, j))) break;
     j = jn;
@@ -183,28 +204,29 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
   auto wait_full = [&](int ps) {
     return mbar_wait_warp(bar(C::kBarFull + ps % C::kStages), (ps / C::kStages) & 1, ctl);
   };
-  int j = next_union(p, qt0, qt1, 0);
+  const TilePlan plan = make_plan(p, qt0, qt1);
+  int j = plan.next(0);
   int i = 0;  // index of j among the union tiles
   if (ok && j < p.n_tiles) {
     ok = wait_full(0);
     tc_fence_after();
     if (ok) {
-      if (tile_active(p, qt0, j)) { issue_s(0, 0); mma_commit(bar(C::kBarS + 0)); }
-      if (tile_active(p, qt1, j)) { issue_s(1, 0); mma_commit(bar(C::kBarS + 1)); }
+      if (plan.active(0, j)) { issue_s(0, 0); mma_commit(bar(C::kBarS + 0)); }
+      if (plan.active(1, j)) { issue_s(1, 0); mma_commit(bar(C::kBarS + 1)); }
       mma_commit(bar(C::kBarEmpty + 0));
     }
   }
   while (ok && j < p.n_tiles) {
-    const bool a0 = tile_active(p, qt0, j), a1 = tile_active(p, qt1, j);
-    const int jn = next_union(p, qt0, qt1, j + 1);
+    const bool a0 = plan.active(0, j), a1 = plan.active(1, j);
+    const int jn = plan.next(j + 1);
     const bool has_next = jn < p.n_tiles;
     const int kpos = 2 * i + 1;                      // K(u_{i+1})
     const int vpos = has_next ? 2 * i + 2 : 2 * i + 1;  // V(u_i)
     const int sv = vpos % C::kStages, skn = kpos % C::kStages;
     if (!wait_full(vpos)) { ok = false; break; }
     tc_fence_after();
-    const bool n0 = has_next && tile_active(p, qt0, jn);
-    const bool n1 = has_next && tile_active(p, qt1, jn);
+    const bool n0 = has_next && plan.active(0, jn);
+    const bool n1 = has_next && plan.active(1, jn);
 
     if (a0) {
       if (!mbar_wait_warp(bar(C::kBarP + 0), pphase[0], ctl)) { ok = false; break; }
@@ -267,8 +289,10 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
   bool any = false;
   uint32_t sphase = 0;
   bool ok = true;
-  for (int j = 0; j < p.n_tiles; ++j) {
-    if (!tile_active(p, qt, j)) continue;
+  const TilePlan plan = make_plan(p, qt0, qt1);
+  const int last = t ? plan.last1 : plan.last0;
+  for (int j = 0; j <= last; ++j) {
+    if (!plan.active(t, j)) continue;
     if (!mbar_wait(bar(C::kBarS + t), sphase, ctl)) { ok = false; break; }
     sphase ^= 1;
     tc_fence_after();

@@ -65,17 +65,27 @@ struct Cfg {
   __device__ static constexpr uint32_t col_s(int b) { return 128u + 128u * b; }
 };
 
-__device__ __forceinline__ bool tile_active(const FwdParams& p, int qt, int j) {
-  if (p.mode == kCausal) return j <= qt;
-  if (p.mode == kBlockSparse) return __ldg(p.block_mask + static_cast<size_t>(qt) * p.n_tiles + j) != 0;
-  return true;
-}
+// Key tiles visited by this CTA's query tile, resolved once per role: dense and causal query
+// tiles need key tiles [0, last]; block-sparse ones additionally look up their row of the tile
+// mask. Kept in registers so that the per-tile bookkeeping stays a few integer compares.
+struct TilePlan {
+  const uint8_t* mask;  // block-sparse: the query tile's row of the tile mask, else null
+  int last, n_tiles;
+  // next key tile >= j this query tile needs, or n_tiles
+  __device__ __forceinline__ int next(int j) const {
+    if (mask == nullptr) return j <= last ? j : n_tiles;
+    for (; j < n_tiles; ++j)
+      if (__ldg(mask + j) != 0) return j;
+    return n_tiles;
+  }
+};
 
-// next key tile >= j this query tile needs, or n_tiles
-__device__ __forceinline__ int next_tile(const FwdParams& p, int qt, int j) {
-  for (; j < p.n_tiles; ++j)
-    if (tile_active(p, qt, j)) return j;
-  return p.n_tiles;
+__device__ __forceinline__ TilePlan make_plan(const FwdParams& p, int qt) {
+  TilePlan t;
+  t.n_tiles = p.n_tiles;
+  t.last = p.mode == kCausal ? qt : p.n_tiles - 1;
+  t.mask = p.mode == kBlockSparse ? p.block_mask + static_cast<size_t>(qt) * p.n_tiles : nullptr;
+  return t;
 }
 
 // CTA -> (head, query tile). Heads are taken in groups small enough for their K/V to stay in
@@ -122,12 +132,13 @@ __device__ void producer(const FwdParams& p, uint32_t sbase, const Ctl& ctl, int
     ++pos;
     return true;
   };
-  int j = next_tile(p, qt, 0);
-  int j1 = j < p.n_tiles ? next_tile(p, qt, j + 1) : p.n_tiles;
+  const TilePlan plan = make_plan(p, qt);
+  int j = plan.next(0);
+  int j1 = j < p.n_tiles ? plan.next(j + 1) : p.n_tiles;
   if (j < p.n_tiles) ok = load(&p.tm_k, j);
   if (ok && j1 < p.n_tiles) ok = load(&p.tm_k, j1);
   while (ok && j < p.n_tiles) {
-    const int j2 = j1 < p.n_tiles ? next_tile(p, qt, j1 + 1) : p.n_tiles;
+    const int j2 = j1 < p.n_tiles ? plan.next(j1 + 1) : p.n_tiles;
     if (j2 < p.n_tiles && !(ok = load(&p.tm_k, j2))) break;
     if (!(ok = load(&p.tm_v, j))) break;
     j = j1;
@@ -175,8 +186,9 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
   auto release = [&](int ps) { mma_commit(bar(C::kBarEmpty + ps % C::kStages)); };
 
   bool ok = mbar_wait_warp(bar(C::kBarQ), 0, ctl);
-  int j = next_tile(p, qt, 0);
-  int j1 = j < p.n_tiles ? next_tile(p, qt, j + 1) : p.n_tiles;
+  const TilePlan plan = make_plan(p, qt);
+  int j = plan.next(0);
+  int j1 = j < p.n_tiles ? plan.next(j + 1) : p.n_tiles;
   int pos = 0;
   for (int b = 0; b < 2 && ok; ++b) {  // S of the first two tiles
     if ((b ? j1 : j) >= p.n_tiles) break;
@@ -189,7 +201,7 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
   uint32_t pph[2] = {0, 0};
   for (int i = 0; ok && j < p.n_tiles; ++i) {
     const int buf = i & 1;
-    const int j2 = j1 < p.n_tiles ? next_tile(p, qt, j1 + 1) : p.n_tiles;
+    const int j2 = j1 < p.n_tiles ? plan.next(j1 + 1) : p.n_tiles;
     const int kpos = j2 < p.n_tiles ? pos++ : -1;  // K(u_{i+2})
     const int vpos = pos++;                         // V(u_i)
     // O += P_i V_i once the softmax has written P_i over S buffer `buf`
@@ -241,7 +253,8 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
   int i = 0;  // tiles processed
   uint32_t sph[2] = {0, 0};
   bool ok = true;
-  for (int j = next_tile(p, qt, 0); j < p.n_tiles; j = next_tile(p, qt, j + 1), ++i) {
+  const TilePlan plan = make_plan(p, qt);
+  for (int j = plan.next(0); j < p.n_tiles; j = plan.next(j + 1), ++i) {
     const int buf = i & 1;
     const uint32_t tS = tmem + lane_off + C::col_s(buf);
     if (!mbar_wait(bar(C::kBarS + buf), sph[buf], ctl)) { ok = false; break; }
