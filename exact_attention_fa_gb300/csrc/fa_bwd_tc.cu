@@ -127,9 +127,9 @@ __device__ __forceinline__ void decode_bwd(const BwdParams& p, int group, int& b
   bh = g * group + within % gsize;
 }
 
-// TMEM column holding the packed bf16 pair of queries (16k, 16k+1) of the P^T / dS^T operand:
-// the warpgroup owning query columns [64c, 64c+64) packs them into columns [64c, 64c+32).
-__device__ __forceinline__ uint32_t packed_col(int k) { return k < 4 ? 8u * k : 64u + 8u * (k - 4); }
+// P^T / dS^T as the TMEM operand of dV / dK: the warpgroup owning query columns [64c, 64c+64)
+// packs them as bf16 pairs into columns [64c, 64c+32), so K-step k (queries 16k .. 16k+15) reads
+// the 8 columns at k < 4 ? 8k : 64 + 8(k - 4) (mma_ts_k128_halves).
 
 template <int D>
 __device__ void bwd_producer(const BwdParams& p, uint32_t sbase, const Ctl& ctl, int bh, int j,
@@ -185,25 +185,33 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
 
   bool ok = mbar_wait_poll_warp(bar(C::kBarKV), 0, ctl);
   tc_fence_after();
-  // Descriptor halves precomputed once; each MMA only adds a constant K-step offset.
+  // Descriptors precomputed once; each MMA only adds a constant K-step offset (lean issue: the
+  // MMA warp shares its SM sub-partition with busy compute warps).
   constexpr uint32_t kHi = sdesc_hi_sw128(1024);
-  const uint32_t k_km = sdesc_lo(sbase + C::kOffK, 16);          // K as A of S^T (K-major)
-  const uint32_t v_km = sdesc_lo(sbase + C::kOffV, 16);          // V as A of dP^T (K-major)
-  const uint32_t k_mn = sdesc_lo(sbase + C::kOffK, kBoxBytes);   // K as B of dQ (MN-major)
-  const uint32_t ds_mn = sdesc_lo(sbase + C::kOffDS, kBoxBytes); // dS as A of dQ (MN-major)
-  const uint32_t st_km = sdesc_lo(sbase + C::kOffStage, 16);     // Q_i / dO_i, K-major
-  const uint32_t st_mn = sdesc_lo(sbase + C::kOffStage, kBoxBytes);  // Q_i / dO_i, MN-major
-  constexpr uint32_t kStageStep = C::kStageBytes >> 4;
-  constexpr uint32_t kDOOff = C::kStageDO >> 4;
+  constexpr int kSteps = D / 16;
+  uint64_t a_k[kSteps], a_v[kSteps];  // K, V as the K-major A operand of S^T / dP^T per K-step
+#pragma unroll
+  for (int k = 0; k < kSteps; ++k) {
+    const uint32_t off = (k / 4) * kBoxBytes + (k % 4) * 32;
+    a_k[k] = sdesc64(sdesc_lo(sbase + C::kOffK + off, 16), kHi);
+    a_v[k] = sdesc64(sdesc_lo(sbase + C::kOffV + off, 16), kHi);
+  }
+  const uint64_t k_mn = sdesc64(sdesc_lo(sbase + C::kOffK, kBoxBytes), kHi);    // K, MN-major
+  const uint64_t ds_mn = sdesc64(sdesc_lo(sbase + C::kOffDS, kBoxBytes), kHi);  // dS, MN-major
+  const uint64_t st_km = sdesc64(sdesc_lo(sbase + C::kOffStage, 16), kHi);       // Q_i / dO_i
+  const uint64_t st_mn = sdesc64(sdesc_lo(sbase + C::kOffStage, kBoxBytes), kHi);
+  constexpr uint64_t kStageStep = C::kStageBytes >> 4;
+  constexpr uint64_t kDOOff = C::kStageDO >> 4;
   const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColDQ;
   const uint32_t tDV = tmem + C::kColDV, tDK = tmem + C::kColDK;
+  auto qk = [&](uint32_t d_tmem, const uint64_t (&a)[kSteps], uint64_t b) {
+    if constexpr (D == 128)
+      mma_qk_d128(d_tmem, a, b, kIdescT);
+    else
+      mma_qk_d64(d_tmem, a, b, kIdescT);
+  };
   auto issue_s = [&](int it) {  // S^T = K Q_i^T
-    const uint32_t q_km = st_km + (it % C::kStages) * kStageStep;
-#pragma unroll
-    for (int k = 0; k < D / 16; ++k) {
-      const uint32_t off = ((k / 4) * kBoxBytes + (k % 4) * 32) >> 4;
-      mma_ss2(tS, k_km + off, q_km + off, kHi, kIdescT, k > 0 ? 1u : 0u);
-    }
+    qk(tS, a_k, st_km + (it % C::kStages) * kStageStep);
     mma_commit(bar(C::kBarS));
   };
   if (ok && i0 < p.n_tiles) {
@@ -211,31 +219,25 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
     tc_fence_after();
     if (ok) issue_s(0);
   }
-  for (int i = i0, it = 0; ok && i < p.n_tiles; ++i, ++it) {
+  const int n_tiles = p.n_tiles;
+  for (int i = i0, it = 0; ok && i < n_tiles; ++i, ++it) {
     const int st = it % C::kStages;
-    const uint32_t q_mn = st_mn + st * kStageStep;
-    const uint32_t do_km = st_km + st * kStageStep + kDOOff, do_mn = q_mn + kDOOff;
+    const uint64_t q_mn = st_mn + st * kStageStep;
+    const uint64_t do_km = st_km + st * kStageStep + kDOOff, do_mn = q_mn + kDOOff;
     // dP^T = V dO_i^T (when dQ shares these columns, only after the previous dQ_i was drained)
     if (C::kDQAliasesDP && it > 0) {
       if (!mbar_wait_poll_warp(bar(C::kBarDQEmpty), (it - 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
     }
-#pragma unroll
-    for (int k = 0; k < D / 16; ++k) {
-      const uint32_t off = ((k / 4) * kBoxBytes + (k % 4) * 32) >> 4;
-      mma_ss2(tDP, v_km + off, do_km + off, kHi, kIdescT, k > 0 ? 1u : 0u);
-    }
+    qk(tDP, a_v, do_km);
     mma_commit(bar(C::kBarDP));
     // dV += P^T dO_i
     if (!mbar_wait_poll_warp(bar(C::kBarP), it & 1, ctl)) { ok = false; break; }
     tc_fence_after();
-#pragma unroll
-    for (int k = 0; k < BT / 16; ++k)
-      mma_ts2(tDV, tS + packed_col(k), do_mn + ((k * 2048) >> 4), kHi, kIdescG,
-              (it > 0 || k > 0) ? 1u : 0u);
+    mma_ts_k128_halves(tDV, tS, do_mn, kIdescG, it > 0 ? 1u : 0u);
     // S^T of the next query tile overwrites P^T: the tensor core runs MMAs in issue order, so
     // the dV product above has read P^T first; the compute warps overlap it with dK, dQ below.
-    if (i + 1 < p.n_tiles) {
+    if (i + 1 < n_tiles) {
       const int nx = it + 1;
       if (!mbar_wait_poll_warp(bar(C::kBarFull + nx % C::kStages), (nx / C::kStages) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
@@ -244,29 +246,17 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
     // dK += dS^T Q_i ; dQ_i = dS K
     if (!mbar_wait_poll_warp(bar(C::kBarDS), it & 1, ctl)) { ok = false; break; }
     tc_fence_after();
-#pragma unroll
-    for (int k = 0; k < BT / 16; ++k)
-      mma_ts2(tDK, tDP + packed_col(k), q_mn + ((k * 2048) >> 4), kHi, kIdescG,
-              (it > 0 || k > 0) ? 1u : 0u);
+    mma_ts_k128_halves(tDK, tDP, q_mn, kIdescG, it > 0 ? 1u : 0u);
     if (!C::kDQAliasesDP && it > 0) {
       if (!mbar_wait_poll_warp(bar(C::kBarDQEmpty), (it - 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
     }
-    if (C::kDQTransposed) {
-#pragma unroll
-      for (int k = 0; k < BT / 16; ++k)
-        mma_ss2(tDQ, k_mn + ((k * 2048) >> 4), ds_mn + ((k * 2048) >> 4), kHi, kIdescQT,
-                k > 0 ? 1u : 0u);
-      mma_commit(bar(C::kBarDQFull));
-      mma_commit(bar(C::kBarEmpty + st));  // Q_i, dO_i (and its lse2, D rows) are no longer read
-    } else {
-#pragma unroll
-      for (int k = 0; k < BT / 16; ++k)
-        mma_ss2(tDQ, ds_mn + ((k * 2048) >> 4), k_mn + ((k * 2048) >> 4), kHi, kIdescQ,
-                k > 0 ? 1u : 0u);
-      mma_commit(bar(C::kBarDQFull));
-      mma_commit(bar(C::kBarEmpty + st));
-    }
+    if (C::kDQTransposed)
+      mma_ss_k128_mn(tDQ, k_mn, ds_mn, kIdescQT);  // dQ_i^T = K^T dS^T
+    else
+      mma_ss_k128_mn(tDQ, ds_mn, k_mn, kIdescQ);   // dQ_i = dS K
+    mma_commit(bar(C::kBarDQFull));
+    mma_commit(bar(C::kBarEmpty + st));  // Q_i, dO_i (and its lse2, D rows) are no longer read
   }
   if (ok) {
     mma_commit(bar(C::kBarAcc));

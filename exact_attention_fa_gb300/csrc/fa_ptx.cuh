@@ -473,6 +473,43 @@ __device__ __forceinline__ void mma_pv_k128(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D (+)= A B over K = 128 with A read from TMEM at 8-column groups {0, 8, 16, 24, 64, 72, 80, 88}
+// (two 64-column halves, each packed into its first 32 columns) and B MN-major in shared memory
+// (+2 KB per K-step). `accumulate` applies to the first step; the rest accumulate.
+__device__ __forceinline__ void mma_ts_k128_halves(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                                   uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .pred p;\n\t.reg .b64 tb;\n\t.reg .b32 ta;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.s32 ta, %1, 8;\n\tadd.s64 tb, %2, 128;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 16;\n\tadd.s64 tb, %2, 256;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 24;\n\tadd.s64 tb, %2, 384;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 64;\n\tadd.s64 tb, %2, 512;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 72;\n\tadd.s64 tb, %2, 640;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 80;\n\tadd.s64 tb, %2, 768;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 88;\n\tadd.s64 tb, %2, 896;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, 1;\n\t"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D = A B over K = 128 with both operands MN-major in shared memory (+2 KB per K-step each).
+__device__ __forceinline__ void mma_ss_k128_mn(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                               uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .b64 ta, tb;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;\n\t"
+      "add.s64 ta, %1, 128;\n\tadd.s64 tb, %2, 128;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, 1;\n\t"
+      "add.s64 ta, %1, 256;\n\tadd.s64 tb, %2, 256;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, 1;\n\t"
+      "add.s64 ta, %1, 384;\n\tadd.s64 tb, %2, 384;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, 1;\n\t"
+      "add.s64 ta, %1, 512;\n\tadd.s64 tb, %2, 512;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, 1;\n\t"
+      "add.s64 ta, %1, 640;\n\tadd.s64 tb, %2, 640;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, 1;\n\t"
+      "add.s64 ta, %1, 768;\n\tadd.s64 tb, %2, 768;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, 1;\n\t"
+      "add.s64 ta, %1, 896;\n\tadd.s64 tb, %2, 896;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, 1;\n\t"
+      "}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc)
+      : "memory");
+}
 __host__ __device__ constexpr uint64_t sdesc64(uint32_t lo, uint32_t hi) {
   return (static_cast<uint64_t>(hi) << 32) | lo;
 }
