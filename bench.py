@@ -396,7 +396,7 @@ def run_ours(args):
         kname = f"bwd_tc_kernel<{w.d}> (+ bwd_prep_kernel<{w.d}> in the same call)"
         kflops, kms = f_bwd, t_bwd
     else:
-        kname = ("fwd_fp32_kernel" if w.dtype == "fp32" else "fwd_tc_kernel") + f"<{w.d}>"
+        kname = forward_kernel_name(w)
         kflops, kms = f_fwd, t_fwd
     achieved = kflops / (kms * 1e-3) / 1e12
     peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
@@ -430,6 +430,16 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def forward_kernel_name(w):
+    """Name of the forward kernel the library runs for this workload (the library picks the
+    two-query-tile kernel for dense / causal d = 64, the one-tile kernel otherwise)."""
+    if w.dtype == "fp32":
+        return f"fwd_fp32_kernel<{w.d}>"
+    if w.d == 64 and not w.block_sparse:
+        return f"fwd_pair_kernel<{w.d}>"
+    return f"fwd_tc_kernel<{w.d}>"
 
 
 def recorded_traffic(kname, w):
