@@ -47,14 +47,6 @@ constexpr int kThreads = 16 * 32;
 // whole 128-column row of dQ^T, at d = 64 it only stages 32 columns at a time and the compute
 // warpgroups take the difference.
 
-template <int N>
-__device__ __forceinline__ void regs_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void regs_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
 constexpr int kBoxBytes = 128 * 64 * 2;
 
 template <int D>

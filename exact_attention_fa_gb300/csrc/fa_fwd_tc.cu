@@ -270,15 +270,17 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
       for (int c = 0; c < 128; ++c)
         if (key0 + c >= lim) s[c] = __float_as_uint(-INFINITY);
     }
-    float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+    // row max: eight independent chains of 3-input max (short dependency chains)
+    float mxa[8];
 #pragma unroll
-    for (int c = 0; c < 128; c += 8) {
-      mx0 = max3(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
-      mx1 = max3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
-      mx2 = max3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
-      mx3 = max3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
-    }
-    const float mx = max3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
+    for (int u = 0; u < 8; ++u) mxa[u] = max3(-INFINITY, __uint_as_float(s[2 * u]), __uint_as_float(s[2 * u + 1]));
+#pragma unroll
+    for (int c = 16; c < 128; c += 16)
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        mxa[u] = max3(mxa[u], __uint_as_float(s[c + 2 * u]), __uint_as_float(s[c + 2 * u + 1]));
+    const float mx = max3(max3(mxa[0], mxa[1], mxa[2]), max3(mxa[3], mxa[4], mxa[5]),
+                          fmaxf(mxa[6], mxa[7])) * sl2;
 
     // Conditional rescaling (the FA4 idea of "3 · FlashAttention", 3.5): the reference max m
     // only moves when this tile's max exceeds it by more than kRescaleSlack (log2 units), so
@@ -314,7 +316,9 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
     const float m_use = m == -INFINITY ? 0.f : m;
     const unsigned long long k2 = f2_pack(sl2, sl2);
     const unsigned long long nm2 = f2_pack(-m_use, -m_use);
-    unsigned long long rs = f2_pack(0.f, 0.f);
+    unsigned long long rs[4];  // row sum in four independent packed chains
+#pragma unroll
+    for (int u = 0; u < 4; ++u) rs[u] = f2_pack(0.f, 0.f);
 #pragma unroll
     for (int c = 0; c < 128; c += 32) {
       uint32_t pk[16];
@@ -325,13 +329,13 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
         float x0, x1;
         f2_unpack(x, x0, x1);
         const float p0 = ex2(x0), p1 = ex2(x1);
-        rs = f2_add(rs, f2_pack(p0, p1));
+        rs[e & 3] = f2_add(rs[e & 3], f2_pack(p0, p1));
         pk[e] = pack_bf16(p0, p1);
       }
       tmem_st16(tS + c / 2, pk);
     }
     float rs0, rs1;
-    f2_unpack(rs, rs0, rs1);
+    f2_unpack(f2_add(f2_add(rs[0], rs[1]), f2_add(rs[2], rs[3])), rs0, rs1);
     l += rs0 + rs1;
     tmem_st_wait();
     tc_fence_before();

@@ -148,6 +148,18 @@ __device__ __forceinline__ bool mbar_wait_poll_warp(uint32_t bar, uint32_t parit
   return __all_sync(0xffffffffu, mbar_wait_poll(bar, parity, ctl));
 }
 
+// Per-warpgroup register budgets (executed by all warps of a warpgroup): a warpgroup that needs
+// few registers gives them back, one that needs many takes them. The sum over the CTA's
+// warpgroups must stay within what the launch allocated.
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------------------------------
 // TMA (bulk tensor copies global -> shared, completion counted in bytes on an mbarrier)
 // ------------------------------------------------------------------------------------------
