@@ -206,30 +206,43 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
     qk(tS, a_k, st_km + (it % C::kStages) * kStageStep);
     mma_commit(bar(C::kBarS));
   };
+  // dP^T = V dO_i^T. When dQ has TMEM columns of its own (d = 64), dP^T of the next query tile is
+  // issued at the end of this tile's products (dK has read dS^T out of these columns, dQ has read
+  // the dS tile), so that the compute warps find it ready when they finish P^T; when dQ_i^T
+  // reuses the columns (d = 128), only after dQ_i^T was drained.
+  constexpr bool kEarlyDP = !C::kDQAliasesDP;
+  auto issue_dp = [&](int it) {
+    qk(tDP, a_v, st_km + (it % C::kStages) * kStageStep + kDOOff);
+    mma_commit(bar(C::kBarDP));
+  };
   if (ok && i0 < p.n_tiles) {
     ok = mbar_wait_poll_warp(bar(C::kBarFull + 0), 0, ctl);
     tc_fence_after();
-    if (ok) issue_s(0);
+    if (ok) {
+      issue_s(0);
+      if (kEarlyDP) issue_dp(0);
+    }
   }
   const int n_tiles = p.n_tiles;
   for (int i = i0, it = 0; ok && i < n_tiles; ++i, ++it) {
     const int st = it % C::kStages;
     const uint64_t q_mn = st_mn + st * kStageStep;
-    const uint64_t do_km = st_km + st * kStageStep + kDOOff, do_mn = q_mn + kDOOff;
-    // dP^T = V dO_i^T (when dQ shares these columns, only after the previous dQ_i was drained)
-    if (C::kDQAliasesDP && it > 0) {
-      if (!mbar_wait_poll_warp(bar(C::kBarDQEmpty), (it - 1) & 1, ctl)) { ok = false; break; }
-      tc_fence_after();
+    const uint64_t do_mn = q_mn + kDOOff;
+    if (!kEarlyDP) {
+      if (it > 0) {
+        if (!mbar_wait_poll_warp(bar(C::kBarDQEmpty), (it - 1) & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+      }
+      issue_dp(it);
     }
-    qk(tDP, a_v, do_km);
-    mma_commit(bar(C::kBarDP));
     // dV += P^T dO_i
     if (!mbar_wait_poll_warp(bar(C::kBarP), it & 1, ctl)) { ok = false; break; }
     tc_fence_after();
     mma_ts_k128_halves(tDV, tS, do_mn, kIdescG, it > 0 ? 1u : 0u);
     // S^T of the next query tile overwrites P^T: the tensor core runs MMAs in issue order, so
     // the dV product above has read P^T first; the compute warps overlap it with dK, dQ below.
-    if (i + 1 < n_tiles) {
+    const bool has_next = i + 1 < n_tiles;
+    if (has_next) {
       const int nx = it + 1;
       if (!mbar_wait_poll_warp(bar(C::kBarFull + nx % C::kStages), (nx / C::kStages) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
@@ -249,6 +262,9 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
       mma_ss_k128_mn(tDQ, ds_mn, k_mn, kIdescQ);   // dQ_i = dS K
     mma_commit(bar(C::kBarDQFull));
     mma_commit(bar(C::kBarEmpty + st));  // Q_i, dO_i (and its lse2, D rows) are no longer read
+    // Only after the dQ product: its completion (in issue order) is what lets the compute warps
+    // rewrite the dS tile in shared memory for the next query tile.
+    if (kEarlyDP && has_next) issue_dp(it + 1);
   }
   if (ok) {
     mma_commit(bar(C::kBarAcc));

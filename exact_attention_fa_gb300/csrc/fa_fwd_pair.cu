@@ -6,7 +6,7 @@
 // running row max m, running sum l and an unnormalised accumulator O rescaled by exp(m - m_new),
 // divide by l once at the end. Neither S nor P ever leaves the SM.
 //
-// GB300 mapping (one CTA per SM, 10 warps; used for dense / causal d = 64):
+// GB300 mapping (one CTA per SM, 12 warps; used for dense / causal d = 64):
 //   * a CTA owns two 128-row query tiles (t = 0, 1) of one (b, h), so the tensor core works on one
 //     tile's QK^T / PV while the other tile's softmax runs on the CUDA cores, and each K/V tile
 //     streamed from L2 serves 256 query rows;
@@ -35,7 +35,13 @@ constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per tile
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // warps 10-11 only complete the producer / MMA warpgroup
+// Registers per thread after the warpgroups re-balance the 168 each thread is launched with: the
+// softmax warpgroups hold a row of 128 scores plus the row statistics.
+constexpr int kRegsSoftmax = 208;
+constexpr int kRegsLoadMma = 88;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsLoadMma <= kThreads * 168,
+              "register split exceeds the launch's allocation");
 constexpr int kBoxBytes = 128 * 64 * 2;  // one TMA box: 128 rows x 64 bf16 (128 B rows)
 constexpr float kRescaleSlack = 8.f;     // log2 units: P stays <= 256
 
@@ -449,13 +455,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_pair_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kLoadWarp) {
-    producer<D>(p, sbase, ctl, bh, qt0, qt1);  // whole warp: one elected lane issues
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    mma_issuer<D>(p, sbase, tmem, ctl, qt0, qt1);  // whole warp: one elected lane issues
+  if (warp >= kLoadWarp) {
+    regs_dec<kRegsLoadMma>();
+    if (warp == kLoadWarp)
+      producer<D>(p, sbase, ctl, bh, qt0, qt1);  // whole warp: one elected lane issues
+    else if (warp == kMmaWarp)
+      mma_issuer<D>(p, sbase, tmem, ctl, qt0, qt1);  // whole warp: one elected lane issues
     __syncwarp();
   } else {
+    regs_inc<kRegsSoftmax>();
     softmax_wg<D>(p, sbase, tmem, ctl, bh, qt0, qt1);
   }
 
