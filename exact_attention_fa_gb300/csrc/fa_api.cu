@@ -226,7 +226,7 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   (void)d;
   if (B < 1 || H < 1 || N < 1) return 0;
   const size_t rows = static_cast<size_t>(B) * H * ((static_cast<size_t>(N) + 127) / 128) * 128;
-  return 2 * rows * sizeof(float);
+  return rows * (2 * sizeof(float) + 64);  // lse2, D; their two 32-byte operand rows
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
@@ -258,6 +258,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   const size_t rows = static_cast<size_t>(BH) * ((static_cast<size_t>(N) + 127) / 128) * 128;
   p.lse2 = static_cast<float*>(workspace);
   p.Dsum = static_cast<float*>(workspace) + rows;
+  p.aug = static_cast<uint8_t*>(workspace) + rows * 2 * sizeof(float);
   p.BH = BH;
   p.N = N;
   p.d = d;

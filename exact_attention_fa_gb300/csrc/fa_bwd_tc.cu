@@ -28,8 +28,6 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
-#include <type_traits>
-
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -53,16 +51,24 @@ template <int D>
 struct BCfg {
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kStages = D == 128 ? 2 : 3;
+  // d = 64 folds the row statistics into the S^T and dP^T products: one more K-step of 16 whose
+  // A operand is a constant tile of ones (columns 0-2) and whose B operand holds -lse2/scale_log2
+  // (for S^T) or -D (for dP^T) split into three bf16 parts, so that the products come out as
+  // scale_log2^-1 * (S scaled - lse2) and dP - D and the compute warps read no statistics from
+  // shared memory. d = 128 has no shared memory left for the operand tiles and reads lse2 / D.
+  static constexpr bool kAugStats = D == 64;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
   static constexpr int kOffDS = 2 * kTileBytes;           // 128 x 128 bf16, two 64-query boxes
   static constexpr int kOffStage = kOffDS + 2 * kBoxBytes;
-  // per stage: Q_i, dO_i, lse2[128], D[128]
+  // per stage: Q_i, dO_i, then lse2[128], D[128] (d = 128) or the two 4 KB operand tiles (d = 64)
   static constexpr int kStageQ = 0;
   static constexpr int kStageDO = kTileBytes;
   static constexpr int kStageLse = 2 * kTileBytes;
   static constexpr int kStageD = 2 * kTileBytes + 512;
-  static constexpr int kStageBytes = 2 * kTileBytes + 1024;
+  static constexpr int kStageQAug = 2 * kTileBytes;
+  static constexpr int kStageDOAug = 2 * kTileBytes + 4096;
+  static constexpr int kStageBytes = 2 * kTileBytes + (kAugStats ? 8192 : 1024);
   // d = 128 computes dQ_i^T = K^T dS^T (d on TMEM lanes, queries on columns): a warp then holds
   // 32 consecutive d of one query row, so the drain adds it into the fp32 output with coalesced
   // reductions straight from registers. d = 64 computes dQ_i (queries on lanes) and stages it
@@ -71,7 +77,8 @@ struct BCfg {
   static constexpr bool kDQTransposed = D == 128;
   static constexpr int kOffDQStage = kOffStage + kStages * kStageBytes;
   static constexpr int kDQStageBytes = kDQTransposed ? 0 : 128 * D * 4;
-  static constexpr int kOffBar = kOffDQStage + kDQStageBytes;
+  static constexpr int kOffOnes = kOffDQStage + kDQStageBytes;  // 4 KB constant A tile (d = 64)
+  static constexpr int kOffBar = kOffOnes + (kAugStats ? 4096 : 0);
   static constexpr int kBarKV = 0;
   static constexpr int kBarFull = 1;
   static constexpr int kBarEmpty = 1 + kStages;
@@ -146,14 +153,19 @@ __device__ void bwd_producer(const BwdParams& p, uint32_t sbase, const Ctl& ctl,
     const int round = it / C::kStages;
     if (!mbar_wait_warp(bar(C::kBarEmpty + st), (round & 1) ^ 1, ctl)) { ok = false; break; }
     const uint32_t sb = sbase + C::kOffStage + st * C::kStageBytes;
-    mbar_arrive_expect_tx(bar(C::kBarFull + st), 2 * C::kTileBytes + 1024);
+    mbar_arrive_expect_tx(bar(C::kBarFull + st), C::kStageBytes);
     for (int b = 0; b < D / 64; ++b) {
       tma_load_3d(sb + C::kStageQ + b * kBoxBytes, &p.tm_q, bar(C::kBarFull + st), b * 64, i * BT, bh);
       tma_load_3d(sb + C::kStageDO + b * kBoxBytes, &p.tm_do, bar(C::kBarFull + st), b * 64, i * BT, bh);
     }
-    const size_t r0 = static_cast<size_t>(bh) * npad + static_cast<size_t>(i) * BT;
-    tma_bulk_g2s(sb + C::kStageLse, p.lse2 + r0, 512, bar(C::kBarFull + st));
-    tma_bulk_g2s(sb + C::kStageD, p.Dsum + r0, 512, bar(C::kBarFull + st));
+    if constexpr (C::kAugStats) {
+      const uint8_t* aug = p.aug + (static_cast<size_t>(bh) * p.n_tiles + i) * 8192;
+      tma_bulk_g2s(sb + C::kStageQAug, aug, 8192, bar(C::kBarFull + st));
+    } else {
+      const size_t r0 = static_cast<size_t>(bh) * npad + static_cast<size_t>(i) * BT;
+      tma_bulk_g2s(sb + C::kStageLse, p.lse2 + r0, 512, bar(C::kBarFull + st));
+      tma_bulk_g2s(sb + C::kStageD, p.Dsum + r0, 512, bar(C::kBarFull + st));
+    }
     issued[st] = round;
   }
   if (!ok) {
@@ -202,8 +214,14 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
     else
       mma_qk_d64(d_tmem, a, b, kIdescT);
   };
-  auto issue_s = [&](int it) {  // S^T = K Q_i^T
+  const uint64_t ones = sdesc_none(sbase + C::kOffOnes, 128, 256);
+  auto aug_desc = [&](int it, int which) {  // the statistics tile of query tile `it`
+    return sdesc_none(sbase + C::kOffStage + (it % C::kStages) * C::kStageBytes +
+                          (which ? C::kStageDOAug : C::kStageQAug), 128, 256);
+  };
+  auto issue_s = [&](int it) {  // S^T = K Q_i^T (d = 64: minus lse2 / scale_log2)
     qk(tS, a_k, st_km + (it % C::kStages) * kStageStep);
+    if constexpr (C::kAugStats) mma_ss(tS, ones, aug_desc(it, 0), kIdescT, 1u);
     mma_commit(bar(C::kBarS));
   };
   // dP^T = V dO_i^T. When dQ has TMEM columns of its own (d = 64), dP^T of the next query tile is
@@ -211,8 +229,9 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
   // the dS tile), so that the compute warps find it ready when they finish P^T; when dQ_i^T
   // reuses the columns (d = 128), only after dQ_i^T was drained.
   constexpr bool kEarlyDP = !C::kDQAliasesDP;
-  auto issue_dp = [&](int it) {
+  auto issue_dp = [&](int it) {  // (d = 64: minus D)
     qk(tDP, a_v, st_km + (it % C::kStages) * kStageStep + kDOOff);
+    if constexpr (C::kAugStats) mma_ss(tDP, ones, aug_desc(it, 1), kIdescT, 1u);
     mma_commit(bar(C::kBarDP));
   };
   if (ok && i0 < p.n_tiles) {
@@ -277,6 +296,52 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
   }
 }
 
+// P^T for one compute thread's 64 query columns of its key row, in two 32-column chunks: scores
+// from TMEM, exp2(S * scale * log2e - lse2) with the row statistics read four at a time from
+// shared memory and the arithmetic on packed fp32 pairs; P kept in pv (fp32) for dS and written
+// back as packed bf16 over the first 32 of the 64 score columns. kMasked: columns x < lim are 0.
+template <bool kMasked, bool kAug>
+__device__ __forceinline__ void bwd_p_tile(uint32_t tS, const float4* lse4, unsigned long long k2,
+                                           int lim, float (&pv)[64]) {
+#pragma unroll
+  for (int ch = 0; ch < 2; ++ch) {
+    uint32_t s[32];
+    tmem_ld32(tS + 32 * ch, s);
+    uint32_t pk[16];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int x0 = 32 * ch + 4 * u;
+      float a0, a1, a2, a3;
+      if constexpr (kAug) {  // the scores already carry -lse2 / scale_log2
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(s[4 * u]), __uint_as_float(s[4 * u + 1])), k2),
+                  a0, a1);
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(s[4 * u + 2]), __uint_as_float(s[4 * u + 3])), k2),
+                  a2, a3);
+      } else {
+        const float4 L = lse4[8 * ch + u];
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * u]), __uint_as_float(s[4 * u + 1])), k2,
+                         f2_pack(-L.x, -L.y)), a0, a1);
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * u + 2]), __uint_as_float(s[4 * u + 3])), k2,
+                         f2_pack(-L.z, -L.w)), a2, a3);
+      }
+      float p0 = ex2(a0), p1 = ex2(a1), p2 = ex2(a2), p3 = ex2(a3);
+      if constexpr (kMasked) {
+        p0 = x0 < lim ? 0.f : p0;
+        p1 = x0 + 1 < lim ? 0.f : p1;
+        p2 = x0 + 2 < lim ? 0.f : p2;
+        p3 = x0 + 3 < lim ? 0.f : p3;
+      }
+      pv[x0] = p0;
+      pv[x0 + 1] = p1;
+      pv[x0 + 2] = p2;
+      pv[x0 + 3] = p3;
+      pk[2 * u] = pack_bf16(p0, p1);
+      pk[2 * u + 1] = pack_bf16(p2, p3);
+    }
+    tmem_st16(tS + 16 * ch, pk);
+  }
+}
+
 template <int D>
 __device__ void bwd_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, uint32_t tmem,
                             const Ctl& ctl, int bh, int j, int i0) {
@@ -316,45 +381,14 @@ __device__ void bwd_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, u
     const float4* lse4 = reinterpret_cast<const float4*>(lse2);
     const unsigned long long k2 = f2_pack(sl2, sl2);
     float pv[64];
-    auto p_phase = [&](auto masked) {
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t s[32];
-        tmem_ld32(tS + 32 * ch, s);
-        uint32_t pk[16];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float4 L = lse4[8 * ch + u];
-          const int x0 = 32 * ch + 4 * u;
-          float a0, a1, a2, a3;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * u]), __uint_as_float(s[4 * u + 1])), k2,
-                           f2_pack(-L.x, -L.y)), a0, a1);
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * u + 2]), __uint_as_float(s[4 * u + 3])), k2,
-                           f2_pack(-L.z, -L.w)), a2, a3);
-          float p0 = ex2(a0), p1 = ex2(a1), p2 = ex2(a2), p3 = ex2(a3);
-          if constexpr (decltype(masked)::value) {
-            p0 = x0 < lim ? 0.f : p0;
-            p1 = x0 + 1 < lim ? 0.f : p1;
-            p2 = x0 + 2 < lim ? 0.f : p2;
-            p3 = x0 + 3 < lim ? 0.f : p3;
-          }
-          pv[x0] = p0;
-          pv[x0 + 1] = p1;
-          pv[x0 + 2] = p2;
-          pv[x0 + 3] = p3;
-          pk[2 * u] = pack_bf16(p0, p1);
-          pk[2 * u + 1] = pack_bf16(p2, p3);
-        }
-        tmem_st16(tS + 16 * ch, pk);
-      }
-    };
     if constexpr (D == 64) {
       if (__any_sync(0xffffffffu, lim > 0))
-        p_phase(std::true_type{});
+        bwd_p_tile<true, C::kAugStats>(tS, lse4, k2, lim, pv);
       else
-        p_phase(std::false_type{});
+        bwd_p_tile<false, C::kAugStats>(tS, lse4, k2, lim, pv);
     } else {
-      p_phase(std::true_type{});  // a single code path measured faster at d = 128
+      // a single code path measured faster at d = 128
+      bwd_p_tile<true, C::kAugStats>(tS, lse4, k2, lim, pv);
     }
     tmem_st_wait();
     tc_fence_before();
@@ -370,15 +404,24 @@ __device__ void bwd_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, u
       uint32_t pk[16];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {  // dS = P * (dP - D)
-        const float4 Dv = d4[8 * ch + u];
         const int x0 = 32 * ch + 4 * u;
         float d0, d1, d2, d3;
-        f2_unpack(f2_mul(f2_pack(pv[x0], pv[x0 + 1]),
-                         f2_add(f2_pack(__uint_as_float(dp[4 * u]), __uint_as_float(dp[4 * u + 1])),
-                                f2_pack(-Dv.x, -Dv.y))), d0, d1);
-        f2_unpack(f2_mul(f2_pack(pv[x0 + 2], pv[x0 + 3]),
-                         f2_add(f2_pack(__uint_as_float(dp[4 * u + 2]), __uint_as_float(dp[4 * u + 3])),
-                                f2_pack(-Dv.z, -Dv.w))), d2, d3);
+        if constexpr (C::kAugStats) {  // the product already carries -D
+          f2_unpack(f2_mul(f2_pack(pv[x0], pv[x0 + 1]),
+                           f2_pack(__uint_as_float(dp[4 * u]), __uint_as_float(dp[4 * u + 1]))),
+                    d0, d1);
+          f2_unpack(f2_mul(f2_pack(pv[x0 + 2], pv[x0 + 3]),
+                           f2_pack(__uint_as_float(dp[4 * u + 2]), __uint_as_float(dp[4 * u + 3]))),
+                    d2, d3);
+        } else {
+          const float4 Dv = d4[8 * ch + u];
+          f2_unpack(f2_mul(f2_pack(pv[x0], pv[x0 + 1]),
+                           f2_add(f2_pack(__uint_as_float(dp[4 * u]), __uint_as_float(dp[4 * u + 1])),
+                                  f2_pack(-Dv.x, -Dv.y))), d0, d1);
+          f2_unpack(f2_mul(f2_pack(pv[x0 + 2], pv[x0 + 3]),
+                           f2_add(f2_pack(__uint_as_float(dp[4 * u + 2]), __uint_as_float(dp[4 * u + 3])),
+                                  f2_pack(-Dv.z, -Dv.w))), d2, d3);
+        }
         pk[2 * u] = pack_bf16(d0, d1);
         pk[2 * u + 1] = pack_bf16(d2, d3);
       }
@@ -571,6 +614,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
+  if constexpr (C::kAugStats) {
+    // the constant A tile of the statistics K-step: 128 rows of [1, 1, 1, 0 ... 0] (16 bf16) in
+    // 8-row x 16-byte core matrices (the second core matrix of each row group is all zero)
+    if (threadIdx.x < 256) {
+      const int c = threadIdx.x;  // 16-byte chunk: row group c / 16, K half (c / 8) % 2, row c % 8
+      const uint4 v = ((c / 8) % 2 == 0) ? make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u)
+                                         : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(smem + C::kOffOnes + (c / 16) * 256 + ((c / 8) % 2) * 128 +
+                                (c % 8) * 16) = v;
+      fence_proxy_async_smem();  // read by the tensor core (async proxy)
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -645,7 +700,31 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ B
     if (valid && part == 0) {
       const bool in = q < p.N;
       p.Dsum[row] = in ? acc : 0.f;
-      p.lse2[row] = in ? p.lse[static_cast<size_t>(bh) * p.N + q] * 1.4426950408889634f : INFINITY;
+      const float l2 = in ? p.lse[static_cast<size_t>(bh) * p.N + q] * 1.4426950408889634f : INFINITY;
+      p.lse2[row] = l2;
+      if constexpr (D == 64) {
+        // the two 32-byte B-operand rows of the statistics K-step: -lse2 / scale_log2 and -D, each
+        // as three bf16 parts (hi + lo + lo2 carries ~24 bits) in columns 0-2, zeros elsewhere;
+        // row r of tile t sits in 8-row x 16-byte core matrices: (r / 8) * 256 + (r % 8) * 16
+        const size_t tile = row / 128;
+        const int r = static_cast<int>(row % 128);
+        uint8_t* base = p.aug + tile * 8192 + (r / 8) * 256 + (r % 8) * 16;
+        const float xs[2] = {-l2 / p.scale_log2, in ? -acc : 0.f};
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          const float x = xs[w];
+          const __nv_bfloat16 h = __float2bfloat16_rn(x);
+          const bool fin = isfinite(x);
+          const float rest = fin ? x - __bfloat162float(h) : 0.f;
+          const __nv_bfloat16 lo = __float2bfloat16_rn(rest);
+          const __nv_bfloat16 lo2 = __float2bfloat16_rn(fin ? rest - __bfloat162float(lo) : 0.f);
+          const uint32_t w0 = static_cast<uint32_t>(__bfloat16_as_ushort(h)) |
+                              (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16);
+          const uint32_t w1 = static_cast<uint32_t>(__bfloat16_as_ushort(lo2));
+          *reinterpret_cast<uint4*>(base + w * 4096) = make_uint4(w0, w1, 0u, 0u);
+          *reinterpret_cast<uint4*>(base + w * 4096 + 128) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
     }
   }
 }

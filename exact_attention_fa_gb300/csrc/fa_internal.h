@@ -54,6 +54,9 @@ struct BwdParams {
   __nv_bfloat16* dv;
   float* lse2;   // workspace: lse * log2(e) per row (+inf for rows >= N)
   float* Dsum;   // workspace: D_i = sum_k dO_ik O_ik
+  // workspace, d = 64: per 128-row tile two 4 KB bf16 operand tiles (128 rows x 16, K-major,
+  // no swizzle) holding -lse2 / scale_log2 and -D, each split into three bf16 parts
+  uint8_t* aug;
   int BH, N, d;
   int n_tiles;
   int causal;

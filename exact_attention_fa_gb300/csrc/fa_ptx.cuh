@@ -403,6 +403,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Descriptor of an operand without swizzle, K-major, in 8-row x 16-byte core matrices (128
+// contiguous bytes each): lbo = byte distance between the core matrices of one 8-row group that
+// are adjacent along K, sbo = byte distance between adjacent 8-row groups. Layout type 0.
+__device__ __forceinline__ uint64_t sdesc_none(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  return d;
+}
+
 // The same descriptor split in two 32-bit halves, so that the MMA issue loop only adds a
 // constant to the low half per K step (the issuing thread is on the tensor pipe's critical path).
 __device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {

@@ -73,8 +73,9 @@ int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, flo
                        int H, int N, int d, float scale, const uint8_t* block_mask,
                        fa_stream_t stream);
 
-/* Bytes of device workspace fa_bwd needs: two fp32 values per row of B*H*ceil(N/128)*128 rows
- * (rows padded to whole 128-row tiles). */
+/* Bytes of device workspace fa_bwd needs: 72 bytes per row of B*H*ceil(N/128)*128 rows (rows
+ * padded to whole 128-row tiles): two fp32 row statistics and two 32-byte bf16 operand rows made
+ * from them. */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
 /* Backward by recomputation ("3 · FlashAttention", 3.4; "FlashAttention：在线 softmax 与
@@ -99,7 +100,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
  * FA_NOALLOC_SCRATCH_BYTES array of device memory that every device holds from the moment the
  * library's module is loaded on it until the process exits. Problems whose
  * fa_bwd_workspace_bytes(B, H, N, d) exceeds that size are rejected with FA_ERR_SCRATCH_LIMIT
- * before anything is enqueued (4 MiB covers B*H*ceil(N/128)*128 <= 524288 rows).
+ * before anything is enqueued (4 MiB covers B*H*ceil(N/128)*128 <= 58240 rows).
  * Allocates nothing: no cudaMalloc/cudaFree or allocating library call. The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress, with that device current);
  * make that first call before any stream capture. All calls on a device share the one array and

@@ -89,8 +89,9 @@ def test_fp32_validation(lib):
 
 
 def test_bwd_validation_and_workspace(lib):
-    assert lib.fa_bwd_workspace_bytes(2, 3, 100, 64) == 2 * 2 * 3 * 128 * 4
-    assert lib.fa_bwd_workspace_bytes(1, 1, 256, 128) == 2 * 256 * 4
+    # 72 bytes per padded row: lse2 and D (fp32) plus their two 32-byte bf16 operand rows
+    assert lib.fa_bwd_workspace_bytes(2, 3, 100, 64) == 2 * 3 * 128 * 72
+    assert lib.fa_bwd_workspace_bytes(1, 1, 256, 128) == 256 * 72
     assert lib.fa_bwd_workspace_bytes(0, 3, 100, 64) == 0
     ptrs = [fake()] * 9
     assert lib.fa_bwd(*ptrs, 1, 1, 128, 64, 0.125, 1, P(0), None) == 1
