@@ -143,7 +143,7 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
   fa::FwdParams p{};
   const int BH = B * H;
   if (!encode_bf16_map(&p.tm_q, q, BH, N, d) || !encode_bf16_map(&p.tm_k, k, BH, N, d) ||
-      !encode_bf16_map(&p.tm_v, v, BH, N, d))
+      !encode_bf16_map(&p.tm_v, v, BH, N, d) || !encode_bf16_map(&p.tm_o, o, BH, N, d))
     return FA_ERR_CUDA;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;

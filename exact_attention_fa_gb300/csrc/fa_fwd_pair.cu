@@ -276,8 +276,8 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
 
 // ---------------------------------------------------------------------------------------------
 template <int D>
-__device__ void softmax_wg(const FwdParams& p, uint32_t sbase, uint32_t tmem, const Ctl& ctl,
-                           int bh, int qt0, int qt1) {
+__device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, uint32_t tmem,
+                           const Ctl& ctl, int bh, int qt0, int qt1) {
   using C = Cfg<D>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -381,28 +381,41 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
     mbar_arrive(bar(C::kBarP + t));
   }
 
-  if (!ok) return;
+  // Every warp of the softmax warpgroup gets here; they agree on failures before the epilogue's
+  // named barrier.
+  if (bar_red_or(1 + t, 128, !ok)) return;
   const size_t grow = static_cast<size_t>(bh) * p.N + row;
   if (any) {
-    if (!mbar_wait(bar(C::kBarO + t), 0, ctl)) return;
+    const bool bad = !mbar_wait(bar(C::kBarO + t), 0, ctl);
+    if (bar_red_or(1 + t, 128, bad)) return;
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
+    // O / l as bf16 into this tile's Q buffer (free: every MMA has completed), 128-byte swizzled
+    // like the TMA boxes; one thread then stores the tile with the TMA (rows past N are clipped).
+    uint8_t* srow = smem + C::kOffQ + t * C::kTileBytes + r * 128;
 #pragma unroll 1
     for (int c = 0; c < D; c += 32) {
       uint32_t o[32];
       tmem_ld32(tO + c, o);
-      if (row < p.N) {
-        uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D + c);
+      uint8_t* box = srow + (c / 64) * kBoxBytes;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint4 w;
-          w.x = pack_bf16(__uint_as_float(o[8 * i + 0]) * inv, __uint_as_float(o[8 * i + 1]) * inv);
-          w.y = pack_bf16(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv);
-          w.z = pack_bf16(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv);
-          w.w = pack_bf16(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv);
-          dst[i] = w;
-        }
+      for (int e = 0; e < 4; ++e) {
+        uint4 w;
+        w.x = pack_bf16(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
+        w.y = pack_bf16(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
+        w.z = pack_bf16(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
+        w.w = pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
+        const int chunk = (c % 64) / 8 + e;
+        *reinterpret_cast<uint4*>(box + ((chunk ^ (r & 7)) << 4)) = w;
       }
+    }
+    fence_proxy_async_smem();
+    bar_sync(1 + t, 128);
+    if (threadIdx.x == 128 * t) {
+      for (int b = 0; b < D / 64; ++b)
+        tma_store_3d(&p.tm_o, sbase + C::kOffQ + t * C::kTileBytes + b * kBoxBytes, b * 64, qt * BM, bh);
+      bulk_commit();
+      bulk_wait_all();
     }
     if (row < p.N)
       p.lse[grow] = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
@@ -464,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_pair_kernel(const __grid_cons
     __syncwarp();
   } else {
     regs_inc<kRegsSoftmax>();
-    softmax_wg<D>(p, sbase, tmem, ctl, bh, qt0, qt1);
+    softmax_wg<D>(p, smem, sbase, tmem, ctl, bh, qt0, qt1);
   }
 
   tc_fence_before();

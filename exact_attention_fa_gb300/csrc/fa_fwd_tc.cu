@@ -238,8 +238,8 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
 
 // ---------------------------------------------------------------------------------------------
 template <int D>
-__device__ void softmax_wg(const FwdParams& p, uint32_t sbase, uint32_t tmem, const Ctl& ctl,
-                           int bh, int qt) {
+__device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, uint32_t tmem,
+                           const Ctl& ctl, int bh, int qt) {
   using C = Cfg<D>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -342,28 +342,41 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
     mbar_arrive(bar(C::kBarP + buf));
   }
 
-  if (!ok) return;
+  // Every warp of the softmax warpgroup gets here; they agree on failures before the epilogue's
+  // named barrier.
+  if (bar_red_or(1, 128, !ok)) return;
   const size_t grow = static_cast<size_t>(bh) * p.N + row;
   if (i > 0) {
-    if (!mbar_wait(bar(C::kBarO), 0, ctl)) return;
+    const bool bad = !mbar_wait(bar(C::kBarO), 0, ctl);
+    if (bar_red_or(1, 128, bad)) return;
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
+    // O / l as bf16 into this tile's Q buffer (free: every MMA has completed), 128-byte swizzled
+    // like the TMA boxes; one thread then stores the tile with the TMA (rows past N are clipped).
+    uint8_t* srow = smem + C::kOffQ + r * 128;
 #pragma unroll 1
     for (int c = 0; c < D; c += 32) {
       uint32_t o[32];
       tmem_ld32(tO + c, o);
-      if (row < p.N) {
-        uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D + c);
+      uint8_t* box = srow + (c / 64) * kBoxBytes;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          uint4 w;
-          w.x = pack_bf16(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
-          w.y = pack_bf16(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
-          w.z = pack_bf16(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
-          w.w = pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
-          dst[e] = w;
-        }
+      for (int e = 0; e < 4; ++e) {
+        uint4 w;
+        w.x = pack_bf16(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
+        w.y = pack_bf16(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
+        w.z = pack_bf16(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
+        w.w = pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
+        const int chunk = (c % 64) / 8 + e;
+        *reinterpret_cast<uint4*>(box + ((chunk ^ (r & 7)) << 4)) = w;
       }
+    }
+    fence_proxy_async_smem();
+    bar_sync(1, 128);
+    if (threadIdx.x == 0) {
+      for (int b = 0; b < D / 64; ++b)
+        tma_store_3d(&p.tm_o, sbase + C::kOffQ + b * kBoxBytes, b * 64, qt * BM, bh);
+      bulk_commit();
+      bulk_wait_all();
     }
     if (row < p.N)
       p.lse[grow] = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
@@ -423,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     mma_issuer<D>(p, sbase, tmem, ctl, qt);  // whole warp: one elected lane issues
     __syncwarp();
   } else {
-    softmax_wg<D>(p, sbase, tmem, ctl, bh, qt);
+    softmax_wg<D>(p, smem, sbase, tmem, ctl, bh, qt);
   }
 
   tc_fence_before();

@@ -17,6 +17,7 @@ struct FwdParams {
   CUtensorMap tm_q;
   CUtensorMap tm_k;
   CUtensorMap tm_v;
+  CUtensorMap tm_o;  // the output, same view as tm_q (the epilogue stores O tiles with the TMA)
   __nv_bfloat16* o;
   float* lse;
   const uint8_t* block_mask;  // [n_tiles][n_tiles] or null

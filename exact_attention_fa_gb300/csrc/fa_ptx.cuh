@@ -181,6 +181,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint3
 
 // Bulk tensor reduction shared -> global: adds a swizzled fp32 shared-memory box into the tensor
 // (element-wise, performed at L2), tracked by the issuing thread's bulk async-group.
+// Tensor store shared -> global of one box (issued by a single thread; rows past the tensor's
+// extent are not written).
+__device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          map),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
 __device__ __forceinline__ void tma_reduce_add_3d(const void* map, uint32_t src, int c0, int c1,
                                                   int c2) {
   asm volatile(
