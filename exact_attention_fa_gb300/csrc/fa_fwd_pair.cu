@@ -52,20 +52,28 @@ struct Cfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-  // barriers: Q, full[S], empty[S], s_full[2], p_full[2], o_full[2], drain
+  // barriers: Q, full[S], empty[S], s_full[2], p_full[2], o_full[2], pv_done[2], drain
   static constexpr int kBarQ = 0;
   static constexpr int kBarFull = 1;
   static constexpr int kBarEmpty = 1 + kStages;
   static constexpr int kBarS = 1 + 2 * kStages;
   static constexpr int kBarP = kBarS + 2;
   static constexpr int kBarO = kBarP + 2;
-  static constexpr int kBarDrain = kBarO + 2;
+  static constexpr int kBarPV = kBarO + 2;
+  static constexpr int kBarDrain = kBarPV + 2;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffTmemPtr = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemPtr + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1 KB
+  // d = 64: P_t has TMEM columns of its own, so S_t of the next key tile can be computed while
+  // PV_t of this one still reads P_t (S 2 x 128, P 2 x 64, O 2 x 64 = 512 columns). d = 128 has
+  // no room and writes P_t over S_t.
+  static constexpr bool kSepP = D == 64;
   __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
-  __device__ static constexpr uint32_t col_o(int t) { return t ? 256u + D : 256u; }
+  __device__ static constexpr uint32_t col_p(int t) { return kSepP ? 256u + 64u * t : col_s(t); }
+  __device__ static constexpr uint32_t col_o(int t) {
+    return kSepP ? 384u + 64u * t : (t ? 256u + D : 256u);
+  }
 };
 
 // Key tiles visited by the two query tiles of a CTA, resolved once per role: dense and causal
@@ -198,8 +206,9 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
       mma_qk_d64(tmem + C::col_s(t), qd[t], kd0 + stage * kStageStep, kIdescQK);
   };
   auto issue_pv = [&](int t, int stage, bool acc) {
-    mma_pv_k128(tmem + C::col_o(t), tmem + C::col_s(t), vd0 + stage * kStageStep, kIdescPV,
+    mma_pv_k128(tmem + C::col_o(t), tmem + C::col_p(t), vd0 + stage * kStageStep, kIdescPV,
                 acc ? 1u : 0u);
+    if constexpr (C::kSepP) mma_commit(bar(C::kBarPV + t));
   };
 
   bool ok = mbar_wait_warp(bar(C::kBarQ), 0, ctl);
@@ -234,28 +243,47 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
     const bool n0 = has_next && plan.active(0, jn);
     const bool n1 = has_next && plan.active(1, jn);
 
-    if (a0) {
-      if (!mbar_wait_warp(bar(C::kBarP + 0), pphase[0], ctl)) { ok = false; break; }
-      pphase[0] ^= 1;
-      tc_fence_after();
-      issue_pv(0, sv, acc[0]);
-      acc[0] = true;
-    }
     if (has_next) {
       if (!wait_full(kpos)) { ok = false; break; }
       tc_fence_after();
     }
-    // S_0 of the next tile overwrites P_0 of this one: the tensor core runs MMAs in issue order,
-    // so the PV above has read P_0 before this write lands.
-    if (n0) { issue_s(0, skn); mma_commit(bar(C::kBarS + 0)); }
-    if (a1) {
-      if (!mbar_wait_warp(bar(C::kBarP + 1), pphase[1], ctl)) { ok = false; break; }
-      pphase[1] ^= 1;
-      tc_fence_after();
-      issue_pv(1, sv, acc[1]);
-      acc[1] = true;
+    if constexpr (C::kSepP) {
+      // S_t of the next tile first (the softmax warps start on it at once), then PV_t of this
+      // one, which reads P_t from its own columns.
+      bool fail = false;
+      for (int t = 0; t < 2; ++t) {
+        if (!(t ? a1 : a0)) {
+          if (t ? n1 : n0) { issue_s(t, skn); mma_commit(bar(C::kBarS + t)); }
+          continue;
+        }
+        if (!mbar_wait_warp(bar(C::kBarP + t), pphase[t], ctl)) { fail = true; break; }
+        pphase[t] ^= 1;
+        tc_fence_after();
+        if (t ? n1 : n0) { issue_s(t, skn); mma_commit(bar(C::kBarS + t)); }
+        issue_pv(t, sv, acc[t]);
+        acc[t] = true;
+      }
+      if (fail) { ok = false; break; }
+    } else {
+      if (a0) {
+        if (!mbar_wait_warp(bar(C::kBarP + 0), pphase[0], ctl)) { ok = false; break; }
+        pphase[0] ^= 1;
+        tc_fence_after();
+        issue_pv(0, sv, acc[0]);
+        acc[0] = true;
+      }
+      // S_0 of the next tile overwrites P_0 of this one: the tensor core runs MMAs in issue
+      // order, so the PV above has read P_0 before this write lands.
+      if (n0) { issue_s(0, skn); mma_commit(bar(C::kBarS + 0)); }
+      if (a1) {
+        if (!mbar_wait_warp(bar(C::kBarP + 1), pphase[1], ctl)) { ok = false; break; }
+        pphase[1] ^= 1;
+        tc_fence_after();
+        issue_pv(1, sv, acc[1]);
+        acc[1] = true;
+      }
+      if (n1) { issue_s(1, skn); mma_commit(bar(C::kBarS + 1)); }
     }
-    if (n1) { issue_s(1, skn); mma_commit(bar(C::kBarS + 1)); }
     if (has_next) mma_commit(bar(C::kBarEmpty + skn));
     mma_commit(bar(C::kBarEmpty + sv));
     ++i;
@@ -288,11 +316,13 @@ __device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, ui
   const int row = qt * BM + r;
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
   const uint32_t tS = tmem + lane_off + C::col_s(t);
+  const uint32_t tP = tmem + lane_off + C::col_p(t);
   const uint32_t tO = tmem + lane_off + C::col_o(t);
   const float sl2 = p.scale_log2;
 
   float m = -INFINITY, l = 0.f;
   bool any = false;
+  int n_done = 0;  // tiles of this query tile processed so far
   uint32_t sphase = 0;
   bool ok = true;
   const TilePlan plan = make_plan(p, qt0, qt1);
@@ -328,10 +358,21 @@ __device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, ui
     // Conditional rescaling (the FA4 idea of "3 · FlashAttention", 3.5): the reference max m
     // only moves when this tile's max exceeds it by more than kRescaleSlack (log2 units), so
     // P <= 2^kRescaleSlack and O, l are rescaled rarely. O = a / l is exact for any reference.
+    // Separate P columns: S of this tile may have landed before PV of the previous tile
+    // completed; O (for a rescale) and the P columns (before they are rewritten) need it first.
+    bool pv_ready = !C::kSepP || n_done == 0;
+    auto wait_pv = [&]() {
+      if (pv_ready) return true;
+      pv_ready = true;
+      const bool good = mbar_wait(bar(C::kBarPV + t), (n_done - 1) & 1, ctl);
+      tc_fence_after();
+      return good;
+    };
     if (__any_sync(~0u, mx > m + kRescaleSlack)) {
       const float m_new = fmaxf(m, mx);
       const float alpha = ex2(m - m_new);  // 0 when nothing was accumulated (m = -inf)
       if (any) {
+        if (!wait_pv()) { ok = false; break; }
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
           uint32_t o[32];
@@ -357,6 +398,7 @@ __device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, ui
     unsigned long long rs[4];  // row sum in four independent packed chains
 #pragma unroll
     for (int u = 0; u < 4; ++u) rs[u] = f2_pack(0.f, 0.f);
+    bool fail = false;
 #pragma unroll
     for (int c = 0; c < 128; c += 32) {
       uint32_t pk[16];
@@ -370,12 +412,15 @@ __device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, ui
         rs[i & 3] = f2_add(rs[i & 3], f2_pack(p0, p1));
         pk[i] = pack_bf16(p0, p1);
       }
-      tmem_st16(tS + c / 2, pk);
+      if (c == 0 && !wait_pv()) fail = true;
+      tmem_st16(tP + c / 2, pk);
     }
+    if (fail) { ok = false; break; }
     float rs0, rs1;
     f2_unpack(f2_add(f2_add(rs[0], rs[1]), f2_add(rs[2], rs[3])), rs0, rs1);
     l += rs0 + rs1;
     any = true;
+    ++n_done;
     tmem_st_wait();
     tc_fence_before();
     mbar_arrive(bar(C::kBarP + t));
@@ -454,6 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_pair_kernel(const __grid_cons
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::kBarS + t), 1);
       mbar_init(bar(C::kBarP + t), 128);
+      mbar_init(bar(C::kBarPV + t), 1);
       mbar_init(bar(C::kBarO + t), 1);
     }
     mbar_init(bar(C::kBarDrain), 1);
