@@ -98,6 +98,11 @@ struct BCfg {
   // d = 64 has room for dQ_i in its own columns; at d = 128 it reuses the dP^T columns.
   static constexpr bool kDQAliasesDP = D == 128;
   static constexpr uint32_t kColDQ = kDQAliasesDP ? kColDP : 256 + 2 * D;
+  // d = 64 also has room for dS^T (bf16 pairs, 64 columns) outside the dP^T columns, so dP^T of
+  // the next query tile can be computed while dK still reads this tile's dS^T. d = 128 packs
+  // dS^T over the dP^T columns it was computed from.
+  static constexpr bool kSepDS = D == 64;
+  static constexpr uint32_t kColDST = kSepDS ? 256 + 3 * D : kColDP;
   static constexpr int kRegsCompute = D == 128 ? 128 : 152;
   static constexpr int kRegsLoadMma = D == 128 ? 104 : 96;
   static constexpr int kRegsDrain = D == 128 ? 144 : 96;
@@ -224,10 +229,10 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
     if constexpr (C::kAugStats) mma_ss(tS, ones, aug_desc(it, 0), kIdescT, 1u);
     mma_commit(bar(C::kBarS));
   };
-  // dP^T = V dO_i^T. When dQ has TMEM columns of its own (d = 64), dP^T of the next query tile is
-  // issued at the end of this tile's products (dK has read dS^T out of these columns, dQ has read
-  // the dS tile), so that the compute warps find it ready when they finish P^T; when dQ_i^T
-  // reuses the columns (d = 128), only after dQ_i^T was drained.
+  // dP^T = V dO_i^T. At d = 64 (dQ and dS^T have TMEM columns of their own) dP^T of the next
+  // query tile is issued as soon as the compute warps have read this one, so that they find it
+  // ready when they finish P^T; at d = 128 (dQ_i^T reuses the columns) only after dQ_i^T was
+  // drained.
   constexpr bool kEarlyDP = !C::kDQAliasesDP;
   auto issue_dp = [&](int it) {  // (d = 64: minus D)
     qk(tDP, a_v, st_km + (it % C::kStages) * kStageStep + kDOOff);
@@ -270,7 +275,14 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
     // dK += dS^T Q_i ; dQ_i = dS K
     if (!mbar_wait_poll_warp(bar(C::kBarDS), it & 1, ctl)) { ok = false; break; }
     tc_fence_after();
-    mma_ts_k128_halves(tDK, tDP, q_mn, kIdescG, it > 0 ? 1u : 0u);
+    if constexpr (C::kSepDS) {
+      // dP^T of the next tile right away (its columns were read before the compute warps
+      // signalled dS); dS^T has columns of its own, 8 per K-step in order.
+      if (has_next) issue_dp(it + 1);
+      mma_pv_k128(tDK, tmem + C::kColDST, q_mn, kIdescG, it > 0 ? 1u : 0u);
+    } else {
+      mma_ts_k128_halves(tDK, tDP, q_mn, kIdescG, it > 0 ? 1u : 0u);
+    }
     if (!C::kDQAliasesDP && it > 0) {
       if (!mbar_wait_poll_warp(bar(C::kBarDQEmpty), (it - 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
@@ -281,9 +293,8 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
       mma_ss_k128_mn(tDQ, ds_mn, k_mn, kIdescQ);   // dQ_i = dS K
     mma_commit(bar(C::kBarDQFull));
     mma_commit(bar(C::kBarEmpty + st));  // Q_i, dO_i (and its lse2, D rows) are no longer read
-    // Only after the dQ product: its completion (in issue order) is what lets the compute warps
-    // rewrite the dS tile in shared memory for the next query tile.
-    if (kEarlyDP && has_next) issue_dp(it + 1);
+    // (d = 64: dP^T of the next tile was issued above; the compute warps wait for this tile's
+    // dQ product before they rewrite the dS tile and dS^T.)
   }
   if (ok) {
     mma_commit(bar(C::kBarAcc));
@@ -355,6 +366,7 @@ __device__ void bwd_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, u
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
   const uint32_t tS = tmem + lane_off + C::kColS + 64 * half;
   const uint32_t tDP = tmem + lane_off + C::kColDP + 64 * half;
+  const uint32_t tDST = tmem + lane_off + C::kColDST + (C::kSepDS ? 32 : 64) * half;
   const float sl2 = p.scale_log2;
   uint8_t* ds_row = smem + C::kOffDS + half * kBoxBytes + r * 128;
 
@@ -396,6 +408,12 @@ __device__ void bwd_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, u
 
     if (!mbar_wait(bar(C::kBarDP), it & 1, ctl)) { ok = false; break; }
     tc_fence_after();
+    if (C::kSepDS && it > 0) {
+      // dP^T of this tile may have been computed before the previous tile's dK / dQ products
+      // read the dS tile (shared memory) and dS^T (TMEM): wait for them before rewriting both.
+      if (!mbar_wait(bar(C::kBarDQFull), (it - 1) & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+    }
     const float4* d4 = reinterpret_cast<const float4*>(dsum);
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
@@ -425,7 +443,7 @@ __device__ void bwd_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, u
         pk[2 * u] = pack_bf16(d0, d1);
         pk[2 * u + 1] = pack_bf16(d2, d3);
       }
-      tmem_st16(tDP + 16 * ch, pk);
+      tmem_st16(tDST + 16 * ch, pk);
       // dS (queries contiguous per key row) into the 128-byte-swizzled MN-major operand
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
