@@ -270,16 +270,6 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// Same with A read from tensor memory (M rows in lanes, K packed two bf16 per column).
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 // Arrives (once) on the mbarrier when every tcgen05 operation issued so far by the elected lane
 // has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -326,20 +316,6 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t* r) {
       : "r"(taddr)
       : "memory");
 }
-// 64 consecutive columns in one load and one wait.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
-      "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
-      "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
-      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63"
-      "}, [%64];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : FA_R8(0), FA_R8(8), FA_R8(16), FA_R8(24), FA_R8(32), FA_R8(40), FA_R8(48), FA_R8(56)
-      : "r"(taddr)
-      : "memory");
-}
 // 128 consecutive columns as two 64-column loads and one wait: the same result as tmem_ld128,
 // but no single instruction needs 128 destination registers, so it also compiles where the
 // register budget is raised per warpgroup.
@@ -361,15 +337,6 @@ __device__ __forceinline__ void tmem_ld64x2(uint32_t taddr, uint32_t* r) {
       : FA_R8(0), FA_R8(8), FA_R8(16), FA_R8(24), FA_R8(32), FA_R8(40), FA_R8(48), FA_R8(56),
         FA_R8(64), FA_R8(72), FA_R8(80), FA_R8(88), FA_R8(96), FA_R8(104), FA_R8(112), FA_R8(120)
       : "r"(taddr), "r"(taddr + 64u)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15}, [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : FA_R8(0), FA_R8(8)
-      : "r"(taddr)
       : "memory");
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
@@ -394,24 +361,9 @@ __device__ __forceinline__ void tmem_st_wait() {
 #undef FA_W8
 
 // ------------------------------------------------------------------------------------------
-// descriptors
+// shared-memory matrix descriptors (start, leading- and stride-dimension byte offsets in 16-byte
+// units at bits 0-13, 16-29, 32-45; version 1 at bit 46; layout type at bits 61-63)
 // ------------------------------------------------------------------------------------------
-// Shared-memory matrix descriptor for a 128-byte-swizzled operand (the layout TMA writes with
-// CU_TENSOR_MAP_SWIZZLE_128B): start address, leading- and stride-dimension byte offsets (all in
-// 16-byte units), descriptor version 1 at bit 46, swizzle mode 2 (128 B) at bits 61-63.
-//   K-major tile (rows of 64 bf16 = 128 B): SBO = 1024 (next group of 8 rows); LBO unused.
-//   MN-major tile: LBO = byte distance to the next 64-element block along M/N, SBO = 1024
-//   (next group of 8 rows along K).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-  d |= 1ull << 46;
-  d |= 2ull << 61;
-  return d;
-}
-
 // Descriptor of an operand without swizzle, K-major, in 8-row x 16-byte core matrices (128
 // contiguous bytes each): lbo = byte distance between the core matrices of one 8-row group that
 // are adjacent along K, sbo = byte distance between adjacent 8-row groups. Layout type 0.
@@ -424,34 +376,16 @@ __device__ __forceinline__ uint64_t sdesc_none(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 
-// The same descriptor split in two 32-bit halves, so that the MMA issue loop only adds a
-// constant to the low half per K step (the issuing thread is on the tensor pipe's critical path).
+// A 128-byte-swizzled operand (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B), as two
+// 32-bit halves so that the MMA issue loop only adds a constant to the low half per K-step.
+//   K-major tile (rows of 64 bf16 = 128 B): SBO = 1024 (next group of 8 rows); LBO unused.
+//   MN-major tile: LBO = byte distance to the next 64-element block along M/N, SBO = 1024 (next
+//   group of 8 rows along K). Layout type 2 (128-byte swizzle).
 __device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
   return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
 __host__ __device__ constexpr uint32_t sdesc_hi_sw128(uint32_t sbo) {
   return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
-}
-__device__ __forceinline__ void mma_ss2(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
-      "setp.ne.b32 p, %5, 0;\n\t"
-      "mov.b64 da, {%1, %3};\n\t"
-      "mov.b64 db, {%2, %3};\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_ts2(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "mov.b64 db, {%2, %3};\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %5, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(accumulate), "r"(idesc)
-      : "memory");
 }
 
 // Lean issue of a whole 128 x 128 (x K) product for the MMA warp, which shares its SM
