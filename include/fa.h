@@ -13,7 +13,8 @@
  *
  * Common conventions of every entry point:
  *   - Layout: Q, K, V, O, dO, dQ, dK, dV are dense row-major [B, H, N, d] (d contiguous);
- *     lse and the backward workspace rows are [B, H, N] fp32.
+ *     lse is [B, H, N] fp32. The backward workspace is opaque scratch of
+ *     fa_bwd_workspace_bytes(...) bytes.
  *   - Pointers are DEVICE pointers owned by the caller, 16-byte aligned; outputs must not alias
  *     inputs. The library allocates no memory on any call.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream). Every call only enqueues work:
