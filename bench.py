@@ -361,7 +361,9 @@ def run_ours(args):
         if w.backward:
             host_in["do"] = do.cpu().pin_memory()
         out_names = ["o", "lse"] + (["dq", "dk", "dv"] if w.backward else [])
-        proto = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+        proto = {"o": o, "lse": lse}
+        if w.backward:
+            proto.update(dq=dq, dk=dk, dv=dv)
         sets = []
         for _ in range(2):
             dev_in = {n: torch.empty_like(t, device=dev) for n, t in host_in.items()}

@@ -1,0 +1,33 @@
+"""bench.py end to end on the GPU: the JSON line carries every key of the reporting contract, for a
+forward-only workload and for the default forward + backward step (short runs)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+        "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e",
+        "gpu_launches", "clocks"}
+
+
+def run_bench(*args):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    return json.loads(lines[0])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("workload", ["single_head_fp32", "mha_N2048_d64"])
+def test_bench_line(cuda, workload):
+    d = run_bench("--workload", workload, "--steps", "3", "--warmup", "3", "--no-cpu-baseline")
+    assert KEYS <= set(d), KEYS - set(d)
+    assert d["value"] > 0 and d["e2e"]["value"] > 0 and d["gpu_launches"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
+    assert d["roofline"]["peak"] > 0 and 0 < d["roofline"]["frac"]
+    assert d["config"]["workload"] == workload
