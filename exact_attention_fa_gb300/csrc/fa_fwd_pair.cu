@@ -12,16 +12,18 @@
 //     streamed from L2 serves 256 query rows;
 //   * warp 8 (one elected lane) streams K_j, V_j with TMA into a ring of 128-byte-swizzled shared-memory
 //     stages guarded by full/empty mbarriers, keys one tile ahead of values; Q is loaded once;
-//   * warp 9 (one elected lane) issues the MMAs: S_t = Q_t K_j^T (both operands in shared memory, fp32
-//     result in TMEM) and O_t += P_t V_j (P_t read from TMEM, V_j from shared memory);
+//   * warps 9 and 10 (one elected lane each) issue the MMAs of tile 0 and tile 1: S_t = Q_t K_j^T
+//     (both operands in shared memory, fp32 result in TMEM) and O_t += P_t V_j (P_t read from
+//     TMEM, V_j from shared memory);
 //   * warps 0-3 / 4-7 are the softmax warpgroups of tile 0 / 1: thread r owns query row r (TMEM
 //     lane r). It loads its 128 scores, applies the scale (log2(e) folded in, exp2 on the SFU),
 //     the causal / tail mask, updates m and l, rescales its O row only when the reference max
-//     moves (conditional rescaling), writes P as bf16 into the columns of S (TMEM), and finally
-//     normalises O and writes O and lse.
+//     moves (conditional rescaling), writes P as bf16 into TMEM, and finally normalises O and
+//     writes O and lse.
 //   * causal / block-sparse: key tiles a query tile does not need are never loaded nor multiplied
 //     ("3 · FlashAttention", question on the causal mask; "拡張: Block-Sparse FlashAttention").
-// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256, 256+d), O_1 [256+d, 256+2d).
+// TMEM columns: d = 128: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512), P_t over S_t;
+// d = 64: S_0, S_1 as above, P_0 [256,320), P_1 [320,384), O_0 [384,448), O_1 [448,512).
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -34,8 +36,8 @@ namespace {
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per tile
 constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 384;  // warps 10-11 only complete the producer / MMA warpgroup
+constexpr int kMmaWarp = 9;    // warps 9 and 10 issue the MMAs of query tiles 0 and 1
+constexpr int kThreads = 384;  // warp 11 only completes the producer / MMA warpgroup
 // Registers per thread after the warpgroups re-balance the 168 each thread is launched with: the
 // softmax warpgroups hold a row of 128 scores plus the row statistics.
 constexpr int kRegsSoftmax = 208;
@@ -52,7 +54,8 @@ struct Cfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-  // barriers: Q, full[S], empty[S], s_full[2], p_full[2], o_full[2], pv_done[2], drain
+  // barriers: Q, full[S], empty[S], s_full[2], p_full[2], o_full[2], pv_done[2], s_free[2],
+  // drain[2]
   static constexpr int kBarQ = 0;
   static constexpr int kBarFull = 1;
   static constexpr int kBarEmpty = 1 + kStages;
@@ -60,14 +63,16 @@ struct Cfg {
   static constexpr int kBarP = kBarS + 2;
   static constexpr int kBarO = kBarP + 2;
   static constexpr int kBarPV = kBarO + 2;
-  static constexpr int kBarDrain = kBarPV + 2;
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarSFree = kBarPV + 2;
+  static constexpr int kBarDrain = kBarSFree + 2;
+  static constexpr int kNumBars = kBarDrain + 2;
   static constexpr int kOffTmemPtr = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemPtr + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1 KB
-  // d = 64: P_t has TMEM columns of its own, so S_t of the next key tile can be computed while
-  // PV_t of this one still reads P_t (S 2 x 128, P 2 x 64, O 2 x 64 = 512 columns). d = 128 has
-  // no room and writes P_t over S_t.
+  // d = 64: P_t has TMEM columns of its own (S 2 x 128, P 2 x 64, O 2 x 64 = 512 columns). The
+  // softmax warps release S_t as soon as they hold its scores in registers, so S_t of the next
+  // key tile is computed while they still work on this one, and PV_t reads P_t meanwhile.
+  // d = 128 has no room and writes P_t over S_t.
   static constexpr bool kSepP = D == 64;
   __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
   __device__ static constexpr uint32_t col_p(int t) { return kSepP ? 256u + 64u * t : col_s(t); }
@@ -178,111 +183,107 @@ __device__ void producer(const FwdParams& p, uint32_t sbase, const Ctl& ctl, int
 }
 
 // ---------------------------------------------------------------------------------------------
+// MMA issue for query tile t, by warp kMmaWarp + t. At d = 64 one tile's MMAs take about as long
+// to issue (about 30-50 cycles per instruction from one thread) as to execute, so each tile has a
+// warp of its own: the two issue streams share the tensor pipe and the K/V ring. Both warps walk
+// every ring position in the producer's order and release each one (the empty barriers count
+// both); a warp waits for a position to be full before releasing it even when its tile skips
+// that key tile, so neither can release a stage ahead of the other's use of it.
 template <int D>
 __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, const Ctl& ctl,
-                           int qt0, int qt1) {
+                           int qt0, int qt1, int t) {
   using C = Cfg<D>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
   constexpr uint32_t kIdescQK = idesc_bf16(128, BN, 0, 0);  // A = Q (K-major), B = K (K-major)
   constexpr uint32_t kIdescPV = idesc_bf16(128, D, 0, 1);   // A = P (TMEM), B = V (MN-major)
 
-  // Descriptors precomputed once (Q of both tiles per K-step, first K and V stage); a stage
-  // is a constant offset away, so each MMA costs the issuing thread one add.
+  // Descriptors precomputed once (Q_t per K-step, first K and V stage); a stage is a constant
+  // offset away, so each MMA costs the issuing thread one add.
   constexpr uint32_t kHi = sdesc_hi_sw128(1024);
   constexpr uint64_t kStageStep = C::kTileBytes >> 4;
-  uint64_t qd[2][D / 16];
+  uint64_t qd[D / 16];
 #pragma unroll
-  for (int t = 0; t < 2; ++t)
-#pragma unroll
-    for (int k = 0; k < D / 16; ++k)
-      qd[t][k] = sdesc64(
-          sdesc_lo(sbase + C::kOffQ + t * C::kTileBytes + (k / 4) * kBoxBytes + (k % 4) * 32, 16), kHi);
+  for (int k = 0; k < D / 16; ++k)
+    qd[k] = sdesc64(
+        sdesc_lo(sbase + C::kOffQ + t * C::kTileBytes + (k / 4) * kBoxBytes + (k % 4) * 32, 16), kHi);
   const uint64_t kd0 = sdesc64(sdesc_lo(sbase + C::kOffKV, 16), kHi);
   const uint64_t vd0 = sdesc64(sdesc_lo(sbase + C::kOffKV, kBoxBytes), kHi);
-  auto issue_s = [&](int t, int stage) {
+  const uint32_t tS = tmem + C::col_s(t);
+  auto issue_s = [&](int stage) {
     if constexpr (D == 128)
-      mma_qk_d128(tmem + C::col_s(t), qd[t], kd0 + stage * kStageStep, kIdescQK);
+      mma_qk_d128(tS, qd, kd0 + stage * kStageStep, kIdescQK);
     else
-      mma_qk_d64(tmem + C::col_s(t), qd[t], kd0 + stage * kStageStep, kIdescQK);
-  };
-  auto issue_pv = [&](int t, int stage, bool acc) {
-    mma_pv_k128(tmem + C::col_o(t), tmem + C::col_p(t), vd0 + stage * kStageStep, kIdescPV,
-                acc ? 1u : 0u);
-    if constexpr (C::kSepP) mma_commit(bar(C::kBarPV + t));
+      mma_qk_d64(tS, qd, kd0 + stage * kStageStep, kIdescQK);
+    mma_commit(bar(C::kBarS + t));
   };
 
   bool ok = mbar_wait_warp(bar(C::kBarQ), 0, ctl);
   tc_fence_after();
-  uint32_t pphase[2] = {0, 0};
-  bool acc[2] = {false, false};
+  uint32_t pphase = 0, sfphase = 0;
+  bool acc = false;
+  bool s_pending = false;  // separate P columns: an S_t issued and not yet released
   // Ring positions in the producer's order: K(u0), then per union tile u_i: K(u_{i+1}), V(u_i).
   auto wait_full = [&](int ps) {
-    return mbar_wait_warp(bar(C::kBarFull + ps % C::kStages), (ps / C::kStages) & 1, ctl);
+    const bool good =
+        mbar_wait_warp(bar(C::kBarFull + ps % C::kStages), (ps / C::kStages) & 1, ctl);
+    tc_fence_after();
+    return good;
   };
   const TilePlan plan = make_plan(p, qt0, qt1);
   int j = plan.next(0);
   int i = 0;  // index of j among the union tiles
   if (ok && j < p.n_tiles) {
     ok = wait_full(0);
-    tc_fence_after();
-    if (ok) {
-      if (plan.active(0, j)) { issue_s(0, 0); mma_commit(bar(C::kBarS + 0)); }
-      if (plan.active(1, j)) { issue_s(1, 0); mma_commit(bar(C::kBarS + 1)); }
-      mma_commit(bar(C::kBarEmpty + 0));
+    if (ok && plan.active(t, j)) {
+      issue_s(0);
+      s_pending = true;
     }
+    mma_commit(bar(C::kBarEmpty + 0));
   }
   while (ok && j < p.n_tiles) {
-    const bool a0 = plan.active(0, j), a1 = plan.active(1, j);
+    const bool a = plan.active(t, j);
     const int jn = plan.next(j + 1);
     const bool has_next = jn < p.n_tiles;
-    const int kpos = 2 * i + 1;                      // K(u_{i+1})
+    const bool n = has_next && plan.active(t, jn);
+    const int kpos = 2 * i + 1;                         // K(u_{i+1})
     const int vpos = has_next ? 2 * i + 2 : 2 * i + 1;  // V(u_i)
     const int sv = vpos % C::kStages, skn = kpos % C::kStages;
-    if (!wait_full(vpos)) { ok = false; break; }
-    tc_fence_after();
-    const bool n0 = has_next && plan.active(0, jn);
-    const bool n1 = has_next && plan.active(1, jn);
-
-    if (has_next) {
-      if (!wait_full(kpos)) { ok = false; break; }
-      tc_fence_after();
-    }
+    if (has_next && !(ok = wait_full(kpos))) break;
     if constexpr (C::kSepP) {
-      // S_t of the next tile first (the softmax warps start on it at once), then PV_t of this
-      // one, which reads P_t from its own columns.
-      bool fail = false;
-      for (int t = 0; t < 2; ++t) {
-        if (!(t ? a1 : a0)) {
-          if (t ? n1 : n0) { issue_s(t, skn); mma_commit(bar(C::kBarS + t)); }
-          continue;
+      // S_t of the next tile as soon as the softmax warps hold S_t of this one in registers,
+      // then PV_t of this tile once they have written P_t.
+      if (n) {
+        if (s_pending) {
+          if (!(ok = mbar_wait_warp(bar(C::kBarSFree + t), sfphase, ctl))) break;
+          sfphase ^= 1;
+          tc_fence_after();
         }
-        if (!mbar_wait_warp(bar(C::kBarP + t), pphase[t], ctl)) { fail = true; break; }
-        pphase[t] ^= 1;
-        tc_fence_after();
-        if (t ? n1 : n0) { issue_s(t, skn); mma_commit(bar(C::kBarS + t)); }
-        issue_pv(t, sv, acc[t]);
-        acc[t] = true;
+        issue_s(skn);
+        s_pending = true;
       }
-      if (fail) { ok = false; break; }
+      if (!(ok = wait_full(vpos))) break;
+      if (a) {
+        if (!(ok = mbar_wait_warp(bar(C::kBarP + t), pphase, ctl))) break;
+        pphase ^= 1;
+        tc_fence_after();
+        mma_pv_k128(tmem + C::col_o(t), tmem + C::col_p(t), vd0 + sv * kStageStep, kIdescPV,
+                    acc ? 1u : 0u);
+        mma_commit(bar(C::kBarPV + t));
+        acc = true;
+      }
     } else {
-      if (a0) {
-        if (!mbar_wait_warp(bar(C::kBarP + 0), pphase[0], ctl)) { ok = false; break; }
-        pphase[0] ^= 1;
+      if (!(ok = wait_full(vpos))) break;
+      if (a) {
+        if (!(ok = mbar_wait_warp(bar(C::kBarP + t), pphase, ctl))) break;
+        pphase ^= 1;
         tc_fence_after();
-        issue_pv(0, sv, acc[0]);
-        acc[0] = true;
+        mma_pv_k128(tmem + C::col_o(t), tmem + C::col_p(t), vd0 + sv * kStageStep, kIdescPV,
+                    acc ? 1u : 0u);
+        acc = true;
       }
-      // S_0 of the next tile overwrites P_0 of this one: the tensor core runs MMAs in issue
-      // order, so the PV above has read P_0 before this write lands.
-      if (n0) { issue_s(0, skn); mma_commit(bar(C::kBarS + 0)); }
-      if (a1) {
-        if (!mbar_wait_warp(bar(C::kBarP + 1), pphase[1], ctl)) { ok = false; break; }
-        pphase[1] ^= 1;
-        tc_fence_after();
-        issue_pv(1, sv, acc[1]);
-        acc[1] = true;
-      }
-      if (n1) { issue_s(1, skn); mma_commit(bar(C::kBarS + 1)); }
+      // S_t of the next tile overwrites P_t of this one: one thread's MMAs run in issue order,
+      // so the PV above has read P_t before this write lands.
+      if (n) issue_s(skn);
     }
     if (has_next) mma_commit(bar(C::kBarEmpty + skn));
     mma_commit(bar(C::kBarEmpty + sv));
@@ -290,15 +291,14 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
     j = jn;
   }
   if (ok) {
-    mma_commit(bar(C::kBarO + 0));
-    mma_commit(bar(C::kBarO + 1));
+    mma_commit(bar(C::kBarO + t));
   } else {
     // Let the MMAs already issued finish before TMEM is released.
     Ctl drain = ctl;
     int zero = 0;
     drain.abort_flag = &zero;
-    mma_commit(bar(C::kBarDrain));
-    mbar_wait_warp(bar(C::kBarDrain), 0, drain);
+    mma_commit(bar(C::kBarDrain + t));
+    mbar_wait_warp(bar(C::kBarDrain + t), 0, drain);
   }
 }
 
@@ -335,6 +335,10 @@ __device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, ui
 
     uint32_t s[128];
     tmem_ld128(tS, s);
+    if constexpr (C::kSepP) {
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarSFree + t));
+    }
 
     const int key0 = j * BN;
     const int lim = (p.mode == kCausal && j == qt) ? min(p.N, row + 1) : p.N;
@@ -494,15 +498,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_pair_kernel(const __grid_cons
     mbar_init(bar(C::kBarQ), 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar(C::kBarFull + s), 1);
-      mbar_init(bar(C::kBarEmpty + s), 1);
+      mbar_init(bar(C::kBarEmpty + s), 2);  // released by both MMA warps
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::kBarS + t), 1);
       mbar_init(bar(C::kBarP + t), 128);
       mbar_init(bar(C::kBarPV + t), 1);
       mbar_init(bar(C::kBarO + t), 1);
+      mbar_init(bar(C::kBarSFree + t), 128);
     }
-    mbar_init(bar(C::kBarDrain), 1);
+    mbar_init(bar(C::kBarDrain + 0), 1);
+    mbar_init(bar(C::kBarDrain + 1), 1);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -518,8 +524,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_pair_kernel(const __grid_cons
     regs_dec<kRegsLoadMma>();
     if (warp == kLoadWarp)
       producer<D>(p, sbase, ctl, bh, qt0, qt1);  // whole warp: one elected lane issues
-    else if (warp == kMmaWarp)
-      mma_issuer<D>(p, sbase, tmem, ctl, qt0, qt1);  // whole warp: one elected lane issues
+    else if (warp == kMmaWarp || warp == kMmaWarp + 1)
+      mma_issuer<D>(p, sbase, tmem, ctl, qt0, qt1, warp - kMmaWarp);  // one elected lane issues
     __syncwarp();
   } else {
     regs_inc<kRegsSoftmax>();
