@@ -29,7 +29,7 @@ _F = ctypes.c_float
 SIGNATURES = [
     ("fa_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     ("fa_fwd_fp32", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
-    ("fa_fwd_blocksparse", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _P]),
+    ("fa_fwd_blocksparse", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
     ("fa_bwd_workspace_bytes", ctypes.c_size_t, [_I, _I, _I, _I]),
     ("fa_bwd", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
     ("fa_bwd_noalloc", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
@@ -115,8 +115,9 @@ def fa_fwd_fp32(q, k, v, o, lse, scale: float, causal: bool = False):
                                              N, d, float(scale), int(bool(causal)), _stream(q)))
 
 
-def fa_fwd_blocksparse(q, k, v, o, lse, scale: float, block_mask):
-    """Block-sparse bf16 forward; block_mask is a uint8 CUDA tensor [N/128, N/128]."""
+def fa_fwd_blocksparse(q, k, v, o, lse, scale: float, block_mask, causal: bool = False):
+    """Block-sparse bf16 forward; block_mask is a uint8 CUDA tensor [ceil(N/128)] * 2; causal
+    additionally applies the causal mask."""
     B, H, N, d = _bhnd(q, k, v, o)
     _rows(lse, q.shape)
     nt = (N + 127) // 128
@@ -125,7 +126,8 @@ def fa_fwd_blocksparse(q, k, v, o, lse, scale: float, block_mask):
         raise ValueError(f"block_mask must be a contiguous uint8 CUDA tensor [{nt}, {nt}]")
     _check("fa_fwd_blocksparse",
            load().fa_fwd_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
-                                     float(scale), _ptr(block_mask), _stream(q)))
+                                     float(scale), int(bool(causal)), _ptr(block_mask),
+                                     _stream(q)))
 
 
 def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
@@ -187,9 +189,7 @@ def attention_forward(q, k, v, scale: float | None = None, causal: bool = False,
             raise ValueError("block-sparse attention is bf16 only")
         fa_fwd_fp32(q, k, v, o, lse, scale, causal)
     elif block_mask is not None:
-        if causal:
-            raise ValueError("block-sparse and causal masks are not combined")
-        fa_fwd_blocksparse(q, k, v, o, lse, scale, block_mask)
+        fa_fwd_blocksparse(q, k, v, o, lse, scale, block_mask, causal)
     else:
         fa_fwd(q, k, v, o, lse, scale, causal)
     return o, lse

@@ -128,13 +128,13 @@ __global__ void selftest_wait_kernel(unsigned* err, unsigned long long timeout_n
 }
 
 int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-             int N, int d, float scale, int mode, const uint8_t* block_mask, fa_stream_t stream) {
+             int N, int d, float scale, int causal, bool sparse, const uint8_t* block_mask,
+             fa_stream_t stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-  if (mode == fa::kBlockSparse && !block_mask) return FA_ERR_INVALID_ARG;
+  if (sparse && !block_mask) return FA_ERR_INVALID_ARG;
   int st = check_common(B, H, N, scale);
   if (st != FA_OK) return st;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (mode == fa::kBlockSparse && N % 128 != 0) return FA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_MISALIGNED;
   DeviceState* ds = nullptr;
@@ -154,7 +154,7 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
   const long long kv_bytes_per_head = 2ll * N * d * 2;
   long long g = (32ll << 20) / kv_bytes_per_head;
   p.heads_per_group = static_cast<int>(g < 1 ? 1 : (g > BH ? BH : g));
-  p.mode = mode;
+  p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.err = ds->err;
   p.timeout_ns = kWaitTimeoutNs;
@@ -168,7 +168,7 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
 #ifndef FA_FWD_POLICY
 #define FA_FWD_POLICY 0  // 0: by shape as above; 1: always pair; 2: always single
 #endif
-  const bool pair = FA_FWD_POLICY == 1 || (FA_FWD_POLICY == 0 && d == 64 && mode != fa::kBlockSparse);
+  const bool pair = FA_FWD_POLICY == 1 || (FA_FWD_POLICY == 0 && d == 64 && !sparse);
   return to_status(pair ? fa::launch_fwd_pair(p, d, cs) : fa::launch_fwd_tc(p, d, ds->num_sms, cs));
 }
 
@@ -176,7 +176,7 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
 
 extern "C" {
 
-int fa_abi_version(void) { return (1 << 16) | 0; }
+int fa_abi_version(void) { return (2 << 16) | 0; }
 
 const char* fa_status_string(int status) {
   switch (status) {
@@ -196,14 +196,13 @@ const char* fa_status_string(int status) {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
            int d, float scale, int causal, fa_stream_t stream) {
-  return fwd_bf16(q, k, v, o, lse, B, H, N, d, scale, causal ? fa::kCausal : fa::kDense, nullptr,
-                  stream);
+  return fwd_bf16(q, k, v, o, lse, B, H, N, d, scale, causal, false, nullptr, stream);
 }
 
 int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                       int H, int N, int d, float scale, const uint8_t* block_mask,
+                       int H, int N, int d, float scale, int causal, const uint8_t* block_mask,
                        fa_stream_t stream) {
-  return fwd_bf16(q, k, v, o, lse, B, H, N, d, scale, fa::kBlockSparse, block_mask, stream);
+  return fwd_bf16(q, k, v, o, lse, B, H, N, d, scale, causal, true, block_mask, stream);
 }
 
 int fa_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,

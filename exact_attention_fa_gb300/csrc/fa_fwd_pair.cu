@@ -106,8 +106,8 @@ struct TilePlan {
 __device__ __forceinline__ TilePlan make_plan(const FwdParams& p, int qt0, int qt1) {
   TilePlan t;
   t.n_tiles = p.n_tiles;
-  const bool sparse = p.mode == kBlockSparse;
-  auto last = [&](int qt) { return qt * BM >= p.N ? -1 : (p.mode == kCausal ? qt : p.n_tiles - 1); };
+  const bool sparse = p.block_mask != nullptr;
+  auto last = [&](int qt) { return qt * BM >= p.N ? -1 : (p.causal ? qt : p.n_tiles - 1); };
   t.last0 = last(qt0);
   t.last1 = last(qt1);
   t.mask0 = sparse ? p.block_mask + static_cast<size_t>(qt0) * p.n_tiles : nullptr;
@@ -341,7 +341,7 @@ __device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, ui
     }
 
     const int key0 = j * BN;
-    const int lim = (p.mode == kCausal && j == qt) ? min(p.N, row + 1) : p.N;
+    const int lim = (p.causal && j == qt) ? min(p.N, row + 1) : p.N;
     if (key0 + BN > lim) {
 #pragma unroll
       for (int c = 0; c < 128; ++c)

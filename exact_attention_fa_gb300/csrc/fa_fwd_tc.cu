@@ -65,16 +65,16 @@ struct Cfg {
   __device__ static constexpr uint32_t col_s(int b) { return 128u + 128u * b; }
 };
 
-// Key tiles visited by this CTA's query tile, resolved once per role: dense and causal query
-// tiles need key tiles [0, last]; block-sparse ones additionally look up their row of the tile
-// mask. Kept in registers so that the per-tile bookkeeping stays a few integer compares.
+// Key tiles visited by this CTA's query tile, resolved once per role: key tiles [0, last] (last =
+// the query tile itself when causal), of which block-sparse query tiles take those their row of
+// the tile mask keeps. Kept in registers so that the per-tile bookkeeping stays a few integer compares.
 struct TilePlan {
   const uint8_t* mask;  // block-sparse: the query tile's row of the tile mask, else null
   int last, n_tiles;
   // next key tile >= j this query tile needs, or n_tiles
   __device__ __forceinline__ int next(int j) const {
     if (mask == nullptr) return j <= last ? j : n_tiles;
-    for (; j < n_tiles; ++j)
+    for (; j <= last; ++j)
       if (__ldg(mask + j) != 0) return j;
     return n_tiles;
   }
@@ -83,8 +83,8 @@ struct TilePlan {
 __device__ __forceinline__ TilePlan make_plan(const FwdParams& p, int qt) {
   TilePlan t;
   t.n_tiles = p.n_tiles;
-  t.last = p.mode == kCausal ? qt : p.n_tiles - 1;
-  t.mask = p.mode == kBlockSparse ? p.block_mask + static_cast<size_t>(qt) * p.n_tiles : nullptr;
+  t.last = p.causal ? qt : p.n_tiles - 1;
+  t.mask = p.block_mask ? p.block_mask + static_cast<size_t>(qt) * p.n_tiles : nullptr;
   return t;
 }
 
@@ -264,7 +264,7 @@ __device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, ui
     tmem_ld128(tS, s);
 
     const int key0 = j * BN;
-    const int lim = (p.mode == kCausal && j == qt) ? min(p.N, row + 1) : p.N;
+    const int lim = (p.causal && j == qt) ? min(p.N, row + 1) : p.N;
     if (key0 + BN > lim) {
 #pragma unroll
       for (int c = 0; c < 128; ++c)

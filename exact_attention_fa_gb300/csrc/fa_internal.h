@@ -8,8 +8,6 @@
 
 namespace fa {
 
-enum MaskMode : int { kDense = 0, kCausal = 1, kBlockSparse = 2 };
-
 // Everything a forward kernel needs. The three tensor maps describe Q, K, V as 3-D tensors
 // [B*H][N][d] (bf16, 128-byte swizzle, box 64 x 128 x 1) so that out-of-range rows of a tile
 // read as zero.
@@ -20,11 +18,11 @@ struct FwdParams {
   CUtensorMap tm_o;  // the output, same view as tm_q (the epilogue stores O tiles with the TMA)
   __nv_bfloat16* o;
   float* lse;
-  const uint8_t* block_mask;  // [n_tiles][n_tiles] or null
+  const uint8_t* block_mask;  // [n_tiles][n_tiles] tile mask, or null (no tile mask)
   int BH, N;
   int n_tiles;                // ceil(N / 128): query tiles = key tiles = block-mask tiles
   int heads_per_group;        // CTA order: groups of heads whose K/V fit in L2
-  int mode;                   // MaskMode
+  int causal;                 // key j > query i masked (combines with a tile mask)
   float scale_log2;           // scale * log2(e)
   unsigned* err;
   unsigned long long timeout_ns;

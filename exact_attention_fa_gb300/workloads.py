@@ -122,19 +122,25 @@ def make_inputs(w: Workload, with_do: bool | None = None) -> Inputs:
         arrays[nm] = bf16_bits_from_f32(x) if w.dtype == "bf16" else x
         del x
     if w.block_sparse:
-        if w.N % TILE:
-            raise ValueError("block-sparse workloads need N to be a multiple of 128")
-        arrays["mask"] = block_mask(w.N // TILE, w.seed)
+        arrays["mask"] = block_mask(-(-w.N // TILE), w.seed)
     return Inputs(w, arrays)
 
 
 def flop_count(w: Workload, mask: np.ndarray | None = None, part: str = "fwd") -> float:
-    """Algorithmic FLOPs: 4*B*H*N^2*d forward (causal: half; block-sparse: active tiles only);
-    the backward counts its five contractions, 2.5 times the forward."""
+    """Algorithmic FLOPs: 4*B*H*N^2*d forward (causal: half; block-sparse: active tiles only,
+    causal block-sparse: active tiles below the diagonal plus half of the active diagonal ones);
+    the backward counts its five contractions, 2.5 times the forward. Block-sparse counts whole
+    tiles, so they need N to be a multiple of 128."""
     if w.block_sparse:
+        if w.N % TILE:
+            raise ValueError("block-sparse FLOP counts need N to be a multiple of 128")
         if mask is None:
             mask = block_mask(w.N // TILE, w.seed)
-        fwd = 4.0 * w.B * w.H * w.d * TILE * TILE * float(mask.sum())
+        if w.causal:
+            tiles = float(np.tril(mask, -1).sum()) + 0.5 * float(np.trace(mask))
+        else:
+            tiles = float(mask.sum())
+        fwd = 4.0 * w.B * w.H * w.d * TILE * TILE * tiles
     else:
         fwd = 4.0 * w.B * w.H * w.N * w.N * w.d * (0.5 if w.causal else 1.0)
     if part == "fwd":

@@ -67,11 +67,14 @@ int fa_fwd_fp32(const float* q, const float* k, const float* v, float* o, float*
                 int H, int N, int d, float scale, int causal, fa_stream_t stream);
 
 /* Block-sparse forward ("FlashAttention: IOを意識した..." (xyznot.com), "拡張: Block-Sparse
- * FlashAttention"): block_mask is a DEVICE uint8 array [N/128][N/128], row = query tile,
- * column = key tile, shared by all (b, h); a zero entry masks the whole 128 x 128 tile of scores
- * and the kernel never visits it. bf16 like fa_fwd; d in {64, 128}; N must be a multiple of 128. */
+ * FlashAttention"): block_mask is a DEVICE uint8 array [T][T] with T = ceil(N/128), row = query
+ * tile, column = key tile, shared by all (b, h); a zero entry masks the whole 128 x 128 tile of
+ * scores and the kernel never visits it. causal != 0 further applies fa_fwd's causal mask (tiles
+ * above the diagonal are skipped whatever the mask says). A row left with no key gets O = 0 and
+ * lse = -inf. bf16 like fa_fwd; d in {64, 128}; any N >= 1 (the last tile's keys past N are
+ * masked). */
 int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                       int H, int N, int d, float scale, const uint8_t* block_mask,
+                       int H, int N, int d, float scale, int causal, const uint8_t* block_mask,
                        fa_stream_t stream);
 
 /* Bytes of device workspace fa_bwd needs: 72 bytes per row of B*H*ceil(N/128)*128 rows (rows
@@ -126,7 +129,7 @@ int fa_check_device_error(fa_stream_t stream);
 /* Static, NUL-terminated description of a status code. */
 const char* fa_status_string(int status);
 
-/* ABI version: (major << 16) | minor. */
+/* ABI version: (major << 16) | minor. Major 2: fa_fwd_blocksparse takes a causal flag. */
 int fa_abi_version(void);
 
 #ifdef __cplusplus

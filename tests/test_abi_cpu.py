@@ -54,7 +54,7 @@ def test_status_strings(lib):
     assert lib.fa_status_string(0) == b"ok"
     assert b"aligned" in lib.fa_status_string(3)
     assert lib.fa_status_string(999) == b"unknown status"
-    assert lib.fa_abi_version() >> 16 == 1
+    assert lib.fa_abi_version() >> 16 == 2
 
 
 @pytest.mark.parametrize("args,want", [
@@ -78,8 +78,8 @@ def test_fwd_validation(lib, args, want):
 
 def test_blocksparse_validation(lib):
     base = (fake(), fake(), fake(), fake(), fake(), 1, 1)
-    assert lib.fa_fwd_blocksparse(*base, 256, 64, 0.125, P(0), None) == 1  # no mask
-    assert lib.fa_fwd_blocksparse(*base, 200, 64, 0.125, fake(), None) == 2  # N % 128
+    assert lib.fa_fwd_blocksparse(*base, 256, 64, 0.125, 0, P(0), None) == 1  # no mask
+    assert lib.fa_fwd_blocksparse(*base, 200, 96, 0.125, 1, fake(), None) == 2  # head dim
 
 
 def test_fp32_validation(lib):

@@ -98,6 +98,45 @@ def test_blocksparse_small_full(cuda, d):
     run_and_compare(w, cuda)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_blocksparse_ragged_N(cuda, d):
+    # N = 1000: an 8 x 8 tile mask whose last row and column cover 104 keys / queries
+    w = wl.Workload("bs_ragged", 1, 2, 1000, d, block_sparse=True, seed=36)
+    run_and_compare(w, cuda)
+
+
+@pytest.mark.parametrize("d,N", [(64, 1024), (128, 1000)])
+def test_blocksparse_causal(cuda, d, N):
+    w = wl.Workload("bs_causal", 2, 2, N, d, causal=True, block_sparse=True, seed=37)
+    run_and_compare(w, cuda)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_all_ones_mask_causal_equals_causal_bitwise(cuda, d):
+    w = wl.Workload("bs_ones_causal", 1, 2, 700, d, causal=True, seed=38)
+    inp = wl.make_inputs(w)
+    q, k, v = (H.to_device(inp, n, cuda) for n in ("q", "k", "v"))
+    ones = torch.ones((6, 6), dtype=torch.uint8, device=cuda)
+    o1, l1 = fa.attention_forward(q, k, v, w.softmax_scale, causal=True)
+    o2, l2 = fa.attention_forward(q, k, v, w.softmax_scale, causal=True, block_mask=ones)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_causal_mask_above_diagonal_only_gives_empty_rows(cuda):
+    """Causal + a tile mask that keeps only tiles above the diagonal for query tile 0: its rows
+    see no key (O = 0, lse = -inf); query tile 1 keeps its diagonal tile."""
+    w = wl.Workload("bs_causal_empty", 1, 1, 256, 128, seed=39)
+    inp = wl.make_inputs(w)
+    q, k, v = (H.to_device(inp, n, cuda) for n in ("q", "k", "v"))
+    m = torch.tensor([[0, 1], [0, 1]], dtype=torch.uint8, device=cuda)
+    o, lse = fa.attention_forward(q, k, v, w.softmax_scale, causal=True, block_mask=m)
+    assert torch.all(o[:, :, :128] == 0) and torch.all(torch.isneginf(lse[:, :, :128]))
+    O_ref, lse_ref = orc.forward_head(inp.f64("q")[0, 0], inp.f64("k")[0, 0], inp.f64("v")[0, 0],
+                                      w.softmax_scale, causal=True, block_mask=m.cpu().numpy())
+    H.compare_o(o[0, 0].float().cpu().numpy(), O_ref, bf16=True)
+    H.compare_lse(lse[0, 0].cpu().numpy(), lse_ref)
+
+
 def test_blocksparse_N16384_d64_sampled(cuda):
     run_and_compare(wl.WORKLOADS["blocksparse_N16384_d64"], cuda, rows_per_head=32, heads=4)
 

@@ -143,6 +143,30 @@ def test_block_mask_matches_masked_scipy_softmax():
     assert np.allclose(lse, scipy.special.logsumexp(Xm, axis=1), atol=1e-13)
 
 
+def test_causal_block_mask_ragged_matches_brute_force():
+    """Causal and tile masks combined, n not a multiple of the tile: the allowed set is the
+    elementwise AND, written out here with plain loops; a query tile whose only tiles lie above
+    the diagonal has rows with no key (O = 0, lse = -inf)."""
+    rng = np.random.default_rng(4)
+    tile, n = 4, 18  # 5 x 5 tile mask, last tile holds 2 keys / queries
+    nt = -(-n // tile)
+    X = rng.standard_normal((n, n)) * 2
+    bm = (rng.random((nt, nt)) < 0.5).astype(np.uint8)
+    np.fill_diagonal(bm, 1)
+    bm[0, 0] = 0  # rows 0..3 keep only tiles above the diagonal -> empty under causal
+    ok = np.zeros((n, n), dtype=bool)
+    for i in range(n):
+        for j in range(n):
+            ok[i, j] = j <= i and bm[i // tile][j // tile] == 1
+    O, lse = orc.forward_head(X, np.eye(n), np.eye(n), 1.0, causal=True, block_mask=bm, tile=tile)
+    empty = ~ok.any(axis=1)
+    assert empty[:4].all() and not empty[4:].any()
+    assert np.all(O[empty] == 0.0) and np.all(np.isneginf(lse[empty]))
+    Xm = np.where(ok, X, -np.inf)[~empty]
+    assert np.allclose(O[~empty], scipy.special.softmax(Xm, axis=1), atol=1e-14)
+    assert np.allclose(lse[~empty], scipy.special.logsumexp(Xm, axis=1), atol=1e-13)
+
+
 # ------------------------------------------------------------------ invariants
 
 def rand_head(n, d, seed, dv=None):
