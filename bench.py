@@ -16,6 +16,10 @@ pinned host buffers, host<->device copies inside the timed region. Under torchru
 its own replica of the workload (independent heads: no collective on the data path) and `value`
 sums over ranks using the slowest rank's time.
 
+Decoding workloads (decode_*: a few query rows per head against a long key/value cache) are
+bound by HBM bandwidth, so their line reports GB/s of algorithmic bytes (K and V read once, q
+read, O and lse written) against the measured copy bandwidth.
+
 --impl reference times the fp64 CPU oracle (the parity reference) on the host cores instead.
 """
 from __future__ import annotations
@@ -62,6 +66,16 @@ def flops(w, mask=None):
     from exact_attention_fa_gb300 import workloads as wl
     f = wl.flop_count(w, mask, "fwd")
     return f, (2.5 * f if w.backward else 0.0)
+
+
+def work_per_head(w, mask=None):
+    """(amount of the metric's unit one (b, h) head represents, unit): TFLOP for attention
+    steps, GB of algorithmic traffic for decoding."""
+    from exact_attention_fa_gb300 import workloads as wl
+    if w.decode:
+        return wl.decode_bytes(w) / (w.B * w.H) / 1e9, "GB/s"
+    f_fwd, f_bwd = flops(w, mask)
+    return (f_fwd + f_bwd) / (w.B * w.H) / 1e12, "TFLOPS"
 
 
 def load_peaks():
@@ -116,8 +130,7 @@ def cpu_baseline_leg(w, inp, budget_s=20.0):
     cores = host_cores()
     pool = make_pool(cores)
     try:
-        f_fwd, f_bwd = flops(w, inp.raw("mask") if w.block_sparse else None)
-        per_head = (f_fwd + f_bwd) / (w.B * w.H)
+        per_head, unit = work_per_head(w, inp.raw("mask") if w.block_sparse else None)
         # one probe round of `cores` heads, then as many whole rounds as fit the budget
         n = min(cores, w.B * w.H)
         dt = time_oracle(pool, oracle_tasks(w, inp, range(n)))
@@ -129,7 +142,7 @@ def cpu_baseline_leg(w, inp, budget_s=20.0):
             heads += len(more)
     finally:
         pool.terminate()
-    return {"value": per_head * heads / total / 1e12, "unit": "TFLOPS", "cores": cores,
+    return {"value": per_head * heads / total, "unit": unit, "cores": cores,
             "kind": "oracle",
             "sample": f"{heads} of {w.B * w.H} heads of {w.name}, fp64 numpy oracle "
                       f"({'forward+backward' if w.backward else 'forward'}), one head per worker",
@@ -145,8 +158,7 @@ def run_reference(args):
     inp = wl.make_inputs(w, with_do=w.backward)
     cores = host_cores()
     n = min(cores, w.B * w.H)
-    f_fwd, f_bwd = flops(w, inp.raw("mask") if w.block_sparse else None)
-    per_head = (f_fwd + f_bwd) / (w.B * w.H)
+    per_head, unit = work_per_head(w, inp.raw("mask") if w.block_sparse else None)
     pool = make_pool(cores)
     times = []
     try:
@@ -157,18 +169,18 @@ def run_reference(args):
     finally:
         pool.terminate()
     t = statistics.fmean(times)
-    value = per_head * n / t / 1e12
+    value = per_head * n / t
     sample = (f"{n} heads of {w.name} per step (one per worker), fp64 numpy oracle, "
               f"{'forward+backward' if w.backward else 'forward'}")
     print(json.dumps({
-        "impl": "reference", "metric": metric_name(w), "value": value, "unit": "TFLOPS",
+        "impl": "reference", "metric": metric_name(w), "value": value, "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(w, args.gpus, note="oracle on host cores"),
-        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": sample},
-        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -190,11 +202,14 @@ def job_tflops(world, flops_per_rank, ms):
 
 
 def metric_name(w):
+    if w.decode:
+        return "attention decode GB/s (K, V read once; q, O, lse)"
     return "attention fwd/bwd TFLOPS (4·B·H·N²·d, causal halved)"
 
 
 def config_of(w, n_gpus, note=None):
     c = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype,
+         **({"Nq": w.nq, "Nk": w.N} if w.decode else {}),
          "causal": w.causal, "block_sparse": w.block_sparse,
          "step": "forward+backward" if w.backward else "forward",
          "global_batch": w.B * n_gpus, "seq_len": w.N, "parallelism": f"replicas{n_gpus}",
@@ -286,6 +301,8 @@ def run_ours(args):
         return torch.from_numpy(a).to(dev)
 
     q, k, v = dev_tensor("q"), dev_tensor("k"), dev_tensor("v")
+    if w.decode:
+        return run_decode(args, w, fa, q, k, v, cpu, world, rank, local, dev)
     do = dev_tensor("do") if w.backward else None
     mask = dev_tensor("mask") if w.block_sparse else None
     scale = w.softmax_scale
@@ -472,6 +489,109 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
+        "clocks": clocks.summary(local),
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_decode(args, w, fa, q, k, v, cpu, world, rank, local, dev):
+    """Decoding: one fa_decode call per step (split kernel + merge kernel), the key/value cache
+    resident in HBM. e2e: each step copies its new query rows from pinned host memory and reads
+    O and lse back (the cache is state that stays on the device, not a per-step input)."""
+    import torch
+    import torch.distributed as dist
+    from exact_attention_fa_gb300 import workloads as wl
+    scale = w.softmax_scale
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    n_ctas = fa.fa_decode_ctas(w.B, w.H, w.nq, w.N, w.d)
+    ws = torch.empty(fa.fa_decode_workspace_bytes(w.B, w.H, w.nq, w.N, w.d), dtype=torch.uint8,
+                     device=dev)
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    algo_bytes = wl.decode_bytes(w)
+
+    def step(qq=q, oo=o, ll=lse):
+        fa.fa_decode(qq, k, v, oo, ll, scale, n_ctas, ws)
+
+    for _ in range(args.warmup):
+        flush_buf.zero_()
+        step()
+    fa.fa_check_device_error(dev)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(os.path.join("/tmp", f"fa_clocks_{os.getpid()}.csv")) as clocks:
+        time.sleep(0.1)
+        t0 = time.perf_counter()
+        for i in range(K):
+            flush_buf.zero_()
+            ev[i][0].record()
+            step()
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        wall = time.perf_counter() - t0
+        time.sleep(0.1)
+    fa.fa_check_device_error(dev)
+    t_step = statistics.fmean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+    t_step = aggregate_over_ranks([t_step], world, dev)[0]
+
+    e2e = None
+    if not args.no_e2e:
+        hq = q.cpu().pin_memory()
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        dq_, do_, dl_ = torch.empty_like(q), torch.empty_like(o), torch.empty_like(lse)
+        E = min(K, 100)
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for i in range(E + 2):
+            if i == 2:
+                torch.cuda.synchronize()
+                t_start.record()
+            dq_.copy_(hq, non_blocking=True)
+            step(dq_, do_, dl_)
+            ho.copy_(do_, non_blocking=True)
+            hl.copy_(dl_, non_blocking=True)
+        t_end.record()
+        torch.cuda.synchronize()
+        fa.fa_check_device_error(dev)
+        t_e2e = aggregate_over_ranks([t_start.elapsed_time(t_end) / E], world, dev)[0]
+        e2e = {"value": world * algo_bytes / (t_e2e * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": hq.numel() * hq.element_size(),
+               "d2h_bytes_per_step": ho.numel() * ho.element_size() + hl.numel() * hl.element_size(),
+               "ms_per_step": t_e2e, "steps": E,
+               "note": "key/value cache resident on the device; the step's new query rows go in, "
+                       "O and lse come back"}
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peaks, peak_src = load_peaks()
+    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    achieved = algo_bytes / (t_step * 1e-3) / 1e9
+    kname = f"decode_stream_kernel<{w.d}> (+ decode_merge_kernel<{w.d}>)"
+    line = {
+        "metric": metric_name(w), "value": world * achieved, "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: i.i.d. N(0,1) inputs, seeded, rounded to bf16",
+        "config": {**config_of(w, world), "n_ctas": n_ctas,
+                   "l2": "inputs (K, V) larger than L2; also flushed between steps"},
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_src} copy bandwidth "
+                                    f"{'MEASURED_PEAKS.json' if peak_src == 'measured' else 'fallback'}",
+                     "algorithmic_bytes": algo_bytes,
+                     "traffic": recorded_traffic(kname, w)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * K,
         "clocks": clocks.summary(local),
         "wall_s_timed_region": wall,
     }

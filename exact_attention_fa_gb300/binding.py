@@ -33,6 +33,9 @@ SIGNATURES = [
     ("fa_bwd_workspace_bytes", ctypes.c_size_t, [_I, _I, _I, _I]),
     ("fa_bwd", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
     ("fa_bwd_noalloc", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    ("fa_decode", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P]),
+    ("fa_decode_ctas", _I, [_I, _I, _I, _I, _I]),
+    ("fa_decode_workspace_bytes", ctypes.c_size_t, [_I, _I, _I, _I, _I]),
     ("fa_selftest_wait_timeout", _I, [ctypes.c_uint, _P]),
     ("fa_check_device_error", _I, [_P]),
     ("fa_status_string", ctypes.c_char_p, [_I]),
@@ -163,6 +166,35 @@ def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool):
                                  _stream(q)))
 
 
+def fa_decode_ctas(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
+    return int(load().fa_decode_ctas(B, H, Nq, Nk, d))
+
+
+def fa_decode_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
+    return int(load().fa_decode_workspace_bytes(B, H, Nq, Nk, d))
+
+
+def fa_decode(q, k, v, o, lse, scale: float, n_ctas: int = 0, workspace=None):
+    """Decoding forward: q, o bf16 [B,H,Nq,d] (Nq <= 8), k, v bf16 [B,H,Nk,d], lse fp32 [B,H,Nq];
+    workspace: fa_decode_workspace_bytes(...) bytes on the device."""
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    _bhnd(q, o)
+    _bhnd(k, v)
+    if k.shape[:2] != q.shape[:2] or k.shape[3] != d or q.device != k.device:
+        raise ValueError("q and k/v must share B, H, d and the device")
+    _rows(lse, q.shape)
+    need = fa_decode_workspace_bytes(B, H, Nq, Nk, d)
+    if (workspace is None or not workspace.is_cuda or not workspace.is_contiguous()
+            or workspace.numel() * workspace.element_size() < need):
+        raise ValueError(f"workspace must be a contiguous CUDA tensor of at least {need} bytes")
+    _check("fa_decode", load().fa_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq,
+                                         Nk, d, float(scale), int(n_ctas), _ptr(workspace),
+                                         _stream(q)))
+
+
 def fa_selftest_wait_timeout(timeout_us: int = 20000, device=None):
     """Runs the library's bounded-wait self-test kernel (a wait that can only time out)."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
@@ -192,6 +224,18 @@ def attention_forward(q, k, v, scale: float | None = None, causal: bool = False,
         fa_fwd_blocksparse(q, k, v, o, lse, scale, block_mask, causal)
     else:
         fa_fwd(q, k, v, o, lse, scale, causal)
+    return o, lse
+
+
+def attention_decode(q, k, v, scale: float | None = None, n_ctas: int = 0):
+    """Allocates O, lse and the workspace and runs fa_decode (n_ctas = 0: the library's choice)."""
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    B, H, Nq, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    ws = torch.empty(max(16, fa_decode_workspace_bytes(B, H, Nq, k.shape[2], d)),
+                     dtype=torch.uint8, device=q.device)
+    fa_decode(q, k, v, o, lse, scale, n_ctas, ws)
     return o, lse
 
 

@@ -172,11 +172,28 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
   return to_status(pair ? fa::launch_fwd_pair(p, d, cs) : fa::launch_fwd_tc(p, d, ds->num_sms, cs));
 }
 
+// CTAs for decoding: as many as the SMs hold at once, never more than there are key blocks.
+int decode_auto_ctas(int BH, int Nk, int d, int num_sms) {
+  constexpr int kB = fa::kDecodeBlockKeys;
+  const long long blocks = static_cast<long long>(BH) * ((Nk + kB - 1) / kB);
+  long long n = static_cast<long long>(num_sms) * fa::decode_ctas_per_sm(d);
+  if (n > fa::kDecodeMaxCtas) n = fa::kDecodeMaxCtas;
+  return static_cast<int>(n < blocks ? n : blocks);
+}
+
+int check_decode(int B, int H, int Nq, int Nk, int d, float scale) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (Nq > fa::kDecodeMaxNq || (d != 64 && d != 128)) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H * (Nk > Nq ? Nk : Nq) > 0x7fffffffll) return FA_ERR_TOO_LARGE;
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
-int fa_abi_version(void) { return (2 << 16) | 0; }
+int fa_abi_version(void) { return (2 << 16) | 1; }
 
 const char* fa_status_string(int status) {
   switch (status) {
@@ -268,6 +285,57 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   p.err = ds->err;
   p.timeout_ns = kWaitTimeoutNs;
   return to_status(fa::launch_bwd(p, ds->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fa_decode_ctas(int B, int H, int Nq, int Nk, int d) {
+  if (check_decode(B, H, Nq, Nk, d, 1.f) != FA_OK) return 0;
+  DeviceState* ds = nullptr;
+  if (device_state(&ds) != FA_OK) return 0;
+  return decode_auto_ctas(B * H, Nk, d, ds->num_sms);
+}
+
+size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
+  if (check_decode(B, H, Nq, Nk, d, 1.f) != FA_OK) return 0;
+  const long long BH = static_cast<long long>(B) * H;
+  long long ctas = BH * ((Nk + fa::kDecodeBlockKeys - 1) / fa::kDecodeBlockKeys);
+  if (ctas > fa::kDecodeMaxCtas) ctas = fa::kDecodeMaxCtas;
+  return static_cast<size_t>((ctas + BH) * Nq * (d + 1)) * sizeof(float);
+}
+
+int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int Nq, int Nk, int d, float scale, int n_ctas, void* workspace,
+              fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+  int st = check_decode(B, H, Nq, Nk, d, scale);
+  if (st != FA_OK) return st;
+  if (n_ctas < 0 || n_ctas > fa::kDecodeMaxCtas) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(workspace))
+    return FA_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != FA_OK) return st;
+  const int BH = B * H;
+  const int nb = (Nk + fa::kDecodeBlockKeys - 1) / fa::kDecodeBlockKeys;
+  const long long blocks = static_cast<long long>(BH) * nb;
+  if (n_ctas == 0) n_ctas = decode_auto_ctas(BH, Nk, d, ds->num_sms);
+  if (n_ctas > blocks) n_ctas = static_cast<int>(blocks);
+  fa::DecodeParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.BH = BH;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.blocks_per_head = nb;
+  p.n_ctas = n_ctas;
+  p.ws_o = static_cast<float*>(workspace);
+  p.ws_lse = p.ws_o + static_cast<size_t>(n_ctas + BH) * Nq * d;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.err = ds->err;
+  p.timeout_ns = kWaitTimeoutNs;
+  return to_status(fa::launch_decode(p, d, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int fa_selftest_wait_timeout(unsigned timeout_us, fa_stream_t stream) {

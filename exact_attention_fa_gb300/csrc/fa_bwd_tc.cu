@@ -115,16 +115,6 @@ struct BCfg {
                 "register split exceeds the launch's 512 x 128 registers");
 };
 
-__device__ __forceinline__ void tma_bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                             uint32_t bar) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      "\n\t}" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 // CTA -> (head, key tile). Heads in L2-sized groups; inside a group the key tiles with the most
 // query tiles to visit (causal: the first ones) come first.
 __device__ __forceinline__ void decode_bwd(const BwdParams& p, int group, int& bh, int& j) {

@@ -1,0 +1,359 @@
+// Decoding attention: a few query rows against a long key/value sequence ("3 · FlashAttention",
+// 3.6 "L'attention en décodage" and the Flash-Decoding row of 3.7).
+//
+// With Nq <= 8 query rows per head the work is a matrix-vector product: every key and value row
+// is used Nq times, so the kernel is bound by HBM bandwidth, not by arithmetic, and the tensor
+// cores would sit idle (128-row MMA tiles for a handful of rows). GB300 mapping:
+//   * Flash-Decoding's split of the keys, balanced for a fixed grid: the key blocks (32 keys) of
+//     all heads, head after head, are dealt out as G equal contiguous ranges, one per CTA, with
+//     G = the CTAs the SMs hold at once (persistent: no tail wave, every SM streams until the
+//     end). A range may start or end inside a head and may span several heads;
+//   * one warp of the CTA streams its range with 1-D bulk copies (cp.async.bulk) into a shared-
+//     memory ring of (K block, V block) pairs (128-160 KB in flight per CTA), across head
+//     boundaries, guarded by full / empty mbarriers;
+//   * eight compute warps take the blocks in turn, each with an online softmax state of its own
+//     ("3 · FlashAttention", 3.3): lane = key for the scores q.k (16-byte loads rotated by lane,
+//     so no bank conflicts), warp shuffles for the block's max and sum, lane = d/32 output
+//     columns for O += P V. No CTA-wide barrier per block: the warps meet only where a head
+//     ends inside the range, to merge their states into that (CTA, head) piece;
+//   * each piece holds O_c / l_c and its log-sum-exp lse_c; a second kernel merges the pieces of
+//     each head with the same statistics merge as the blockwise forward (lse = log Σ exp lse_c,
+//     O = Σ exp(lse_c - lse) O_c).
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kWarps = 8;              // compute warps; warp kWarps streams the blocks in
+constexpr int kThreads = 32 * (kWarps + 1);
+constexpr int kBK = kDecodeBlockKeys;  // keys per block: one key per lane
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct DCfg {
+  static constexpr int kStages = D == 128 ? 10 : 16;  // ring depth: 160 / 128 KB in flight
+  static constexpr int kBlockBytes = kBK * D * 2;  // one K or V block, bf16
+  static constexpr int kStageBytes = 2 * kBlockBytes;
+  static constexpr int kOffQ = kStages * kStageBytes;                // fp32 [kDecodeMaxNq][D]
+  static constexpr int kOffO = kOffQ + kDecodeMaxNq * D * 4;         // fp32 [kWarps][Nq][D]
+  static constexpr int kOffML = kOffO + kWarps * kDecodeMaxNq * D * 4;  // fp32 [kWarps][Nq][2]
+  static constexpr int kOffBar = kOffML + kWarps * kDecodeMaxNq * 8;
+  static constexpr int kOffAbort = kOffBar + 16 * kStages;         // full[S], empty[S]
+  static constexpr int kSmemBytes = kOffAbort + 16;
+  static constexpr int kDimsPerLane = D / 32;
+};
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// CTA of global key block g (blocks of all heads in a row, head-major): blocks are dealt out as
+// G contiguous ranges [c*T/G, (c+1)*T/G).
+__device__ __forceinline__ int cta_of_block(long long g, long long T, int G) {
+  return static_cast<int>(((g + 1) * G - 1) / T);
+}
+
+// CTA c streams its range of key blocks. Warp kWarps copies them in order into the ring; inside
+// each head's stretch of the range, compute warp w takes every kWarps-th block (lane = key) with
+// an online softmax state of its own, and at the end of the stretch the warps' states are merged
+// into the piece (c, head h) at slot c + h: O_piece / l_piece and lse_piece (log2 units). Along
+// the ranges (c, h) only ever steps forward, so c + h is unique.
+template <int D, int NQ>
+__global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const __grid_constant__ DecodeParams p) {
+  using C = DCfg<D>;
+  constexpr int S = C::kStages;
+  constexpr int kDL = C::kDimsPerLane;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int Nq = p.Nq;
+  const int nb = p.blocks_per_head;
+  const long long T = static_cast<long long>(p.BH) * nb;
+  const int G = gridDim.x, c = blockIdx.x;
+  const long long g0 = c * T / G;
+  const int nblk = static_cast<int>((c + 1) * T / G - g0);
+  float* qs = reinterpret_cast<float*>(smem + C::kOffQ);
+  float* wo = reinterpret_cast<float*>(smem + C::kOffO);
+  float* wml = reinterpret_cast<float*>(smem + C::kOffML);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
+  const Ctl ctl{abort_flag, p.err, p.timeout_ns};
+  auto full = [&](int s) { return sbase + C::kOffBar + 8u * s; };
+  auto empty = [&](int s) { return sbase + C::kOffBar + 8u * (S + s); };
+  auto keys_in = [&](long long g) {
+    const int jb = static_cast<int>(g % nb);
+    return min(kBK, p.Nk - jb * kBK);
+  };
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kWarps) {
+    // ---------------------------------------------------------------- producer (whole warp)
+    int i = 0;
+    bool ok = true;
+    for (; i < nblk; ++i) {
+      const int s = i % S;
+      if (!mbar_wait_warp(empty(s), ((i / S) & 1) ^ 1, ctl)) { ok = false; break; }
+      const long long g = g0 + i;
+      const int h = static_cast<int>(g / nb), jb = static_cast<int>(g % nb);
+      const uint32_t bytes = static_cast<uint32_t>(keys_in(g)) * D * 2;
+      const size_t off = (static_cast<size_t>(h) * p.Nk + static_cast<size_t>(jb) * kBK) * D;
+      mbar_arrive_expect_tx(full(s), 2 * bytes);
+      tma_bulk_g2s(sbase + s * C::kStageBytes, p.k + off, bytes, full(s));
+      tma_bulk_g2s(sbase + s * C::kStageBytes + C::kBlockBytes, p.v + off, bytes, full(s));
+    }
+    if (!ok) {
+      // Give the copies in flight a bounded time to land before the CTA exits.
+      Ctl drain = ctl;
+      int zero = 0;
+      drain.abort_flag = &zero;
+      for (int b = max(0, i - S); b < i; ++b) mbar_wait_warp(full(b % S), (b / S) & 1, drain);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ compute warps
+  constexpr int kChunks = D / 8;  // 16-byte chunks per key row
+  bool ok = true;
+  long long g = g0;
+  const long long g_end = g0 + nblk;
+  while (g < g_end) {
+    const int h = static_cast<int>(g / nb);
+    const long long seg_end = min(g_end, static_cast<long long>(h + 1) * nb);
+    // q of head h, pre-multiplied by scale * log2(e) so that scores come out in log2 units
+    const __nv_bfloat16* qg = p.q + static_cast<size_t>(h) * Nq * D;
+    for (int e = tid; e < Nq * D; e += 32 * kWarps) qs[e] = __bfloat162float(qg[e]) * p.scale_log2;
+    bar_sync(1, 32 * kWarps);
+
+    float m[NQ], l[NQ], acc[NQ][kDL];
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) {
+      m[j] = -INFINITY;
+      l[j] = 0.f;
+#pragma unroll
+      for (int t = 0; t < kDL; ++t) acc[j][t] = 0.f;
+    }
+    for (long long gb = g + warp; ok && gb < seg_end; gb += kWarps) {
+      const int i = static_cast<int>(gb - g0);  // position in the ring order
+      const int s = i % S;
+      if (!mbar_wait_warp(full(s), (i / S) & 1, ctl)) { ok = false; break; }
+      const int n = keys_in(gb);
+      const __nv_bfloat16* Ks = reinterpret_cast<const __nv_bfloat16*>(smem + s * C::kStageBytes);
+      const __nv_bfloat16* Vs = Ks + kBK * D;
+
+      // scores of key `lane` (16-byte chunks in an order rotated by lane: no bank conflicts),
+      // four partial sums per query row for short dependency chains
+      float sc[NQ][4];
+#pragma unroll
+      for (int j = 0; j < NQ; ++j)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) sc[j][u] = 0.f;
+      if (lane < n) {
+#pragma unroll
+        for (int cc = 0; cc < kChunks; ++cc) {
+          const int ch = (cc + lane) % kChunks;
+          float kf[8];
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(Ks + lane * D + ch * 8), kf);
+#pragma unroll
+          for (int j = 0; j < NQ; ++j) {
+            if (j < Nq) {
+              const float4 qa = *reinterpret_cast<const float4*>(qs + j * D + ch * 8);
+              const float4 qb = *reinterpret_cast<const float4*>(qs + j * D + ch * 8 + 4);
+              float a = sc[j][cc % 4];
+              a = fmaf(qa.x, kf[0], a); a = fmaf(qa.y, kf[1], a);
+              a = fmaf(qa.z, kf[2], a); a = fmaf(qa.w, kf[3], a);
+              a = fmaf(qb.x, kf[4], a); a = fmaf(qb.y, kf[5], a);
+              a = fmaf(qb.z, kf[6], a); a = fmaf(qb.w, kf[7], a);
+              sc[j][cc % 4] = a;
+            }
+          }
+        }
+      }
+      // online softmax per query row (the block's 32 scores sit one per lane)
+      float pj[NQ];
+#pragma unroll
+      for (int j = 0; j < NQ; ++j) {
+        if (j < Nq) {
+          const float sj = lane < n ? (sc[j][0] + sc[j][1]) + (sc[j][2] + sc[j][3]) : -INFINITY;
+          float mx = sj;
+#pragma unroll
+          for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, o));
+          const float m_new = fmaxf(m[j], mx);  // finite: the block has at least one key
+          pj[j] = ex2(sj - m_new);
+          float ps = pj[j];
+#pragma unroll
+          for (int o = 16; o; o >>= 1) ps += __shfl_xor_sync(~0u, ps, o);
+          const float alpha = ex2(m[j] - m_new);  // 0 while nothing was accumulated
+          l[j] = l[j] * alpha + ps;
+          m[j] = m_new;
+#pragma unroll
+          for (int t = 0; t < kDL; ++t) acc[j][t] *= alpha;
+        }
+      }
+      // O (this lane's kDL columns) += P V over the block's keys, eight keys per step
+      for (int k0 = 0; k0 < n; k0 += 8) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int key = k0 + u;
+          if (key < n) {
+            float vf[kDL];
+            if constexpr (kDL == 4) {
+              const uint2 w = *reinterpret_cast<const uint2*>(Vs + key * D + lane * 4);
+              vf[0] = __uint_as_float(w.x << 16);
+              vf[1] = __uint_as_float(w.x & 0xffff0000u);
+              vf[2] = __uint_as_float(w.y << 16);
+              vf[3] = __uint_as_float(w.y & 0xffff0000u);
+            } else {
+              const uint32_t w = *reinterpret_cast<const uint32_t*>(Vs + key * D + lane * 2);
+              vf[0] = __uint_as_float(w << 16);
+              vf[1] = __uint_as_float(w & 0xffff0000u);
+            }
+#pragma unroll
+            for (int j = 0; j < NQ; ++j) {
+              if (j < Nq) {
+                const float pk = __shfl_sync(~0u, pj[j], key);
+#pragma unroll
+                for (int t = 0; t < kDL; ++t) acc[j][t] = fmaf(pk, vf[t], acc[j][t]);
+              }
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty(s));
+    }
+
+    // merge the warps' states into the piece (c, h)
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) {
+      if (j < Nq) {
+#pragma unroll
+        for (int t = 0; t < kDL; ++t) wo[(warp * kDecodeMaxNq + j) * D + lane * kDL + t] = acc[j][t];
+        if (lane == 0) {
+          wml[(warp * kDecodeMaxNq + j) * 2] = m[j];
+          wml[(warp * kDecodeMaxNq + j) * 2 + 1] = l[j];
+        }
+      }
+    }
+    if (bar_red_or(1, 32 * kWarps, !ok)) return;
+    const size_t slot = static_cast<size_t>(c) + h;
+    for (int e = tid; e < Nq * D; e += 32 * kWarps) {
+      const int j = e / D, col = e % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wml[(w * kDecodeMaxNq + j) * 2]);
+      float L = 0.f, a = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float f = ex2(wml[(w * kDecodeMaxNq + j) * 2] - M);  // 0 for an idle warp
+          L = fmaf(f, wml[(w * kDecodeMaxNq + j) * 2 + 1], L);
+          a = fmaf(f, wo[(w * kDecodeMaxNq + j) * D + col], a);
+        }
+      }
+      p.ws_o[(slot * Nq + j) * D + col] = L > 0.f ? a / L : 0.f;
+      if (col == 0) p.ws_lse[slot * Nq + j] = L > 0.f ? M + __log2f(L) : -INFINITY;
+    }
+    bar_sync(1, 32 * kWarps);  // wo, wml and qs are free again
+    g = seg_end;
+  }
+}
+
+// One CTA of D threads per (head, query row): merges the partial results of the CTAs whose block
+// ranges cover the head (lse = log2 Σ 2^lse_part, O = Σ 2^(lse_part - lse) O_part).
+template <int D>
+__global__ void __launch_bounds__(D) decode_merge_kernel(const __grid_constant__ DecodeParams p) {
+  const int row = blockIdx.x;  // h * Nq + i
+  const int h = row / p.Nq, i = row - h * p.Nq;
+  const int col = threadIdx.x;
+  const long long T = static_cast<long long>(p.BH) * p.blocks_per_head;
+  const int c0 = cta_of_block(static_cast<long long>(h) * p.blocks_per_head, T, p.n_ctas);
+  const int c1 = cta_of_block(static_cast<long long>(h + 1) * p.blocks_per_head - 1, T, p.n_ctas);
+  float mx = -INFINITY;
+  for (int cc = c0; cc <= c1; ++cc)
+    mx = fmaxf(mx, p.ws_lse[(static_cast<size_t>(cc) + h) * p.Nq + i]);
+  const size_t out = static_cast<size_t>(row) * D + col;
+  if (mx == -INFINITY) {
+    p.o[out] = __float2bfloat16_rn(0.f);
+    if (col == 0) p.lse[row] = -INFINITY;
+    return;
+  }
+  float den = 0.f, a = 0.f;
+  for (int cc = c0; cc <= c1; ++cc) {
+    const size_t slot = (static_cast<size_t>(cc) + h) * p.Nq + i;
+    const float w = ex2(p.ws_lse[slot] - mx);
+    den += w;
+    a = fmaf(w, p.ws_o[slot * D + col], a);
+  }
+  p.o[out] = __float2bfloat16_rn(a / den);
+  if (col == 0) p.lse[row] = (mx + __log2f(den)) * kLn2;
+}
+
+template <int D, int NQ>
+cudaError_t configure() {
+  static cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<D, NQ>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              DCfg<D>::kSmemBytes);
+  return e;
+}
+
+// Kernel instances for at most 1, 2, 4 and 8 query rows (registers scale with the bound).
+template <int D, int NQ>
+cudaError_t launch_nq(const DecodeParams& p, cudaStream_t s) {
+  cudaError_t e = configure<D, NQ>();
+  if (e != cudaSuccess) return e;
+  decode_stream_kernel<D, NQ><<<p.n_ctas, kThreads, DCfg<D>::kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch(const DecodeParams& p, cudaStream_t s) {
+  cudaError_t e = p.Nq <= 1   ? launch_nq<D, 1>(p, s)
+                  : p.Nq <= 2 ? launch_nq<D, 2>(p, s)
+                  : p.Nq <= 4 ? launch_nq<D, 4>(p, s)
+                              : launch_nq<D, 8>(p, s);
+  if (e != cudaSuccess) return e;
+  decode_merge_kernel<D><<<static_cast<unsigned>(p.BH) * p.Nq, D, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// Resident CTAs per SM of the largest instance (the others use no more registers).
+template <int D>
+int resident_ctas() {
+  int n = 0;
+  if (configure<D, kDecodeMaxNq>() != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_stream_kernel<D, kDecodeMaxNq>,
+                                                    kThreads, DCfg<D>::kSmemBytes) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  return n < 1 ? 1 : n;
+}
+
+}  // namespace
+
+int decode_ctas_per_sm(int d) { return d == 128 ? resident_ctas<128>() : resident_ctas<64>(); }
+
+cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t s) {
+  if (d == 64) return launch<64>(p, s);
+  if (d == 128) return launch<128>(p, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -65,10 +65,33 @@ struct BwdParams {
   unsigned long long timeout_ns;
 };
 
+// Decoding: Nq <= kDecodeMaxNq query rows per head against Nk keys. The 32-key blocks of all
+// heads are dealt out to n_ctas CTAs in contiguous ranges; piece (CTA c, head h) is slot c + h.
+constexpr int kDecodeMaxNq = 8;
+constexpr int kDecodeMaxCtas = 1024;
+constexpr int kDecodeBlockKeys = 32;
+struct DecodeParams {
+  const __nv_bfloat16* q;  // [BH][Nq][d]
+  const __nv_bfloat16* k;  // [BH][Nk][d]
+  const __nv_bfloat16* v;
+  __nv_bfloat16* o;        // [BH][Nq][d]
+  float* lse;              // [BH][Nq]
+  float* ws_o;             // [n_ctas + BH][Nq][d] pieces' outputs O_c / l_c
+  float* ws_lse;           // [n_ctas + BH][Nq] pieces' lse, log2 units
+  int BH, Nq, Nk;
+  int blocks_per_head;     // ceil(Nk / kDecodeBlockKeys)
+  int n_ctas;              // 1 .. min(BH * blocks_per_head, kDecodeMaxCtas)
+  float scale_log2;
+  unsigned* err;
+  unsigned long long timeout_ns;
+};
+
 // Launchers; return a cudaError_t (cudaSuccess on success).
 cudaError_t launch_fwd_tc(const FwdParams& p, int d, int num_sms, cudaStream_t s);    // 1 tile/CTA
 cudaError_t launch_fwd_pair(const FwdParams& p, int d, cudaStream_t s);               // 2 tiles/CTA
 cudaError_t launch_fwd_fp32(const Fp32FwdParams& p, cudaStream_t s);
 cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t s);
+int decode_ctas_per_sm(int d);  // resident split-kernel CTAs per SM (shared-memory bound)
 
 }  // namespace fa

@@ -169,6 +169,18 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
       "@e prefetch.tensormap [%0];\n\t}" ::"l"(map)
       : "memory");
 }
+// Contiguous global -> shared copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// completing on mbarrier `bar`. Whole warp; one elected lane issues.
+__device__ __forceinline__ void tma_bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      "\n\t}" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint32_t bar, int c0,
                                             int c1, int c2) {
   asm volatile(

@@ -69,6 +69,15 @@ class Workload:
     backward: bool = False
     seed: int = 0
     scale: float | None = None  # None means 1/sqrt(d)
+    nq: int = 0  # decoding: query rows per head (keys and values keep N rows); 0: N queries
+
+    @property
+    def decode(self) -> bool:
+        return self.nq > 0
+
+    @property
+    def n_queries(self) -> int:
+        return self.nq if self.nq > 0 else self.N
 
     @property
     def softmax_scale(self) -> float:
@@ -87,6 +96,8 @@ WORKLOADS = {
                                        block_sparse=True, seed=4),
     "bwd_causal_N4096_d128": Workload("bwd_causal_N4096_d128", 4, 16, 4096, 128, causal=True,
                                       backward=True, seed=5),
+    # decoding ("3 · FlashAttention", 3.6): one new query row per head against a 32k-key cache
+    "decode_N32768_d128": Workload("decode_N32768_d128", 8, 32, 32768, 128, nq=1, seed=6),
 }
 
 
@@ -113,12 +124,13 @@ class Inputs:
 
 def make_inputs(w: Workload, with_do: bool | None = None) -> Inputs:
     shape = (w.B, w.H, w.N, w.d)
+    qshape = (w.B, w.H, w.n_queries, w.d)
     names = [("q", STREAM_Q), ("k", STREAM_K), ("v", STREAM_V)]
     if with_do or (with_do is None and w.backward):
         names.append(("do", STREAM_DO))
     arrays = {}
     for nm, st in names:
-        x = normal_f32(shape, w.seed, st)
+        x = normal_f32(qshape if nm in ("q", "do") else shape, w.seed, st)
         arrays[nm] = bf16_bits_from_f32(x) if w.dtype == "bf16" else x
         del x
     if w.block_sparse:
@@ -130,8 +142,10 @@ def flop_count(w: Workload, mask: np.ndarray | None = None, part: str = "fwd") -
     """Algorithmic FLOPs: 4*B*H*N^2*d forward (causal: half; block-sparse: active tiles only,
     causal block-sparse: active tiles below the diagonal plus half of the active diagonal ones);
     the backward counts its five contractions, 2.5 times the forward. Block-sparse counts whole
-    tiles, so they need N to be a multiple of 128."""
-    if w.block_sparse:
+    tiles, so they need N to be a multiple of 128. Decoding: 4*B*H*nq*N*d."""
+    if w.decode:
+        fwd = 4.0 * w.B * w.H * w.nq * w.N * w.d
+    elif w.block_sparse:
         if w.N % TILE:
             raise ValueError("block-sparse FLOP counts need N to be a multiple of 128")
         if mask is None:
@@ -150,3 +164,8 @@ def flop_count(w: Workload, mask: np.ndarray | None = None, part: str = "fwd") -
     if part == "fwd+bwd":
         return 3.5 * fwd
     raise ValueError(part)
+
+
+def decode_bytes(w: Workload) -> float:
+    """Algorithmic HBM bytes of one decoding pass: K and V read once, q read, O and lse written."""
+    return float(w.B * w.H * (2 * w.N * w.d * 2 + 2 * w.nq * w.d * 2 + 4 * w.nq))

@@ -114,6 +114,32 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    const float* lse, float* dq, void* dk, void* dv, int B, int H, int N, int d,
                    float scale, int causal, fa_stream_t stream);
 
+/* Decoding attention ("3 · FlashAttention", 3.6 "L'attention en décodage"; Flash-Decoding in
+ * 3.7): Nq (1 .. 8) new query rows per head attend to all Nk keys of that head (no mask):
+ *     o = softmax(scale * q K^T) V,   lse = log sum_j exp(scale * q.k_j).
+ * q, o : bf16 [B,H,Nq,d];  k, v : bf16 [B,H,Nk,d];  lse : fp32 [B,H,Nq] (all DEVICE pointers,
+ * 16-byte aligned, caller-owned; q, k, v read, o and lse written). d in {64, 128}; Nk >= 1.
+ * The work is a matrix-vector product bound by HBM bandwidth. The 32-key blocks of all heads are
+ * split into n_ctas equal contiguous ranges streamed by separate CTAs (a range may cut a head and
+ * span several); the pieces of each head are merged with the softmax statistics merge.
+ * n_ctas = 0 takes as many CTAs as the device holds at once (fa_decode_ctas); 1 .. 1024 forces
+ * the count (capped at the number of key blocks). `workspace`: fa_decode_workspace_bytes(...)
+ * bytes of device scratch, contents undefined on entry and on exit. Errors: FA_ERR_INVALID_ARG
+ * (null pointer, bad size or scale, n_ctas out of range), FA_ERR_UNSUPPORTED (Nq > 8, d),
+ * FA_ERR_MISALIGNED, FA_ERR_TOO_LARGE, FA_ERR_NO_DEVICE, FA_ERR_CUDA; all before any launch. */
+int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int Nq, int Nk, int d, float scale, int n_ctas, void* workspace,
+              fa_stream_t stream);
+
+/* The CTA count fa_decode uses for n_ctas = 0 on the current device; 0 for invalid sizes or
+ * without a usable device. */
+int fa_decode_ctas(int B, int H, int Nq, int Nk, int d);
+
+/* Bytes of workspace fa_decode needs for any n_ctas: (min(B*H*ceil(Nk/32), 1024) + B*H) pieces
+ * of Nq rows, each row d + 1 floats (the piece's normalised output and log-sum-exp); 0 for
+ * invalid sizes. */
+size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d);
+
 /* Diagnostic, with no counterpart on the pages: launches one CTA whose thread waits on an
  * on-chip barrier that nothing ever arrives at, bounded by timeout_us (1 .. 10^7 microseconds).
  * The wait gives up, records FA_ERR_DEVICE_TIMEOUT in the device error word and the kernel
@@ -129,7 +155,8 @@ int fa_check_device_error(fa_stream_t stream);
 /* Static, NUL-terminated description of a status code. */
 const char* fa_status_string(int status);
 
-/* ABI version: (major << 16) | minor. Major 2: fa_fwd_blocksparse takes a causal flag. */
+/* ABI version: (major << 16) | minor. Major 2: fa_fwd_blocksparse takes a causal flag; minor 1:
+ * fa_decode. */
 int fa_abi_version(void);
 
 #ifdef __cplusplus

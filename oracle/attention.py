@@ -200,6 +200,33 @@ def forward_fa1_head(q, k, v, scale, block):
     return O, m + np.log(ell)
 
 
+def decode_split_head(q, k, v, scale, n_splits):
+    """Flash-Decoding ([REAPER] 3.6 "L'attention en décodage" and the Flash-Decoding row of 3.7):
+    the keys are cut into ``n_splits`` contiguous chunks of ceil(n_k / n_splits) keys, each chunk
+    gives (O_c, lse_c) by the plain definition, and the chunks are combined with the softmax
+    statistics merge ([XYZ] "手法", merge of (m, l); [REAPER] 3.3):
+    lse = log sum_c exp(lse_c),  O = sum_c exp(lse_c - lse) O_c.
+    A chunk past the end of the keys is empty (lse_c = -inf) and gets weight 0.
+    """
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    n_q, n_k = np.asarray(q).shape[0], k.shape[0]
+    per = -(-n_k // n_splits)
+    parts = []
+    for c in range(n_splits):
+        j0, j1 = c * per, min(n_k, (c + 1) * per)
+        if j0 >= j1:
+            parts.append((np.zeros((n_q, v.shape[1])), np.full(n_q, NEG_INF)))
+        else:
+            parts.append(forward_head(q, k[j0:j1], v[j0:j1], scale))
+    L = np.stack([p[1] for p in parts])  # [n_splits, n_q]
+    top = L.max(axis=0)
+    W = np.exp(L - top[None, :])
+    den = W.sum(axis=0)
+    O = sum(W[c][:, None] * parts[c][0] for c in range(n_splits)) / den[:, None]
+    return O, top + np.log(den)
+
+
 # ----------------------------------------------------------------------------------------------
 # backward ([REAPER] 3.4, [Q67] section 五: recompute P from the inputs; gradients by calculus)
 # ----------------------------------------------------------------------------------------------

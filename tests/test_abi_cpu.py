@@ -21,6 +21,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for want in ("fa_fwd", "fa_fwd_fp32", "fa_fwd_blocksparse", "fa_bwd", "fa_bwd_workspace_bytes",
+                 "fa_decode", "fa_decode_ctas", "fa_decode_workspace_bytes",
                  "fa_check_device_error", "fa_status_string", "fa_abi_version"):
         assert want in names
 
@@ -80,6 +81,29 @@ def test_blocksparse_validation(lib):
     base = (fake(), fake(), fake(), fake(), fake(), 1, 1)
     assert lib.fa_fwd_blocksparse(*base, 256, 64, 0.125, 0, P(0), None) == 1  # no mask
     assert lib.fa_fwd_blocksparse(*base, 200, 96, 0.125, 1, fake(), None) == 2  # head dim
+
+
+def test_decode_validation(lib):
+    q = (fake(), fake(), fake(), fake(), fake())
+    ws = fake()
+    assert lib.fa_decode(P(0), *q[1:], 1, 1, 1, 100, 64, 0.125, 0, ws, None) == 1  # null q
+    assert lib.fa_decode(*q, 1, 1, 1, 100, 64, 0.125, 0, P(0), None) == 1  # no workspace
+    assert lib.fa_decode(*q, 1, 1, 0, 100, 64, 0.125, 0, ws, None) == 1  # Nq = 0
+    assert lib.fa_decode(*q, 1, 1, 1, 0, 64, 0.125, 0, ws, None) == 1  # Nk = 0
+    assert lib.fa_decode(*q, 1, 1, 9, 100, 64, 0.125, 0, ws, None) == 2  # Nq > 8
+    assert lib.fa_decode(*q, 1, 1, 1, 100, 96, 0.125, 0, ws, None) == 2  # head dim
+    assert lib.fa_decode(*q, 1, 1, 1, 100, 64, 0.125, -1, ws, None) == 1  # n_ctas
+    assert lib.fa_decode(*q, 1, 1, 1, 100, 64, 0.125, 1025, ws, None) == 1
+    assert lib.fa_decode(*q, 1, 1, 1, 100, 64, 0.0, 0, ws, None) == 1  # scale
+    assert lib.fa_decode(fake(0x10008), *q[1:], 1, 1, 1, 100, 64, 0.125, 1, ws, None) == 3
+
+
+def test_decode_workspace_and_ctas(lib):
+    # pieces: min(key blocks, 1024) CTAs + B*H heads, Nq rows of d + 1 floats each
+    assert lib.fa_decode_workspace_bytes(2, 3, 4, 1000, 128) == (6 * 32 + 6) * 4 * 129 * 4
+    assert lib.fa_decode_workspace_bytes(8, 32, 1, 32768, 128) == (1024 + 256) * 129 * 4
+    assert lib.fa_decode_workspace_bytes(1, 1, 9, 100, 64) == 0  # unsupported sizes
+    assert lib.fa_decode_ctas(1, 1, 9, 100, 64) == 0
 
 
 def test_fp32_validation(lib):

@@ -167,6 +167,29 @@ def test_causal_block_mask_ragged_matches_brute_force():
     assert np.allclose(lse[~empty], scipy.special.logsumexp(Xm, axis=1), atol=1e-13)
 
 
+@pytest.mark.parametrize("n_q,n_k,splits", [(1, 1, 1), (1, 200, 1), (3, 200, 7), (8, 1000, 13),
+                                              (2, 5, 9), (1, 129, 128)])
+def test_decode_split_merge_equals_definition(n_q, n_k, splits):
+    """Chunked decoding merged by the statistics formula is the plain softmax over all keys
+    (closed form, any chunk count, empty chunks included)."""
+    q, k, v = rand_head(max(n_q, n_k), 16, 11 + n_k)
+    q = q[:n_q] * 2.0
+    k, v = k[:n_k], v[:n_k]
+    O, lse = orc.decode_split_head(q, k, v, 0.7, splits)
+    O_ref, lse_ref = orc.forward_head(q, k, v, 0.7)
+    assert np.allclose(O, O_ref, atol=1e-13) and np.allclose(lse, lse_ref, atol=1e-12)
+
+
+def test_decode_single_key_and_uniform_scores():
+    """One key: O = v_0, lse = scale q.k_0. Zero query: O = mean of V, lse = log n_k."""
+    q, k, v = rand_head(40, 8, 5)
+    O, lse = orc.decode_split_head(q[:2], k[:1], v[:1], 0.5, 3)
+    assert np.allclose(O, np.repeat(v[:1], 2, axis=0), atol=1e-15)
+    assert np.allclose(lse, 0.5 * (q[:2] @ k[0]), atol=1e-14)
+    O, lse = orc.decode_split_head(np.zeros((1, 8)), k, v, 0.5, 6)
+    assert np.allclose(O[0], v.mean(axis=0), atol=1e-14) and np.isclose(lse[0], np.log(40))
+
+
 # ------------------------------------------------------------------ invariants
 
 def rand_head(n, d, seed, dv=None):
