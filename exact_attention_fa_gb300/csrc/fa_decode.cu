@@ -8,14 +8,15 @@
 //     all heads, head after head, are dealt out as G equal contiguous ranges, one per CTA, with
 //     G = the CTAs the SMs hold at once (persistent: no tail wave, every SM streams until the
 //     end). A range may start or end inside a head and may span several heads;
-//   * one warp of the CTA streams its range with 1-D bulk copies (cp.async.bulk) into a shared-
-//     memory ring of (K block, V block) pairs (128-160 KB in flight per CTA), across head
+//   * one warp of the CTA streams its range with 1-D bulk copies (cp.async.bulk) into per-warp
+//     shared-memory rings of (K block, V block) pairs (128 KB in flight per CTA), across head
 //     boundaries, guarded by full / empty mbarriers;
 //   * eight compute warps take the blocks in turn, each with an online softmax state of its own
 //     ("3 · FlashAttention", 3.3): lane = key for the scores q.k (16-byte loads rotated by lane,
-//     so no bank conflicts), warp shuffles for the block's max and sum, lane = d/32 output
-//     columns for O += P V. No CTA-wide barrier per block: the warps meet only where a head
-//     ends inside the range, to merge their states into that (CTA, head) piece;
+//     so no bank conflicts), warp shuffles for the block's max and sum, lane = 4 output columns
+//     for O += P V (at d = 64 the two half-warps take alternate keys). No CTA-wide barrier per
+//     block: the warps meet only where a head ends inside the range, to merge their states into
+//     that (CTA, head) piece;
 //   * each piece holds O_c / l_c and its log-sum-exp lse_c; a second kernel merges the pieces of
 //     each head with the same statistics merge as the blockwise forward (lse = log Σ exp lse_c,
 //     O = Σ exp(lse_c - lse) O_c).
@@ -35,7 +36,11 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D>
 struct DCfg {
-  static constexpr int kStages = D == 128 ? 10 : 16;  // ring depth: 160 / 128 KB in flight
+  // Each compute warp has a ring of its own (one consumer per stage, so the phase parity of a
+  // stage's barrier always refers to the block the warp expects): 1 stage per warp at d = 128
+  // (16 KB blocks), 2 at d = 64 (8 KB); 128 KB in flight per CTA either way.
+  static constexpr int kStagesPerWarp = D == 128 ? 1 : 2;
+  static constexpr int kStages = kWarps * kStagesPerWarp;
   static constexpr int kBlockBytes = kBK * D * 2;  // one K or V block, bf16
   static constexpr int kStageBytes = 2 * kBlockBytes;
   static constexpr int kOffQ = kStages * kStageBytes;                // fp32 [kDecodeMaxNq][D]
@@ -44,7 +49,8 @@ struct DCfg {
   static constexpr int kOffBar = kOffML + kWarps * kDecodeMaxNq * 8;
   static constexpr int kOffAbort = kOffBar + 16 * kStages;         // full[S], empty[S]
   static constexpr int kSmemBytes = kOffAbort + 16;
-  static constexpr int kDimsPerLane = D / 32;
+  static constexpr int kLanesPerRow = D / 4;   // lanes covering one V row, 4 columns each
+  static constexpr int kKeySplit = 32 / kLanesPerRow;  // keys a warp takes at once in O += P V
 };
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
@@ -62,16 +68,21 @@ __device__ __forceinline__ int cta_of_block(long long g, long long T, int G) {
   return static_cast<int>(((g + 1) * G - 1) / T);
 }
 
-// CTA c streams its range of key blocks. Warp kWarps copies them in order into the ring; inside
-// each head's stretch of the range, compute warp w takes every kWarps-th block (lane = key) with
-// an online softmax state of its own, and at the end of the stretch the warps' states are merged
-// into the piece (c, head h) at slot c + h: O_piece / l_piece and lse_piece (log2 units). Along
-// the ranges (c, h) only ever steps forward, so c + h is unique.
+// CTA c streams its range of key blocks. Warp kWarps copies them in order into the rings;
+// compute warp w takes the CTA-local blocks i = w (mod kWarps) (lane = key) with an online
+// softmax state of its own per head, and at the end of each head's stretch of the range the
+// warps' states are merged into the piece (c, head h) at slot c + h: O_piece / l_piece and
+// lse_piece (log2 units). Along the ranges (c, h) only ever steps forward, so c + h is unique.
 template <int D, int NQ>
 __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const __grid_constant__ DecodeParams p) {
   using C = DCfg<D>;
   constexpr int S = C::kStages;
-  constexpr int kDL = C::kDimsPerLane;
+  constexpr int R = C::kStagesPerWarp;
+  // CTA-local block i belongs to compute warp i % kWarps, as that warp's k-th block
+  // (k = i / kWarps): stage (i % kWarps) * R + k % R, phase k / R of that stage.
+  auto stage_of = [&](int i) { return (i % kWarps) * R + (i / kWarps) % R; };
+  auto parity_of = [&](int i) { return static_cast<uint32_t>((i / kWarps / R) & 1); };
+  constexpr int kKS = C::kKeySplit;
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -108,8 +119,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const __grid
     int i = 0;
     bool ok = true;
     for (; i < nblk; ++i) {
-      const int s = i % S;
-      if (!mbar_wait_warp(empty(s), ((i / S) & 1) ^ 1, ctl)) { ok = false; break; }
+      const int s = stage_of(i);
+      if (!mbar_wait_warp(empty(s), parity_of(i) ^ 1u, ctl)) { ok = false; break; }
       const long long g = g0 + i;
       const int h = static_cast<int>(g / nb), jb = static_cast<int>(g % nb);
       const uint32_t bytes = static_cast<uint32_t>(keys_in(g)) * D * 2;
@@ -123,13 +134,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const __grid
       Ctl drain = ctl;
       int zero = 0;
       drain.abort_flag = &zero;
-      for (int b = max(0, i - S); b < i; ++b) mbar_wait_warp(full(b % S), (b / S) & 1, drain);
+      for (int b = max(0, i - S); b < i; ++b) mbar_wait_warp(full(stage_of(b)), parity_of(b), drain);
     }
     return;
   }
 
   // ------------------------------------------------------------------ compute warps
   constexpr int kChunks = D / 8;  // 16-byte chunks per key row
+  const int sub = lane / C::kLanesPerRow, col4 = (lane % C::kLanesPerRow) * 4;
   bool ok = true;
   long long g = g0;
   const long long g_end = g0 + nblk;
@@ -141,18 +153,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const __grid
     for (int e = tid; e < Nq * D; e += 32 * kWarps) qs[e] = __bfloat162float(qg[e]) * p.scale_log2;
     bar_sync(1, 32 * kWarps);
 
-    float m[NQ], l[NQ], acc[NQ][kDL];
+    float m[NQ], l[NQ], acc[NQ][4];
 #pragma unroll
     for (int j = 0; j < NQ; ++j) {
       m[j] = -INFINITY;
       l[j] = 0.f;
 #pragma unroll
-      for (int t = 0; t < kDL; ++t) acc[j][t] = 0.f;
+      for (int t = 0; t < 4; ++t) acc[j][t] = 0.f;
     }
-    for (long long gb = g + warp; ok && gb < seg_end; gb += kWarps) {
-      const int i = static_cast<int>(gb - g0);  // position in the ring order
-      const int s = i % S;
-      if (!mbar_wait_warp(full(s), (i / S) & 1, ctl)) { ok = false; break; }
+    // this warp's blocks of the stretch: CTA-local indices congruent to warp mod kWarps
+    const int first = static_cast<int>(g - g0);
+    for (int i = first + (warp - first % kWarps + kWarps) % kWarps; ok && g0 + i < seg_end;
+         i += kWarps) {
+      const long long gb = g0 + i;
+      const int s = stage_of(i);
+      if (!mbar_wait_warp(full(s), parity_of(i), ctl)) { ok = false; break; }
       const int n = keys_in(gb);
       const __nv_bfloat16* Ks = reinterpret_cast<const __nv_bfloat16*>(smem + s * C::kStageBytes);
       const __nv_bfloat16* Vs = Ks + kBK * D;
@@ -203,34 +218,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const __grid
           l[j] = l[j] * alpha + ps;
           m[j] = m_new;
 #pragma unroll
-          for (int t = 0; t < kDL; ++t) acc[j][t] *= alpha;
+          for (int t = 0; t < 4; ++t) acc[j][t] *= alpha;
         }
       }
-      // O (this lane's kDL columns) += P V over the block's keys, eight keys per step
-      for (int k0 = 0; k0 < n; k0 += 8) {
+      // O += P V: lane owns 4 columns of a V row; at d = 64 the two half-warps take alternate
+      // keys (kKS = 2) and are summed at the end. Keys past n contribute p = 0 and v = 0.
+      for (int k0 = 0; k0 < n; k0 += 8 * kKS) {
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const int key = k0 + u;
-          if (key < n) {
-            float vf[kDL];
-            if constexpr (kDL == 4) {
-              const uint2 w = *reinterpret_cast<const uint2*>(Vs + key * D + lane * 4);
-              vf[0] = __uint_as_float(w.x << 16);
-              vf[1] = __uint_as_float(w.x & 0xffff0000u);
-              vf[2] = __uint_as_float(w.y << 16);
-              vf[3] = __uint_as_float(w.y & 0xffff0000u);
-            } else {
-              const uint32_t w = *reinterpret_cast<const uint32_t*>(Vs + key * D + lane * 2);
-              vf[0] = __uint_as_float(w << 16);
-              vf[1] = __uint_as_float(w & 0xffff0000u);
-            }
+          const int key = k0 + u * kKS + sub;
+          uint2 w = make_uint2(0u, 0u);
+          if (key < n) w = *reinterpret_cast<const uint2*>(Vs + key * D + col4);
+          const float vf[4] = {__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                               __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u)};
 #pragma unroll
-            for (int j = 0; j < NQ; ++j) {
-              if (j < Nq) {
-                const float pk = __shfl_sync(~0u, pj[j], key);
+          for (int j = 0; j < NQ; ++j) {
+            if (j < Nq) {
+              const float pk = __shfl_sync(~0u, pj[j], key);
 #pragma unroll
-                for (int t = 0; t < kDL; ++t) acc[j][t] = fmaf(pk, vf[t], acc[j][t]);
-              }
+              for (int t = 0; t < 4; ++t) acc[j][t] = fmaf(pk, vf[t], acc[j][t]);
             }
           }
         }
@@ -244,7 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const __grid
     for (int j = 0; j < NQ; ++j) {
       if (j < Nq) {
 #pragma unroll
-        for (int t = 0; t < kDL; ++t) wo[(warp * kDecodeMaxNq + j) * D + lane * kDL + t] = acc[j][t];
+        for (int t = 0; t < 4; ++t) {
+          float a = acc[j][t];
+          if constexpr (kKS == 2) a += __shfl_xor_sync(~0u, a, 16);
+          if (sub == 0) wo[(warp * kDecodeMaxNq + j) * D + col4 + t] = a;
+        }
         if (lane == 0) {
           wml[(warp * kDecodeMaxNq + j) * 2] = m[j];
           wml[(warp * kDecodeMaxNq + j) * 2 + 1] = l[j];

@@ -50,6 +50,14 @@ def test_decode_small(cuda, nq, nk, d, ctas):
     run_decode(w, cuda, ctas)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_long_ranges(cuda, d):
+    """Eight CTAs, each streaming about 500 blocks through its warps' rings and across a head
+    boundary (ragged last block per head)."""
+    w = wl.Workload("decode_long", 2, 4, 16384 + 7, d, nq=2, seed=50 + d)
+    run_decode(w, cuda, 8)
+
+
 def test_decode_cta_counts_agree(cuda):
     w = wl.Workload("decode_counts", 1, 4, 3000, 128, nq=2, seed=48)
     outs = [run_decode(w, cuda, n)[0] for n in (1, 2, 13, 47, 188)]
