@@ -285,34 +285,57 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const __grid
   }
 }
 
-// One CTA of D threads per (head, query row): merges the partial results of the CTAs whose block
-// ranges cover the head (lse = log2 Σ 2^lse_part, O = Σ 2^(lse_part - lse) O_part).
+// One CTA of D threads per (head, query row): merges the pieces of the CTAs whose block ranges
+// cover the head (lse = log2 Σ 2^lse_c, O = Σ 2^(lse_c - lse) O_c). The pieces' weights are
+// formed in parallel in shared memory, so the loop over pieces issues independent loads.
 template <int D>
 __global__ void __launch_bounds__(D) decode_merge_kernel(const __grid_constant__ DecodeParams p) {
+  __shared__ float wts[kDecodeMaxCtas];
+  __shared__ float red[D / 32];
   const int row = blockIdx.x;  // h * Nq + i
   const int h = row / p.Nq, i = row - h * p.Nq;
-  const int col = threadIdx.x;
+  const int t = threadIdx.x, lane = t % 32, warp = t / 32;
   const long long T = static_cast<long long>(p.BH) * p.blocks_per_head;
   const int c0 = cta_of_block(static_cast<long long>(h) * p.blocks_per_head, T, p.n_ctas);
   const int c1 = cta_of_block(static_cast<long long>(h + 1) * p.blocks_per_head - 1, T, p.n_ctas);
+  const int n = c1 - c0 + 1;  // <= n_ctas <= kDecodeMaxCtas
+  auto slot = [&](int k) { return (static_cast<size_t>(c0 + k) + h) * p.Nq + i; };
+  auto block_reduce = [&](float v, bool is_max) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float x = __shfl_xor_sync(~0u, v, o);
+      v = is_max ? fmaxf(v, x) : v + x;
+    }
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float r = red[0];
+    for (int w = 1; w < D / 32; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+    __syncthreads();
+    return r;
+  };
   float mx = -INFINITY;
-  for (int cc = c0; cc <= c1; ++cc)
-    mx = fmaxf(mx, p.ws_lse[(static_cast<size_t>(cc) + h) * p.Nq + i]);
-  const size_t out = static_cast<size_t>(row) * D + col;
+  for (int k = t; k < n; k += D) {
+    wts[k] = p.ws_lse[slot(k)];
+    mx = fmaxf(mx, wts[k]);
+  }
+  mx = block_reduce(mx, true);
+  const size_t out = static_cast<size_t>(row) * D + t;
   if (mx == -INFINITY) {
     p.o[out] = __float2bfloat16_rn(0.f);
-    if (col == 0) p.lse[row] = -INFINITY;
+    if (t == 0) p.lse[row] = -INFINITY;
     return;
   }
-  float den = 0.f, a = 0.f;
-  for (int cc = c0; cc <= c1; ++cc) {
-    const size_t slot = (static_cast<size_t>(cc) + h) * p.Nq + i;
-    const float w = ex2(p.ws_lse[slot] - mx);
-    den += w;
-    a = fmaf(w, p.ws_o[slot * D + col], a);
+  float den = 0.f;
+  for (int k = t; k < n; k += D) {
+    wts[k] = ex2(wts[k] - mx);  // 0 for an empty piece
+    den += wts[k];
   }
+  den = block_reduce(den, false);  // its barrier also publishes wts
+  float a = 0.f;
+#pragma unroll 4
+  for (int k = 0; k < n; ++k) a = fmaf(wts[k], p.ws_o[slot(k) * D + t], a);
   p.o[out] = __float2bfloat16_rn(a / den);
-  if (col == 0) p.lse[row] = (mx + __log2f(den)) * kLn2;
+  if (t == 0) p.lse[row] = (mx + __log2f(den)) * kLn2;
 }
 
 template <int D, int NQ>
