@@ -601,13 +601,11 @@ def run_decode(args, w, fa, q, k, v, cpu, world, rank, local, dev):
 
 
 def forward_kernel_name(w):
-    """Name of the forward kernel the library runs for this workload (the library picks the
-    two-query-tile kernel for dense / causal d = 64, the one-tile kernel otherwise)."""
+    """Name of the forward kernel the library runs for this workload (the two-query-tile kernel
+    for every bf16 forward)."""
     if w.dtype == "fp32":
         return f"fwd_fp32_kernel<{w.d}>"
-    if w.d == 64 and not w.block_sparse:
-        return f"fwd_pair_kernel<{w.d}>"
-    return f"fwd_tc_kernel<{w.d}>"
+    return f"fwd_pair_kernel<{w.d}>"
 
 
 def recorded_traffic(kname, w):
