@@ -160,17 +160,12 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.timeout_ns = kWaitTimeoutNs;
   if (static_cast<long long>(p.n_tiles) * BH > 0x7fffffffll) return FA_ERR_TOO_LARGE;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  // Two kernels: two 128-row query tiles per CTA, each with its own MMA-issuing warp (K/V
-  // streamed once for 256 rows), or one query tile per CTA with double-buffered scores. The pair
-  // kernel is faster on every measured shape (TFLOPS, pair / single): d = 128 causal N = 8192
-  // 1618 / 1376, dense N = 8192 1692 / 1446, causal N = 4096 1251 / 1125, dense B16 N = 512
-  // 593 / 554; d = 64 dense N = 2048 702-728 / ~600; block-sparse d = 64 at 25% density
-  // 678 / 632. The single kernel stays selectable for comparison.
-#ifndef FA_FWD_POLICY
-#define FA_FWD_POLICY 0  // 0 (or 1): the pair kernel; 2: the one-tile kernel
-#endif
-  const bool pair = FA_FWD_POLICY != 2;
-  return to_status(pair ? fa::launch_fwd_pair(p, d, cs) : fa::launch_fwd_tc(p, d, ds->num_sms, cs));
+  // Two 128-row query tiles per CTA, each with its own MMA-issuing warp, K/V streamed once for
+  // 256 rows. It beat a one-query-tile kernel with double-buffered scores on every measured shape
+  // (TFLOPS, pair / single): d = 128 causal N = 8192 1618 / 1376, dense N = 8192 1692 / 1446,
+  // causal N = 4096 1251 / 1125, dense B16 N = 512 593 / 554; d = 64 dense N = 2048 702-728 /
+  // ~600; block-sparse d = 64 at 25% density 678 / 632.
+  return to_status(fa::launch_fwd_pair(p, d, cs));
 }
 
 // CTAs for decoding: as many as the SMs hold at once, never more than there are key blocks.

@@ -6,7 +6,8 @@
 // running row max m, running sum l and an unnormalised accumulator O rescaled by exp(m - m_new),
 // divide by l once at the end. Neither S nor P ever leaves the SM.
 //
-// GB300 mapping (one CTA per SM, 12 warps; used for dense / causal d = 64):
+// GB300 mapping (one CTA per SM, 12 warps; every bf16 forward: d = 64 and 128, dense, causal and
+// block-sparse):
 //   * a CTA owns two 128-row query tiles (t = 0, 1) of one (b, h), so the tensor core works on one
 //     tile's QK^T / PV while the other tile's softmax runs on the CUDA cores, and each K/V tile
 //     streamed from L2 serves 256 query rows;

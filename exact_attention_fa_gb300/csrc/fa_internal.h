@@ -87,7 +87,6 @@ struct DecodeParams {
 };
 
 // Launchers; return a cudaError_t (cudaSuccess on success).
-cudaError_t launch_fwd_tc(const FwdParams& p, int d, int num_sms, cudaStream_t s);    // 1 tile/CTA
 cudaError_t launch_fwd_pair(const FwdParams& p, int d, cudaStream_t s);               // 2 tiles/CTA
 cudaError_t launch_fwd_fp32(const Fp32FwdParams& p, cudaStream_t s);
 cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t s);
