@@ -1,5 +1,6 @@
 """bench.py end to end on the GPU: the JSON line carries every key of the reporting contract, for a
-forward-only workload and for the default forward + backward step (short runs)."""
+forward-only workload, the default forward + backward step and the decoding workload (short
+runs)."""
 import json
 import os
 import subprocess
@@ -23,7 +24,7 @@ def run_bench(*args):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("workload", ["single_head_fp32", "mha_N2048_d64"])
+@pytest.mark.parametrize("workload", ["single_head_fp32", "mha_N2048_d64", "decode_N32768_d128_h8"])
 def test_bench_line(cuda, workload):
     d = run_bench("--workload", workload, "--steps", "3", "--warmup", "3", "--no-cpu-baseline")
     assert KEYS <= set(d), KEYS - set(d)
@@ -31,3 +32,11 @@ def test_bench_line(cuda, workload):
     assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
     assert d["roofline"]["peak"] > 0 and 0 < d["roofline"]["frac"]
     assert d["config"]["workload"] == workload
+
+
+@pytest.mark.gpu
+def test_bench_decode_reports_bandwidth(cuda):
+    d = run_bench("--workload", "decode_N32768_d128_h8", "--steps", "3", "--warmup", "3",
+                  "--no-cpu-baseline", "--no-e2e")
+    assert d["unit"] == "GB/s" and d["roofline"]["bound"] == "hbm" and d["roofline"]["unit"] == "GB/s"
+    assert 0 < d["roofline"]["frac"] < 1.2
