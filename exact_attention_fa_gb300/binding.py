@@ -33,6 +33,8 @@ SIGNATURES = [
     ("fa_bwd_workspace_bytes", ctypes.c_size_t, [_I, _I, _I, _I]),
     ("fa_bwd", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
     ("fa_bwd_noalloc", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    ("fa_bwd_blocksparse", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P,
+                                _P]),
     ("fa_decode", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P]),
     ("fa_decode_ctas", _I, [_I, _I, _I, _I, _I]),
     ("fa_decode_workspace_bytes", ctypes.c_size_t, [_I, _I, _I, _I, _I]),
@@ -152,6 +154,28 @@ def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool, workspac
                                    int(bool(causal)), _ptr(workspace), _stream(q)))
 
 
+def fa_bwd_blocksparse(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool, block_mask,
+                       workspace):
+    """Block-sparse backward: fa_bwd with the forward's uint8 tile mask [ceil(N/128)] * 2."""
+    B, H, N, d = _bhnd(q, k, v, o, do, dk, dv)
+    _bhnd(dq, dtype=torch.float32)
+    if tuple(dq.shape) != tuple(q.shape):
+        raise ValueError("dq must have the shape of q")
+    _rows(lse, q.shape)
+    nt = (N + 127) // 128
+    if (block_mask.dtype != torch.uint8 or tuple(block_mask.shape) != (nt, nt)
+            or not block_mask.is_cuda or not block_mask.is_contiguous()):
+        raise ValueError(f"block_mask must be a contiguous uint8 CUDA tensor [{nt}, {nt}]")
+    need = fa_bwd_workspace_bytes(B, H, N, d)
+    if workspace.numel() * workspace.element_size() < need or not workspace.is_cuda:
+        raise ValueError(f"workspace must hold at least {need} bytes on the device")
+    _check("fa_bwd_blocksparse",
+           load().fa_bwd_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+                                     _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+                                     int(bool(causal)), _ptr(block_mask), _ptr(workspace),
+                                     _stream(q)))
+
+
 def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool):
     """fa_bwd for callers that cannot allocate: the library's static scratch replaces the
     workspace (see include/fa.h for its size limit and sharing rules)."""
@@ -239,13 +263,18 @@ def attention_decode(q, k, v, scale: float | None = None, n_ctas: int = 0):
     return o, lse
 
 
-def attention_backward(q, k, v, o, lse, do, scale: float | None = None, causal: bool = False):
-    """Allocates dq (fp32), dk, dv (bf16) and the workspace, and runs fa_bwd."""
+def attention_backward(q, k, v, o, lse, do, scale: float | None = None, causal: bool = False,
+                       block_mask=None):
+    """Allocates dq (fp32), dk, dv (bf16) and the workspace, and runs fa_bwd (with a tile mask:
+    fa_bwd_blocksparse)."""
     scale = q.shape[-1] ** -0.5 if scale is None else scale
     B, H, N, d = q.shape
     dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
     ws = torch.empty(fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=q.device)
-    fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, causal, ws)
+    if block_mask is not None:
+        fa_bwd_blocksparse(q, k, v, o, do, lse, dq, dk, dv, scale, causal, block_mask, ws)
+    else:
+        fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, causal, ws)
     return dq, dk, dv

@@ -185,11 +185,57 @@ int check_decode(int B, int H, int Nq, int Nk, int d, float scale) {
   return FA_OK;
 }
 
+int bwd_bf16(const void* q, const void* k, const void* v, const void* o, const void* dO,
+             const float* lse, float* dq, void* dk, void* dv, int B, int H, int N, int d,
+             float scale, int causal, bool sparse, const uint8_t* block_mask, void* workspace,
+             fa_stream_t stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace)
+    return FA_ERR_INVALID_ARG;
+  if (sparse && !block_mask) return FA_ERR_INVALID_ARG;
+  int st = check_common(B, H, N, scale);
+  if (st != FA_OK) return st;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (sparse && (N + 127) / 128 > fa::kBwdMaxMaskTiles) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(workspace))
+    return FA_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != FA_OK) return st;
+  fa::BwdParams p{};
+  const int BH = B * H;
+  if (!encode_bf16_map(&p.tm_q, q, BH, N, d) || !encode_bf16_map(&p.tm_k, k, BH, N, d) ||
+      !encode_bf16_map(&p.tm_v, v, BH, N, d) || !encode_bf16_map(&p.tm_do, dO, BH, N, d) ||
+      !encode_f32_map(&p.tm_dq, dq, BH, N, d))
+    return FA_ERR_CUDA;
+  p.o = static_cast<const __nv_bfloat16*>(o);
+  p.dO = static_cast<const __nv_bfloat16*>(dO);
+  p.lse = lse;
+  p.dq = dq;
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  const size_t rows = static_cast<size_t>(BH) * ((static_cast<size_t>(N) + 127) / 128) * 128;
+  p.lse2 = static_cast<float*>(workspace);
+  p.Dsum = static_cast<float*>(workspace) + rows;
+  p.aug = static_cast<uint8_t*>(workspace) + rows * 2 * sizeof(float);
+  p.BH = BH;
+  p.N = N;
+  p.d = d;
+  p.n_tiles = (N + 127) / 128;
+  p.causal = causal ? 1 : 0;
+  p.block_mask = block_mask;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.err = ds->err;
+  p.timeout_ns = kWaitTimeoutNs;
+  return to_status(fa::launch_bwd(p, ds->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
 
-int fa_abi_version(void) { return (2 << 16) | 1; }
+int fa_abi_version(void) { return (2 << 16) | 2; }
 
 const char* fa_status_string(int status) {
   switch (status) {
@@ -244,43 +290,16 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
            const float* lse, float* dq, void* dk, void* dv, int B, int H, int N, int d,
            float scale, int causal, void* workspace, fa_stream_t stream) {
-  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace)
-    return FA_ERR_INVALID_ARG;
-  int st = check_common(B, H, N, scale);
-  if (st != FA_OK) return st;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
-      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
-      !aligned16(workspace))
-    return FA_ERR_MISALIGNED;
-  DeviceState* ds = nullptr;
-  if ((st = device_state(&ds)) != FA_OK) return st;
-  fa::BwdParams p{};
-  const int BH = B * H;
-  if (!encode_bf16_map(&p.tm_q, q, BH, N, d) || !encode_bf16_map(&p.tm_k, k, BH, N, d) ||
-      !encode_bf16_map(&p.tm_v, v, BH, N, d) || !encode_bf16_map(&p.tm_do, dO, BH, N, d) ||
-      !encode_f32_map(&p.tm_dq, dq, BH, N, d))
-    return FA_ERR_CUDA;
-  p.o = static_cast<const __nv_bfloat16*>(o);
-  p.dO = static_cast<const __nv_bfloat16*>(dO);
-  p.lse = lse;
-  p.dq = dq;
-  p.dk = static_cast<__nv_bfloat16*>(dk);
-  p.dv = static_cast<__nv_bfloat16*>(dv);
-  const size_t rows = static_cast<size_t>(BH) * ((static_cast<size_t>(N) + 127) / 128) * 128;
-  p.lse2 = static_cast<float*>(workspace);
-  p.Dsum = static_cast<float*>(workspace) + rows;
-  p.aug = static_cast<uint8_t*>(workspace) + rows * 2 * sizeof(float);
-  p.BH = BH;
-  p.N = N;
-  p.d = d;
-  p.n_tiles = (N + 127) / 128;
-  p.causal = causal ? 1 : 0;
-  p.scale = scale;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.err = ds->err;
-  p.timeout_ns = kWaitTimeoutNs;
-  return to_status(fa::launch_bwd(p, ds->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+  return bwd_bf16(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, false, nullptr,
+                  workspace, stream);
+}
+
+int fa_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o,
+                       const void* dO, const float* lse, float* dq, void* dk, void* dv, int B,
+                       int H, int N, int d, float scale, int causal, const uint8_t* block_mask,
+                       void* workspace, fa_stream_t stream) {
+  return bwd_bf16(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, true, block_mask,
+                  workspace, stream);
 }
 
 int fa_decode_ctas(int B, int H, int Nq, int Nk, int d) {

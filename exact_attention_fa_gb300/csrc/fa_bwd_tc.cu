@@ -46,6 +46,27 @@ constexpr int kThreads = 16 * 32;
 // warpgroups take the difference.
 
 constexpr int kBoxBytes = 128 * 64 * 2;
+constexpr int kMaxMaskTiles = kBwdMaxMaskTiles;  // block-sparse: query tiles the bitmask holds
+
+// The query tiles a CTA (key tile j) visits, in order: [first, n_tiles) (first = j when causal),
+// and with a tile mask (kMask, a separate kernel instance) only those whose mask entry M[i][j] is
+// set. The mask column is turned into a bitmask in shared memory once per CTA, so each role's
+// next() is a few integer operations; without a mask it is the identity.
+template <bool kMask>
+struct QueryPlan {
+  const uint32_t* bits;  // shared memory (kMask)
+  int first, n_tiles;
+  __device__ __forceinline__ int next(int i) const {
+    if constexpr (!kMask) return i;
+    while (i < n_tiles) {
+      const uint32_t w = bits[i >> 5] >> (i & 31);
+      if (w) return i + __ffs(w) - 1;
+      i = (i | 31) + 1;
+    }
+    return n_tiles;
+  }
+  __device__ __forceinline__ int begin() const { return next(first); }
+};
 
 template <int D>
 struct BCfg {
@@ -98,7 +119,8 @@ struct BCfg {
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffTmemPtr = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemPtr + 4;
-  static constexpr int kSmemBytes = kOffAbort + 4;  // the base must be 1024-aligned (checked)
+  static constexpr int kOffQMask = kOffAbort + 12;  // block-sparse: query tiles to visit (bits)
+  static constexpr int kSmemBytes = kOffQMask + kMaxMaskTiles / 8;  // base 1024-aligned (checked)
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
   // d = 64 has room for dQ_i in its own columns; at d = 128 it reuses the dP^T columns.
   static constexpr bool kDQAliasesDP = D == 128;
@@ -130,9 +152,9 @@ __device__ __forceinline__ void decode_bwd(const BwdParams& p, int group, int& b
 // packs them as bf16 pairs into columns [64c, 64c+32), so K-step k (queries 16k .. 16k+15) reads
 // the 8 columns at k < 4 ? 8k : 64 + 8(k - 4) (mma_ts_k128_halves).
 
-template <int D>
+template <int D, class Plan>
 __device__ void bwd_producer(const BwdParams& p, uint32_t sbase, const Ctl& ctl, int bh, int j,
-                             int i0, int npad) {
+                             const Plan& plan, int npad) {
   using C = BCfg<D>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
   tma_prefetch_desc(&p.tm_q);
@@ -148,7 +170,7 @@ __device__ void bwd_producer(const BwdParams& p, uint32_t sbase, const Ctl& ctl,
 #pragma unroll
   for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
   bool ok = true;
-  for (int i = i0, it = 0; i < p.n_tiles; ++i, ++it) {
+  for (int i = plan.begin(), it = 0; i < p.n_tiles; i = plan.next(i + 1), ++it) {
     const int st = it % C::kStages;
     const int round = it / C::kStages;
     if (!mbar_wait_warp(bar(C::kBarEmpty + st), (round & 1) ^ 1, ctl)) { ok = false; break; }
@@ -183,8 +205,9 @@ __device__ void bwd_producer(const BwdParams& p, uint32_t sbase, const Ctl& ctl,
   }
 }
 
-template <int D>
-__device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const Ctl& ctl, int i0) {
+template <int D, class Plan>
+__device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const Ctl& ctl,
+                        const Plan& plan) {
   using C = BCfg<D>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
   constexpr uint32_t kIdescT = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T: both K-major
@@ -246,7 +269,8 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
     mma_commit(bar(C::kBarDP));
     return true;
   };
-  if (ok && i0 < p.n_tiles) {
+  const int ibeg = plan.begin();
+  if (ok && ibeg < p.n_tiles) {
     ok = mbar_wait_poll_warp(bar(C::kBarFull + 0), 0, ctl);
     tc_fence_after();
     if (ok) {
@@ -255,7 +279,7 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
     }
   }
   const int n_tiles = p.n_tiles;
-  for (int i = i0, it = 0; ok && i < n_tiles; ++i, ++it) {
+  for (int i = ibeg, it = 0; ok && i < n_tiles; i = plan.next(i + 1), ++it) {
     const int st = it % C::kStages;
     const uint64_t q_mn = st_mn + st * kStageStep;
     const uint64_t do_mn = q_mn + kDOOff;
@@ -272,7 +296,7 @@ __device__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem, const
     mma_ts_k128_halves(tDV, tS, do_mn, kIdescG, it > 0 ? 1u : 0u);
     // S^T of the next query tile overwrites P^T: the tensor core runs MMAs in issue order, so
     // the dV product above has read P^T first; the compute warps overlap it with dK, dQ below.
-    const bool has_next = i + 1 < n_tiles;
+    const bool has_next = plan.next(i + 1) < n_tiles;
     if (has_next) {
       const int nx = it + 1;
       if (!mbar_wait_poll_warp(bar(C::kBarFull + nx % C::kStages), (nx / C::kStages) & 1, ctl)) { ok = false; break; }
@@ -360,9 +384,9 @@ __device__ __forceinline__ void bwd_p_tile(uint32_t tS, const float4* lse4, unsi
   }
 }
 
-template <int D>
+template <int D, class Plan>
 __device__ void bwd_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, uint32_t tmem,
-                            const Ctl& ctl, int bh, int j, int i0) {
+                            const Ctl& ctl, int bh, int j, const Plan& plan) {
   using C = BCfg<D>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -378,7 +402,9 @@ __device__ void bwd_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, u
   uint8_t* ds_row = smem + C::kOffDS + half * kBoxBytes + r * 128;
 
   bool ok = true;
-  for (int i = i0, it = 0; i < p.n_tiles; ++i, ++it) {
+  int n_done = 0;  // query tiles processed
+  for (int i = plan.begin(), it = 0; i < p.n_tiles; i = plan.next(i + 1), ++it) {
+    n_done = it + 1;
     const int st = it % C::kStages;
     const float* lse2 = reinterpret_cast<const float*>(smem + C::kOffStage + st * C::kStageBytes +
                                                        C::kStageLse) + 64 * half;
@@ -483,6 +509,10 @@ __device__ void bwd_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, u
     for (int c = 0; c < kHalf; c += 32) {
       uint32_t v[32];
       tmem_ld32(tmem + lane_off + col + c, v);
+      if (n_done == 0) {  // no query tile visits this key tile: dK = dV = 0 (TMEM never written)
+#pragma unroll
+        for (int u = 0; u < 32; ++u) v[u] = 0u;
+      }
       if (key < p.N) {
         uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
@@ -502,9 +532,9 @@ __device__ void bwd_compute(const BwdParams& p, uint32_t sbase, uint8_t* smem, u
 // dQ_i (TMEM, thread = query row) -> scale -> swizzled fp32 staging tile in shared memory ->
 // bulk tensor reduction into the fp32 output (coalesced adds at L2, done by the TMA unit). The
 // TMEM columns are handed back as soon as they are read, the staging tile once the TMA has read it.
-template <int D>
+template <int D, class Plan>
 __device__ void bwd_drain(const BwdParams& p, uint32_t sbase, uint8_t* smem, uint32_t tmem,
-                          const Ctl& ctl, int bh, int i0) {
+                          const Ctl& ctl, int bh, const Plan& plan) {
   using C = BCfg<D>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -514,7 +544,7 @@ __device__ void bwd_drain(const BwdParams& p, uint32_t sbase, uint8_t* smem, uin
   const uint32_t tQ = tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::kColDQ;
   constexpr uint32_t kBox = 64 * 128;       // one TMA box: 64 rows x 128 B
   constexpr uint32_t kColBox = 128 * 128;   // 32 columns of the 128 rows
-  for (int i = i0, it = 0; i < p.n_tiles; ++i, ++it) {
+  for (int i = plan.begin(), it = 0; i < p.n_tiles; i = plan.next(i + 1), ++it) {
     const bool bad = !mbar_wait(bar(C::kBarDQFull), it & 1, ctl);
     if (bar_red_or(1, 128, bad)) return;
     tc_fence_after();
@@ -567,9 +597,9 @@ __device__ __forceinline__ void red_add_f32(float* addr, float v) {
 // dQ_i^T (TMEM, thread = column d of dQ, 128 query columns) -> scale -> fp32 reductions: for each
 // query a warp adds 32 consecutive floats (128 bytes, one coalesced request). The TMEM columns are
 // handed back right after the single load, before the reductions are issued.
-template <int D>
+template <int D, class Plan>
 __device__ void bwd_drain_transposed(const BwdParams& p, uint32_t sbase, uint32_t tmem,
-                                     const Ctl& ctl, int bh, int i0) {
+                                     const Ctl& ctl, int bh, const Plan& plan) {
   using C = BCfg<D>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -577,7 +607,7 @@ __device__ void bwd_drain_transposed(const BwdParams& p, uint32_t sbase, uint32_
   const int dcol = quad * 32 + lane;  // column of dQ (TMEM lane)
   const uint32_t tQ = tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::kColDQ;
   const float scale = p.scale;
-  for (int i = i0, it = 0; i < p.n_tiles; ++i, ++it) {
+  for (int i = plan.begin(), it = 0; i < p.n_tiles; i = plan.next(i + 1), ++it) {
     const bool bad = !mbar_wait(bar(C::kBarDQFull), it & 1, ctl);
     if (bar_red_or(1, 128, bad)) return;
     tc_fence_after();
@@ -603,7 +633,7 @@ __device__ void bwd_drain_transposed(const BwdParams& p, uint32_t sbase, uint32_
   }
 }
 
-template <int D>
+template <int D, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_constant__ BwdParams p,
                                                              int group, int npad) {
   using C = BCfg<D>;
@@ -620,7 +650,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   const int warp = threadIdx.x / 32;
   int bh, j;
   decode_bwd(p, group, bh, j);
-  const int i0 = p.causal ? j : 0;
+  uint32_t* qbits = reinterpret_cast<uint32_t*>(smem + C::kOffQMask);
+  const QueryPlan<kMask> plan{qbits, p.causal ? j : 0, p.n_tiles};
+  if (kMask) {
+    // column j of the tile mask -> bitmask of the query tiles to visit (one load per thread)
+    for (int i0 = warp * 32; i0 < p.n_tiles; i0 += kThreads) {
+      const int i = i0 + static_cast<int>(threadIdx.x % 32);
+      const bool on = i < p.n_tiles && __ldg(p.block_mask + static_cast<size_t>(i) * p.n_tiles + j) != 0;
+      const uint32_t w = __ballot_sync(0xffffffffu, on);
+      if (threadIdx.x % 32 == 0) qbits[i0 / 32] = w;
+    }
+  }
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -663,13 +703,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 
   if (warp < kComputeWarps) {
     if constexpr (C::kRegsCompute > 128) regs_inc<C::kRegsCompute>();
-    bwd_compute<D>(p, sbase, smem, tmem, ctl, bh, j, i0);
+    bwd_compute<D>(p, sbase, smem, tmem, ctl, bh, j, plan);
   } else if (warp < kDrainWarp0) {
     regs_dec<C::kRegsLoadMma>();
     if (warp == kLoadWarp) {
-      bwd_producer<D>(p, sbase, ctl, bh, j, i0, npad);  // whole warp: one elected lane issues
+      bwd_producer<D>(p, sbase, ctl, bh, j, plan, npad);  // whole warp: one elected lane issues
     } else if (warp == kMmaWarp) {
-      bwd_mma<D>(p, sbase, tmem, ctl, i0);  // whole warp: one elected lane issues
+      bwd_mma<D>(p, sbase, tmem, ctl, plan);  // whole warp: one elected lane issues
     }
     __syncwarp();
   } else {
@@ -678,9 +718,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     else
       regs_dec<C::kRegsDrain>();
     if (C::kDQTransposed)
-      bwd_drain_transposed<D>(p, sbase, tmem, ctl, bh, i0);
+      bwd_drain_transposed<D>(p, sbase, tmem, ctl, bh, plan);
     else
-      bwd_drain<D>(p, sbase, smem, tmem, ctl, bh, i0);
+      bwd_drain<D>(p, sbase, smem, tmem, ctl, bh, plan);
   }
 
   tc_fence_before();
@@ -764,9 +804,11 @@ cudaError_t launch_d(const BwdParams& p, int num_sms, cudaStream_t s) {
   using C = BCfg<D>;
   static bool configured = false;
   if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
+    for (auto k : {bwd_tc_kernel<D, false>, bwd_tc_kernel<D, true>}) {
+      const cudaError_t e =
+          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+      if (e != cudaSuccess) return e;
+    }
     configured = true;
   }
   const int npad = p.n_tiles * BT;
@@ -778,7 +820,10 @@ cudaError_t launch_d(const BwdParams& p, int num_sms, cudaStream_t s) {
   const int group = static_cast<int>(g < 1 ? 1 : (g > p.BH ? p.BH : g));
   const long long grid = static_cast<long long>(p.n_tiles) * p.BH;
   if (grid > 0x7fffffffll) return cudaErrorInvalidConfiguration;
-  bwd_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, s>>>(p, group, npad);
+  if (p.block_mask)
+    bwd_tc_kernel<D, true><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, s>>>(p, group, npad);
+  else
+    bwd_tc_kernel<D, false><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, s>>>(p, group, npad);
   return cudaGetLastError();
 }
 

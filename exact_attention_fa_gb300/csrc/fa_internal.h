@@ -39,6 +39,9 @@ struct Fp32FwdParams {
   float scale_log2;
 };
 
+// Block-sparse backward: largest tile mask (query tiles) a CTA's shared-memory bitmask holds.
+constexpr int kBwdMaxMaskTiles = 2048;
+
 struct BwdParams {
   CUtensorMap tm_q;
   CUtensorMap tm_k;
@@ -56,6 +59,7 @@ struct BwdParams {
   // workspace, d = 64: per 128-row tile two 4 KB bf16 operand tiles (128 rows x 16, K-major,
   // no swizzle) holding -lse2 / scale_log2 and -D, each split into three bf16 parts
   uint8_t* aug;
+  const uint8_t* block_mask;  // [n_tiles][n_tiles] tile mask (row = query tile), or null
   int BH, N, d;
   int n_tiles;
   int causal;

@@ -94,6 +94,17 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            const float* lse, float* dq, void* dk, void* dv, int B, int H, int N, int d,
            float scale, int causal, void* workspace, fa_stream_t stream);
 
+/* Block-sparse backward ("FlashAttention: IOを意識した..." (xyznot.com), "拡張: Block-Sparse
+ * FlashAttention": the tile mask skips the same tiles in the backward). Same arguments, results
+ * and workspace as fa_bwd, plus block_mask: the DEVICE uint8 [T][T] tile mask (T = ceil(N/128),
+ * row = query tile) the forward used, combined with the causal mask when causal != 0. o and lse
+ * must come from fa_fwd_blocksparse with the same mask. A key tile that no query tile visits gets
+ * dK = dV = 0. T <= 2048 (FA_ERR_UNSUPPORTED above). */
+int fa_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o,
+                       const void* dO, const float* lse, float* dq, void* dk, void* dv, int B,
+                       int H, int N, int d, float scale, int causal, const uint8_t* block_mask,
+                       void* workspace, fa_stream_t stream);
+
 /* Bytes of device scratch built into the library for fa_bwd_noalloc (per device). */
 #define FA_NOALLOC_SCRATCH_BYTES (4u << 20)
 
@@ -156,7 +167,7 @@ int fa_check_device_error(fa_stream_t stream);
 const char* fa_status_string(int status);
 
 /* ABI version: (major << 16) | minor. Major 2: fa_fwd_blocksparse takes a causal flag; minor 1:
- * fa_decode. */
+ * fa_decode; minor 2: fa_bwd_blocksparse. */
 int fa_abi_version(void);
 
 #ifdef __cplusplus

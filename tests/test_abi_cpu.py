@@ -106,6 +106,14 @@ def test_decode_workspace_and_ctas(lib):
     assert lib.fa_decode_ctas(1, 1, 9, 100, 64) == 0
 
 
+def test_bwd_blocksparse_validation(lib):
+    ptrs = [fake()] * 9
+    assert lib.fa_bwd_blocksparse(*ptrs, 1, 1, 256, 64, 0.125, 0, P(0), fake(), None) == 1  # mask
+    assert lib.fa_bwd_blocksparse(*ptrs, 1, 1, 256, 96, 0.125, 0, fake(), fake(), None) == 2
+    # more query tiles than the kernel's bitmask holds (2048 tiles)
+    assert lib.fa_bwd_blocksparse(*ptrs, 1, 1, 2049 * 128, 64, 0.125, 0, fake(), fake(), None) == 2
+
+
 def test_fp32_validation(lib):
     base = (fake(), fake(), fake(), fake(), fake(), 1, 1, 64)
     assert lib.fa_fwd_fp32(*base, 48, 0.125, 0, None) == 2

@@ -16,11 +16,16 @@ from oracle import attention as orc
 pytestmark = pytest.mark.gpu
 
 
-def run_bwd(w: wl.Workload, device, heads=None):
+def run_bwd(w: wl.Workload, device, heads=None, mask_np=None):
+    """mask_np: a uint8 tile mask to use instead of the workload's own (block-sparse only)."""
     inp = wl.make_inputs(w, with_do=True)
     q, k, v, do = (H.to_device(inp, n, device) for n in ("q", "k", "v", "do"))
-    o, lse = fa.attention_forward(q, k, v, w.softmax_scale, causal=w.causal)
-    dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, w.softmax_scale, causal=w.causal)
+    if w.block_sparse and mask_np is None:
+        mask_np = inp.raw("mask")
+    mask = torch.from_numpy(mask_np).to(device) if mask_np is not None else None
+    o, lse = fa.attention_forward(q, k, v, w.softmax_scale, causal=w.causal, block_mask=mask)
+    dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, w.softmax_scale, causal=w.causal,
+                                       block_mask=mask)
     fa.fa_check_device_error()
     got = {n: t.float().cpu().numpy() for n, t in (("dq", dq), ("dk", dk), ("dv", dv))}
     for n, t in got.items():
@@ -35,7 +40,7 @@ def run_bwd(w: wl.Workload, device, heads=None):
     have = {"dq": [], "dk": [], "dv": []}
     for b, h in all_heads:
         gq, gk, gv = orc.backward_head(qf[b, h], kf[b, h], vf[b, h], dof[b, h], w.softmax_scale,
-                                       causal=w.causal)
+                                       causal=w.causal, block_mask=mask_np)
         for n, g in (("dq", gq), ("dk", gk), ("dv", gv)):
             want[n].append(g)
             have[n].append(got[n][b, h])
@@ -55,6 +60,32 @@ def run_bwd(w: wl.Workload, device, heads=None):
 @pytest.mark.parametrize("N", [1, 64, 128, 200, 384])
 def test_bwd_small(cuda, N, d, causal):
     run_bwd(wl.Workload("bwd_small", 2, 2, N, d, causal=causal, seed=41), cuda)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [300, 1024])
+def test_bwd_blocksparse_small(cuda, N, d, causal):
+    run_bwd(wl.Workload("bwd_bs", 2, 2, N, d, causal=causal, block_sparse=True, seed=44), cuda)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_blocksparse_unvisited_key_tile(cuda, d):
+    """Key tile 1 is in no query tile's mask row: its dK and dV are exactly zero."""
+    m = np.array([[1, 0, 0], [1, 0, 0], [1, 0, 1]], np.uint8)
+    w = wl.Workload("bwd_bs_empty", 1, 2, 300, d, block_sparse=True, seed=45)
+    run_bwd(w, cuda, mask_np=m)
+    inp = wl.make_inputs(w, with_do=True)
+    q, k, v, do = (H.to_device(inp, n, cuda) for n in ("q", "k", "v", "do"))
+    mt = torch.from_numpy(m).to(cuda)
+    o, lse = fa.attention_forward(q, k, v, w.softmax_scale, block_mask=mt)
+    _, dk, dv = fa.attention_backward(q, k, v, o, lse, do, w.softmax_scale, block_mask=mt)
+    assert torch.all(dk[:, :, 128:256] == 0) and torch.all(dv[:, :, 128:256] == 0)
+
+
+def test_bwd_blocksparse_N4096_d64_sampled(cuda):
+    w = wl.Workload("bwd_bs_4096", 1, 8, 4096, 64, block_sparse=True, seed=46)
+    run_bwd(w, cuda, heads=2)
 
 
 def test_bwd_big_scores(cuda):

@@ -339,12 +339,14 @@ def test_backward_matches_finite_differences(causal):
         assert np.max(np.abs(num - g)) < 1e-7 * max(1.0, np.max(np.abs(g))), name
 
 
-def test_backward_block_mask_matches_finite_differences():
-    n, d, tile = 12, 4, 4
+@pytest.mark.parametrize("n,causal", [(12, False), (10, True)])
+def test_backward_block_mask_matches_finite_differences(n, causal):
+    """Tile mask alone, and combined with the causal mask on a ragged size (last tile 2 rows)."""
+    d, tile = 4, 4
     rng = np.random.default_rng(18)
     q, k, v, do = (rng.standard_normal((n, d)) for _ in range(4))
     bm = np.array([[1, 0, 1], [0, 1, 0], [1, 1, 1]], np.uint8)
-    dq, dk, dv = orc.backward_head(q, k, v, do, 0.5, block_mask=bm, tile=tile)
+    dq, dk, dv = orc.backward_head(q, k, v, do, 0.5, causal=causal, block_mask=bm, tile=tile)
     h = 1e-6
     for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
         num = np.zeros_like(x)
@@ -354,8 +356,8 @@ def test_backward_block_mask_matches_finite_differences():
             xm[idx] -= h
             a_p = {"q": q, "k": k, "v": v, name: xp}
             a_m = {"q": q, "k": k, "v": v, name: xm}
-            num[idx] = (loss(a_p["q"], a_p["k"], a_p["v"], do, 0.5, False, bm, tile)
-                        - loss(a_m["q"], a_m["k"], a_m["v"], do, 0.5, False, bm, tile)) / (2 * h)
+            num[idx] = (loss(a_p["q"], a_p["k"], a_p["v"], do, 0.5, causal, bm, tile)
+                        - loss(a_m["q"], a_m["k"], a_m["v"], do, 0.5, causal, bm, tile)) / (2 * h)
         assert np.max(np.abs(num - g)) < 1e-7 * max(1.0, np.max(np.abs(g))), name
 
 
