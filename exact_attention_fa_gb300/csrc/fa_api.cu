@@ -170,7 +170,7 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
 
 // CTAs for decoding: as many as the SMs hold at once, never more than there are key blocks.
 int decode_auto_ctas(int BH, int Nk, int d, int num_sms) {
-  constexpr int kB = fa::kDecodeBlockKeys;
+  constexpr int kB = fa::kDecodeMinBlockKeys;
   const long long blocks = static_cast<long long>(BH) * ((Nk + kB - 1) / kB);
   long long n = static_cast<long long>(num_sms) * fa::decode_ctas_per_sm(d);
   if (n > fa::kDecodeMaxCtas) n = fa::kDecodeMaxCtas;
@@ -312,7 +312,7 @@ int fa_decode_ctas(int B, int H, int Nq, int Nk, int d) {
 size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
   if (check_decode(B, H, Nq, Nk, d, 1.f) != FA_OK) return 0;
   const long long BH = static_cast<long long>(B) * H;
-  long long ctas = BH * ((Nk + fa::kDecodeBlockKeys - 1) / fa::kDecodeBlockKeys);
+  long long ctas = BH * ((Nk + fa::kDecodeMinBlockKeys - 1) / fa::kDecodeMinBlockKeys);
   if (ctas > fa::kDecodeMaxCtas) ctas = fa::kDecodeMaxCtas;
   return static_cast<size_t>((ctas + BH) * Nq * (d + 1)) * sizeof(float);
 }
@@ -330,11 +330,8 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != FA_OK) return st;
   const int BH = B * H;
-  const int nb = (Nk + fa::kDecodeBlockKeys - 1) / fa::kDecodeBlockKeys;
-  const long long blocks = static_cast<long long>(BH) * nb;
   if (n_ctas == 0) n_ctas = decode_auto_ctas(BH, Nk, d, ds->num_sms);
-  if (n_ctas > blocks) n_ctas = static_cast<int>(blocks);
-  fa::DecodeParams p{};
+  fa::DecodeParams p{};  // the launcher sets the block count and caps n_ctas at it
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);
   p.v = static_cast<const __nv_bfloat16*>(v);
@@ -343,10 +340,8 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.BH = BH;
   p.Nq = Nq;
   p.Nk = Nk;
-  p.blocks_per_head = nb;
   p.n_ctas = n_ctas;
   p.ws_o = static_cast<float*>(workspace);
-  p.ws_lse = p.ws_o + static_cast<size_t>(n_ctas + BH) * Nq * d;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.err = ds->err;
   p.timeout_ns = kWaitTimeoutNs;

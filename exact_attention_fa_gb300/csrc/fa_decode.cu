@@ -4,19 +4,20 @@
 // With Nq <= 8 query rows per head the work is a matrix-vector product: every key and value row
 // is used Nq times, so the kernel is bound by HBM bandwidth, not by arithmetic, and the tensor
 // cores would sit idle (128-row MMA tiles for a handful of rows). GB300 mapping:
-//   * Flash-Decoding's split of the keys, balanced for a fixed grid: the key blocks (32 keys) of
-//     all heads, head after head, are dealt out as G equal contiguous ranges, one per CTA, with
-//     G = the CTAs the SMs hold at once (persistent: no tail wave, every SM streams until the
-//     end). A range may start or end inside a head and may span several heads;
+//   * Flash-Decoding's split of the keys, balanced for a fixed grid: the key blocks (32 keys at
+//     d = 128, 64 at d = 64: 16 KB of K and V either way) of all heads, head after head, are
+//     dealt out as G equal contiguous ranges, one per CTA, with G = the CTAs the SMs hold at
+//     once (persistent: no tail wave, every SM streams until the end). A range may start or end
+//     inside a head and may span several heads;
 //   * one warp of the CTA streams its range with 1-D bulk copies (cp.async.bulk) into per-warp
 //     shared-memory rings of (K block, V block) pairs (128 KB in flight per CTA), across head
 //     boundaries, guarded by full / empty mbarriers;
 //   * eight compute warps take the blocks in turn, each with an online softmax state of its own
-//     ("3 · FlashAttention", 3.3): lane = key for the scores q.k (16-byte loads rotated by lane,
-//     so no bank conflicts), warp shuffles for the block's max and sum, lane = 4 output columns
-//     for O += P V (at d = 64 the two half-warps take alternate keys). No CTA-wide barrier per
-//     block: the warps meet only where a head ends inside the range, to merge their states into
-//     that (CTA, head) piece;
+//     ("3 · FlashAttention", 3.3): lane = key (two keys at d = 64) for the scores q.k (16-byte
+//     loads rotated by lane, so no bank conflicts), warp shuffles for the block's max and sum,
+//     lane = 4 output columns for O += P V (at d = 64 the two half-warps take alternate keys).
+//     No CTA-wide barrier per block: the warps meet only where a head ends inside the range, to
+//     merge their states into that (CTA, head) piece;
 //   * each piece holds O_c / l_c and its log-sum-exp lse_c; a second kernel merges the pieces of
 //     each head with the same statistics merge as the blockwise forward (lse = log Σ exp lse_c,
 //     O = Σ exp(lse_c - lse) O_c).
@@ -31,16 +32,19 @@ namespace {
 
 constexpr int kWarps = 8;              // compute warps; warp kWarps streams the blocks in
 constexpr int kThreads = 32 * (kWarps + 1);
-constexpr int kBK = kDecodeBlockKeys;  // keys per block: one key per lane
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D>
 struct DCfg {
   // Each compute warp has a ring of its own (one consumer per stage, so the phase parity of a
-  // stage's barrier always refers to the block the warp expects): 1 stage per warp at d = 128
-  // (16 KB blocks), 2 at d = 64 (8 KB); 128 KB in flight per CTA either way.
-  static constexpr int kStagesPerWarp = D == 128 ? 1 : 2;
+  // stage's barrier always refers to the block the warp expects): one 16 KB stage per warp,
+  // 128 KB in flight per CTA.
+  static constexpr int kStagesPerWarp = 1;
   static constexpr int kStages = kWarps * kStagesPerWarp;
+  // keys per block: 16 KB per (K, V) block pair either way, so one key per lane at d = 128 and two
+  // at d = 64 (lanes l and l + 32)
+  static constexpr int kBK = D == 128 ? 32 : 64;
+  static constexpr int kKeysPerLane = kBK / 32;
   static constexpr int kBlockBytes = kBK * D * 2;  // one K or V block, bf16
   static constexpr int kStageBytes = 2 * kBlockBytes;
   static constexpr int kOffQ = kStages * kStageBytes;                // fp32 [kDecodeMaxNq][D]
@@ -83,6 +87,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const __grid
   auto stage_of = [&](int i) { return (i % kWarps) * R + (i / kWarps) % R; };
   auto parity_of = [&](int i) { return static_cast<uint32_t>((i / kWarps / R) & 1); };
   constexpr int kKS = C::kKeySplit;
+  constexpr int kBK = C::kBK;
+  constexpr int kKPL = C::kKeysPerLane;
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -172,46 +178,59 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const __grid
       const __nv_bfloat16* Ks = reinterpret_cast<const __nv_bfloat16*>(smem + s * C::kStageBytes);
       const __nv_bfloat16* Vs = Ks + kBK * D;
 
-      // scores of key `lane` (16-byte chunks in an order rotated by lane: no bank conflicts),
-      // four partial sums per query row for short dependency chains
-      float sc[NQ][4];
+      // scores of keys lane + 32 u (16-byte chunks in an order rotated by lane: no bank
+      // conflicts), two partial sums per key and query row for short dependency chains
+      float sc[NQ][kKPL][2];
 #pragma unroll
       for (int j = 0; j < NQ; ++j)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) sc[j][u] = 0.f;
-      if (lane < n) {
+        for (int u = 0; u < kKPL; ++u) sc[j][u][0] = sc[j][u][1] = 0.f;
 #pragma unroll
-        for (int cc = 0; cc < kChunks; ++cc) {
-          const int ch = (cc + lane) % kChunks;
-          float kf[8];
-          bf16x8_to_f32(*reinterpret_cast<const uint4*>(Ks + lane * D + ch * 8), kf);
+      for (int u = 0; u < kKPL; ++u) {
+        const int key = lane + 32 * u;
+        if (key < n) {
 #pragma unroll
-          for (int j = 0; j < NQ; ++j) {
-            if (j < Nq) {
-              const float4 qa = *reinterpret_cast<const float4*>(qs + j * D + ch * 8);
-              const float4 qb = *reinterpret_cast<const float4*>(qs + j * D + ch * 8 + 4);
-              float a = sc[j][cc % 4];
-              a = fmaf(qa.x, kf[0], a); a = fmaf(qa.y, kf[1], a);
-              a = fmaf(qa.z, kf[2], a); a = fmaf(qa.w, kf[3], a);
-              a = fmaf(qb.x, kf[4], a); a = fmaf(qb.y, kf[5], a);
-              a = fmaf(qb.z, kf[6], a); a = fmaf(qb.w, kf[7], a);
-              sc[j][cc % 4] = a;
+          for (int cc = 0; cc < kChunks; ++cc) {
+            const int ch = (cc + lane) % kChunks;
+            float kf[8];
+            bf16x8_to_f32(*reinterpret_cast<const uint4*>(Ks + key * D + ch * 8), kf);
+#pragma unroll
+            for (int j = 0; j < NQ; ++j) {
+              if (j < Nq) {
+                const float4 qa = *reinterpret_cast<const float4*>(qs + j * D + ch * 8);
+                const float4 qb = *reinterpret_cast<const float4*>(qs + j * D + ch * 8 + 4);
+                float a = sc[j][u][cc % 2];
+                a = fmaf(qa.x, kf[0], a); a = fmaf(qa.y, kf[1], a);
+                a = fmaf(qa.z, kf[2], a); a = fmaf(qa.w, kf[3], a);
+                a = fmaf(qb.x, kf[4], a); a = fmaf(qb.y, kf[5], a);
+                a = fmaf(qb.z, kf[6], a); a = fmaf(qb.w, kf[7], a);
+                sc[j][u][cc % 2] = a;
+              }
             }
           }
         }
       }
-      // online softmax per query row (the block's 32 scores sit one per lane)
-      float pj[NQ];
+      // online softmax per query row (the block's scores sit kKPL per lane)
+      float pj[NQ][kKPL];
 #pragma unroll
       for (int j = 0; j < NQ; ++j) {
         if (j < Nq) {
-          const float sj = lane < n ? (sc[j][0] + sc[j][1]) + (sc[j][2] + sc[j][3]) : -INFINITY;
-          float mx = sj;
+          float sj[kKPL];
+          float mx = -INFINITY;
+#pragma unroll
+          for (int u = 0; u < kKPL; ++u) {
+            sj[u] = lane + 32 * u < n ? sc[j][u][0] + sc[j][u][1] : -INFINITY;
+            mx = fmaxf(mx, sj[u]);
+          }
 #pragma unroll
           for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, o));
           const float m_new = fmaxf(m[j], mx);  // finite: the block has at least one key
-          pj[j] = ex2(sj - m_new);
-          float ps = pj[j];
+          float ps = 0.f;
+#pragma unroll
+          for (int u = 0; u < kKPL; ++u) {
+            pj[j][u] = ex2(sj[u] - m_new);
+            ps += pj[j][u];
+          }
 #pragma unroll
           for (int o = 16; o; o >>= 1) ps += __shfl_xor_sync(~0u, ps, o);
           const float alpha = ex2(m[j] - m_new);  // 0 while nothing was accumulated
@@ -234,7 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const __grid
 #pragma unroll
           for (int j = 0; j < NQ; ++j) {
             if (j < Nq) {
-              const float pk = __shfl_sync(~0u, pj[j], key);
+              // key's P sits in lane key % 32, slot key / 32 (the same slot for both
+              // half-warps: k0 + u * kKS is even)
+              const float pk = __shfl_sync(~0u, pj[j][(k0 + u * kKS) >> 5], key & 31);
 #pragma unroll
               for (int t = 0; t < 4; ++t) acc[j][t] = fmaf(pk, vf[t], acc[j][t]);
             }
@@ -356,7 +377,14 @@ cudaError_t launch_nq(const DecodeParams& p, cudaStream_t s) {
 }
 
 template <int D>
-cudaError_t launch(const DecodeParams& p, cudaStream_t s) {
+cudaError_t launch(const DecodeParams& p_in, cudaStream_t s) {
+  // the block size is the kernel's: blocks per head, the CTA count (at most one per block) and
+  // the pieces' layout in the workspace follow from it
+  DecodeParams p = p_in;
+  p.blocks_per_head = (p.Nk + DCfg<D>::kBK - 1) / DCfg<D>::kBK;
+  const long long blocks = static_cast<long long>(p.BH) * p.blocks_per_head;
+  if (p.n_ctas > blocks) p.n_ctas = static_cast<int>(blocks);
+  p.ws_lse = p.ws_o + static_cast<size_t>(p.n_ctas + p.BH) * p.Nq * D;
   cudaError_t e = p.Nq <= 1   ? launch_nq<D, 1>(p, s)
                   : p.Nq <= 2 ? launch_nq<D, 2>(p, s)
                   : p.Nq <= 4 ? launch_nq<D, 4>(p, s)

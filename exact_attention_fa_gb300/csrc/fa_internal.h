@@ -69,11 +69,12 @@ struct BwdParams {
   unsigned long long timeout_ns;
 };
 
-// Decoding: Nq <= kDecodeMaxNq query rows per head against Nk keys. The 32-key blocks of all
-// heads are dealt out to n_ctas CTAs in contiguous ranges; piece (CTA c, head h) is slot c + h.
+// Decoding: Nq <= kDecodeMaxNq query rows per head against Nk keys. The key blocks of all heads
+// (kDecodeMinBlockKeys keys or more, by head dimension) are dealt out to n_ctas CTAs in
+// contiguous ranges; piece (CTA c, head h) is slot c + h.
 constexpr int kDecodeMaxNq = 8;
 constexpr int kDecodeMaxCtas = 1024;
-constexpr int kDecodeBlockKeys = 32;
+constexpr int kDecodeMinBlockKeys = 32;
 struct DecodeParams {
   const __nv_bfloat16* q;  // [BH][Nq][d]
   const __nv_bfloat16* k;  // [BH][Nk][d]
@@ -83,8 +84,8 @@ struct DecodeParams {
   float* ws_o;             // [n_ctas + BH][Nq][d] pieces' outputs O_c / l_c
   float* ws_lse;           // [n_ctas + BH][Nq] pieces' lse, log2 units
   int BH, Nq, Nk;
-  int blocks_per_head;     // ceil(Nk / kDecodeBlockKeys)
-  int n_ctas;              // 1 .. min(BH * blocks_per_head, kDecodeMaxCtas)
+  int blocks_per_head;     // set by the launcher (its block size)
+  int n_ctas;              // 1 .. kDecodeMaxCtas; the launcher caps it at the number of blocks
   float scale_log2;
   unsigned* err;
   unsigned long long timeout_ns;

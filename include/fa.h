@@ -130,9 +130,10 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
  *     o = softmax(scale * q K^T) V,   lse = log sum_j exp(scale * q.k_j).
  * q, o : bf16 [B,H,Nq,d];  k, v : bf16 [B,H,Nk,d];  lse : fp32 [B,H,Nq] (all DEVICE pointers,
  * 16-byte aligned, caller-owned; q, k, v read, o and lse written). d in {64, 128}; Nk >= 1.
- * The work is a matrix-vector product bound by HBM bandwidth. The 32-key blocks of all heads are
- * split into n_ctas equal contiguous ranges streamed by separate CTAs (a range may cut a head and
- * span several); the pieces of each head are merged with the softmax statistics merge.
+ * The work is a matrix-vector product bound by HBM bandwidth. The key blocks of all heads (32
+ * keys at d = 128, 64 at d = 64) are split into n_ctas equal contiguous ranges streamed by
+ * separate CTAs (a range may cut a head and span several); the pieces of each head are merged
+ * with the softmax statistics merge.
  * n_ctas = 0 takes as many CTAs as the device holds at once (fa_decode_ctas); 1 .. 1024 forces
  * the count (capped at the number of key blocks). `workspace`: fa_decode_workspace_bytes(...)
  * bytes of device scratch, contents undefined on entry and on exit. Errors: FA_ERR_INVALID_ARG
