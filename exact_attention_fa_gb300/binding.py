@@ -29,6 +29,7 @@ _F = ctypes.c_float
 SIGNATURES = [
     ("fa_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     ("fa_fwd_fp32", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    ("fa_fwd_fp32_fa1", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     ("fa_fwd_blocksparse", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
     ("fa_bwd_workspace_bytes", ctypes.c_size_t, [_I, _I, _I, _I]),
     ("fa_bwd", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
@@ -118,6 +119,15 @@ def fa_fwd_fp32(q, k, v, o, lse, scale: float, causal: bool = False):
     _rows(lse, q.shape)
     _check("fa_fwd_fp32", load().fa_fwd_fp32(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
                                              N, d, float(scale), int(bool(causal)), _stream(q)))
+
+
+def fa_fwd_fp32_fa1(q, k, v, o, lse, scale: float, causal: bool = False):
+    """fa_fwd_fp32 with the FlashAttention-1 per-block normalised update (same result)."""
+    B, H, N, d = _bhnd(q, k, v, o, dtype=torch.float32)
+    _rows(lse, q.shape)
+    _check("fa_fwd_fp32_fa1", load().fa_fwd_fp32_fa1(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                                     B, H, N, d, float(scale), int(bool(causal)),
+                                                     _stream(q)))
 
 
 def fa_fwd_blocksparse(q, k, v, o, lse, scale: float, block_mask, causal: bool = False):

@@ -235,7 +235,7 @@ int bwd_bf16(const void* q, const void* k, const void* v, const void* o, const v
 
 extern "C" {
 
-int fa_abi_version(void) { return (2 << 16) | 2; }
+int fa_abi_version(void) { return (2 << 16) | 3; }
 
 const char* fa_status_string(int status) {
   switch (status) {
@@ -264,8 +264,9 @@ int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, flo
   return fwd_bf16(q, k, v, o, lse, B, H, N, d, scale, causal, true, block_mask, stream);
 }
 
-int fa_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
-                int H, int N, int d, float scale, int causal, fa_stream_t stream) {
+namespace {
+int fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int H,
+             int N, int d, float scale, int causal, bool fa1, fa_stream_t stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   int st = check_common(B, H, N, scale);
   if (st != FA_OK) return st;
@@ -276,8 +277,19 @@ int fa_fwd_fp32(const float* q, const float* k, const float* v, float* o, float*
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != FA_OK) return st;
   fa::Fp32FwdParams p{q, k, v, o, lse, B * H, N, d, causal ? 1 : 0,
-                      scale * 1.4426950408889634f};
+                      scale * 1.4426950408889634f, fa1 ? 1 : 0};
   return to_status(fa::launch_fwd_fp32(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+int fa_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
+                int H, int N, int d, float scale, int causal, fa_stream_t stream) {
+  return fwd_fp32(q, k, v, o, lse, B, H, N, d, scale, causal, false, stream);
+}
+
+int fa_fwd_fp32_fa1(const float* q, const float* k, const float* v, float* o, float* lse, int B,
+                    int H, int N, int d, float scale, int causal, fa_stream_t stream) {
+  return fwd_fp32(q, k, v, o, lse, B, H, N, d, scale, causal, true, stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {

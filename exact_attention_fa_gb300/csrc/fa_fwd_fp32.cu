@@ -8,8 +8,18 @@
 //   m_new = max(m, block max),  alpha = exp(m - m_new),  l = l*alpha + sum p,  o = o*alpha + sum p v
 // with each lane owning d/32 output columns, and divides by l once at the end. Exponentials are
 // base 2 with log2(e) folded into the scale.
+//
+// The kFA1 instance keeps the output normalised after every key block instead, the per-block
+// update of FlashAttention-1 ("FlashAttention: IOを意識した高速かつメモリ効率の高い厳密なアテンション",
+// "手法" steps 1-4): P~ is taken against the block's own max m~, l~ = rowsum P~, and
+//   m_new = max(m, m~),  l_new = e^(m - m_new) l + e^(m~ - m_new) l~,
+//   o = (l e^(m - m_new) o + e^(m~ - m_new) P~ V_j) / l_new.
+// The result is the same up to rounding; the accumulator stays in registers (FA-2's loop order),
+// so the per-block read and write of O that FA-1 does through HBM has no counterpart here.
 #include <cuda_bf16.h>
 #include <math.h>
+
+#include <type_traits>
 
 #include "fa_internal.h"
 
@@ -19,7 +29,7 @@ namespace {
 constexpr int kRows = 8;   // query rows (warps) per CTA
 constexpr int kKeys = 32;  // keys per shared-memory block
 
-template <int D>
+template <int D, bool kFA1>
 __global__ void __launch_bounds__(kRows * 32) fwd_fp32_kernel(const Fp32FwdParams p) {
   constexpr int C = D / 32;
   __shared__ float ks[kKeys][D + 1];  // +1: lane j reads row j without bank conflicts
@@ -66,6 +76,33 @@ __global__ void __launch_bounds__(kRows * 32) fwd_fp32_kernel(const Fp32FwdParam
     float bmax = s;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(~0u, bmax, off));
+    if constexpr (kFA1) {
+      if (bmax == -INFINITY) continue;  // no allowed key in this block
+      const float pj = ok ? exp2f(s - bmax) : 0.f;  // P~ against the block max m~
+      float lt = pj;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(~0u, lt, off);
+      const float m_new = fmaxf(m, bmax);
+      const float c_old = exp2f(m - m_new);  // 0 before the first block (m = -inf)
+      const float c_new = exp2f(bmax - m_new);
+      const float l_new = c_old * l + c_new * lt;
+      float pv[C];
+#pragma unroll
+      for (int c = 0; c < C; ++c) pv[c] = 0.f;
+#pragma unroll 4
+      for (int jj = 0; jj < kKeys; ++jj) {
+        const float pjj = __shfl_sync(~0u, pj, jj);
+#pragma unroll
+        for (int c = 0; c < C; ++c) pv[c] = fmaf(pjj, vs[jj][lane + 32 * c], pv[c]);
+      }
+      const float inv = 1.f / l_new;
+      const float keep = l * c_old * inv, add = c_new * inv;
+#pragma unroll
+      for (int c = 0; c < C; ++c) acc[c] = fmaf(acc[c], keep, pv[c] * add);
+      l = l_new;
+      m = m_new;
+      continue;
+    }
     const float m_new = fmaxf(m, bmax);
     if (m_new == -INFINITY) continue;  // no allowed key for this row yet
     const float alpha = exp2f(m - m_new);  // 0 while nothing has been accumulated
@@ -86,7 +123,7 @@ __global__ void __launch_bounds__(kRows * 32) fwd_fp32_kernel(const Fp32FwdParam
   }
 
   if (row < p.N) {
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float inv = kFA1 ? 1.f : (l > 0.f ? 1.f / l : 0.f);  // FA-1: o is already normalised
     float* o = p.o + head + static_cast<size_t>(row) * D;
 #pragma unroll
     for (int c = 0; c < C; ++c) o[lane + 32 * c] = acc[c] * inv;
@@ -101,14 +138,18 @@ __global__ void __launch_bounds__(kRows * 32) fwd_fp32_kernel(const Fp32FwdParam
 cudaError_t launch_fwd_fp32(const Fp32FwdParams& p, cudaStream_t s) {
   const dim3 grid((p.N + kRows - 1) / kRows, p.BH);
   const dim3 block(kRows * 32);
-  switch (p.d) {
-    case 32: fwd_fp32_kernel<32><<<grid, block, 0, s>>>(p); break;
-    case 64: fwd_fp32_kernel<64><<<grid, block, 0, s>>>(p); break;
-    case 96: fwd_fp32_kernel<96><<<grid, block, 0, s>>>(p); break;
-    case 128: fwd_fp32_kernel<128><<<grid, block, 0, s>>>(p); break;
-    default: return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+  auto go = [&](auto fa1) {
+    constexpr bool F = decltype(fa1)::value;
+    switch (p.d) {
+      case 32: fwd_fp32_kernel<32, F><<<grid, block, 0, s>>>(p); break;
+      case 64: fwd_fp32_kernel<64, F><<<grid, block, 0, s>>>(p); break;
+      case 96: fwd_fp32_kernel<96, F><<<grid, block, 0, s>>>(p); break;
+      case 128: fwd_fp32_kernel<128, F><<<grid, block, 0, s>>>(p); break;
+      default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+  };
+  return p.fa1 ? go(std::true_type{}) : go(std::false_type{});
 }
 
 }  // namespace fa

@@ -37,6 +37,7 @@ struct Fp32FwdParams {
   int BH, N, d;
   int causal;
   float scale_log2;
+  int fa1;  // 1: FlashAttention-1 per-block normalised update
 };
 
 // Block-sparse backward: largest tile mask (query tiles) a CTA's shared-memory bitmask holds.

@@ -66,6 +66,14 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 int fa_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
                 int H, int N, int d, float scale, int causal, fa_stream_t stream);
 
+/* fa_fwd_fp32 in the FlashAttention-1 form ("FlashAttention: IOを意識した高速かつメモリ効率の高い
+ * 厳密なアテンション" (xyznot.com), "手法" steps 1-4): after every key block the output row is kept
+ * normalised, O <- diag(l_new)^-1 (diag(l) e^(m - m_new) O + e^(m~ - m_new) P~ V_j), with P~ and
+ * l~ taken against the block's own max m~. Same arguments, result (to rounding) and errors as
+ * fa_fwd_fp32. */
+int fa_fwd_fp32_fa1(const float* q, const float* k, const float* v, float* o, float* lse, int B,
+                    int H, int N, int d, float scale, int causal, fa_stream_t stream);
+
 /* Block-sparse forward ("FlashAttention: IOを意識した..." (xyznot.com), "拡張: Block-Sparse
  * FlashAttention"): block_mask is a DEVICE uint8 array [T][T] with T = ceil(N/128), row = query
  * tile, column = key tile, shared by all (b, h); a zero entry masks the whole 128 x 128 tile of
@@ -168,7 +176,7 @@ int fa_check_device_error(fa_stream_t stream);
 const char* fa_status_string(int status);
 
 /* ABI version: (major << 16) | minor. Major 2: fa_fwd_blocksparse takes a causal flag; minor 1:
- * fa_decode; minor 2: fa_bwd_blocksparse. */
+ * fa_decode; minor 2: fa_bwd_blocksparse; minor 3: fa_fwd_fp32_fa1. */
 int fa_abi_version(void);
 
 #ifdef __cplusplus

@@ -20,7 +20,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for want in ("fa_fwd", "fa_fwd_fp32", "fa_fwd_blocksparse", "fa_bwd", "fa_bwd_workspace_bytes",
+    for want in ("fa_fwd", "fa_fwd_fp32", "fa_fwd_fp32_fa1", "fa_fwd_blocksparse", "fa_bwd", "fa_bwd_workspace_bytes",
                  "fa_decode", "fa_decode_ctas", "fa_decode_workspace_bytes",
                  "fa_check_device_error", "fa_status_string", "fa_abi_version"):
         assert want in names
@@ -116,8 +116,11 @@ def test_bwd_blocksparse_validation(lib):
 
 def test_fp32_validation(lib):
     base = (fake(), fake(), fake(), fake(), fake(), 1, 1, 64)
-    assert lib.fa_fwd_fp32(*base, 48, 0.125, 0, None) == 2
-    assert lib.fa_fwd_fp32(*base, 256, 0.125, 0, None) == 2
+    for fn in (lib.fa_fwd_fp32, lib.fa_fwd_fp32_fa1):
+        assert fn(*base, 48, 0.125, 0, None) == 2
+        assert fn(*base, 256, 0.125, 0, None) == 2
+        assert fn(fake(), fake(), fake(), fake(), P(0), 1, 1, 64, 64, 0.125, 0, None) == 1
+        assert fn(fake(), fake(), fake(), fake(), fake(0x10004), 1, 1, 64, 64, 0.125, 0, None) == 3
 
 
 def test_bwd_validation_and_workspace(lib):

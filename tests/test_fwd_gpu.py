@@ -65,6 +65,49 @@ def test_fp32_shapes(cuda, N, d, causal):
     run_and_compare(w, cuda)
 
 
+def run_fa1(w: wl.Workload, device):
+    """fa_fwd_fp32_fa1 on every row against the oracle's plain definition; dense workloads also
+    against the oracle's FA-1 form with the kernel's 32-key blocks."""
+    inp = wl.make_inputs(w)
+    q, k, v = (H.to_device(inp, n, device) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=device)
+    fa.fa_fwd_fp32_fa1(q, k, v, o, lse, w.softmax_scale, w.causal)
+    fa.fa_check_device_error()
+    o = o.cpu().numpy()
+    lse = lse.cpu().numpy()
+    qf, kf, vf = inp.f64("q"), inp.f64("k"), inp.f64("v")
+    worst = 0.0
+    for b in range(w.B):
+        for h in range(w.H):
+            O_ref, lse_ref = orc.forward_head(qf[b, h], kf[b, h], vf[b, h], w.softmax_scale,
+                                              causal=w.causal)
+            mx, _ = H.compare_o(o[b, h], O_ref, bf16=False)
+            H.compare_lse(lse[b, h], lse_ref)
+            worst = max(worst, mx)
+            if not w.causal:
+                O1, lse1 = orc.forward_fa1_head(qf[b, h], kf[b, h], vf[b, h], w.softmax_scale, 32)
+                H.compare_o(o[b, h], O1, bf16=False)
+                H.compare_lse(lse[b, h], lse1)
+    return worst
+
+
+def test_single_head_fp32_fa1_form(cuda):
+    assert run_fa1(wl.WORKLOADS["single_head_fp32"], cuda) < 1e-6
+
+
+@pytest.mark.parametrize("N", [1, 31, 257])
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp32_fa1_form_shapes(cuda, N, d, causal):
+    run_fa1(wl.Workload("fp32_fa1", 2, 3, N, d, dtype="fp32", causal=causal, seed=12), cuda)
+
+
+def test_fp32_fa1_form_large_scores(cuda):
+    # scale 1: block maxima differ widely, so both rescale factors of the FA-1 update matter
+    run_fa1(wl.Workload("fp32_fa1_big", 1, 2, 300, 64, dtype="fp32", scale=1.0, seed=13), cuda)
+
+
 # ------------------------------------------------------------------------- bf16 tensor-core path
 
 @pytest.mark.parametrize("d", [64, 128])
