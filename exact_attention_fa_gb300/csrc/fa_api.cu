@@ -24,7 +24,8 @@ struct DeviceState {
   bool ready = false;
   int status = FA_OK;
   int num_sms = 0;
-  unsigned* err = nullptr;  // device address of g_error_word on this device
+  int decode_resident[2] = {1, 1};  // decoding split-kernel CTAs per SM, d = 64 / 128
+  unsigned* err = nullptr;          // device address of g_error_word on this device
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -32,7 +33,8 @@ std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 // Per-device set-up, once, with that device current: check it is an sm_103 part, look up the
-// device address of the error word and the SM count.
+// device address of the error word and the SM count, and opt the kernels in to their shared
+// memory (a function attribute of this device's context).
 int device_state(DeviceState** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -55,6 +57,16 @@ int device_state(DeviceState** out) {
                    cudaSuccess) {
       cudaGetLastError();
       st.status = FA_ERR_CUDA;
+    }
+    if (st.status == FA_OK) {
+      if (fa::configure_fwd_pair() != cudaSuccess || fa::configure_bwd() != cudaSuccess ||
+          fa::configure_decode() != cudaSuccess) {
+        cudaGetLastError();
+        st.status = FA_ERR_CUDA;
+      } else {
+        st.decode_resident[0] = fa::decode_ctas_per_sm(64);
+        st.decode_resident[1] = fa::decode_ctas_per_sm(128);
+      }
     }
     if (st.status == FA_OK && g_encode == nullptr) {
       void* fn = nullptr;
@@ -169,10 +181,10 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
 }
 
 // CTAs for decoding: as many as the SMs hold at once, never more than there are key blocks.
-int decode_auto_ctas(int BH, int Nk, int d, int num_sms) {
+int decode_auto_ctas(int BH, int Nk, int d, const DeviceState& ds) {
   constexpr int kB = fa::kDecodeMinBlockKeys;
   const long long blocks = static_cast<long long>(BH) * ((Nk + kB - 1) / kB);
-  long long n = static_cast<long long>(num_sms) * fa::decode_ctas_per_sm(d);
+  long long n = static_cast<long long>(ds.num_sms) * ds.decode_resident[d == 128 ? 1 : 0];
   if (n > fa::kDecodeMaxCtas) n = fa::kDecodeMaxCtas;
   return static_cast<int>(n < blocks ? n : blocks);
 }
@@ -318,7 +330,7 @@ int fa_decode_ctas(int B, int H, int Nq, int Nk, int d) {
   if (check_decode(B, H, Nq, Nk, d, 1.f) != FA_OK) return 0;
   DeviceState* ds = nullptr;
   if (device_state(&ds) != FA_OK) return 0;
-  return decode_auto_ctas(B * H, Nk, d, ds->num_sms);
+  return decode_auto_ctas(B * H, Nk, d, *ds);
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
@@ -342,7 +354,7 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != FA_OK) return st;
   const int BH = B * H;
-  if (n_ctas == 0) n_ctas = decode_auto_ctas(BH, Nk, d, ds->num_sms);
+  if (n_ctas == 0) n_ctas = decode_auto_ctas(BH, Nk, d, *ds);
   fa::DecodeParams p{};  // the launcher sets the block count and caps n_ctas at it
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);

@@ -800,17 +800,18 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ B
 }
 
 template <int D>
+cudaError_t configure_d() {
+  for (auto k : {bwd_tc_kernel<D, false>, bwd_tc_kernel<D, true>}) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <int D>
 cudaError_t launch_d(const BwdParams& p, int num_sms, cudaStream_t s) {
   using C = BCfg<D>;
-  static bool configured = false;
-  if (!configured) {
-    for (auto k : {bwd_tc_kernel<D, false>, bwd_tc_kernel<D, true>}) {
-      const cudaError_t e =
-          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-      if (e != cudaSuccess) return e;
-    }
-    configured = true;
-  }
   const int npad = p.n_tiles * BT;
   bwd_prep_kernel<D><<<num_sms * 8, 256, 0, s>>>(p, npad);
   cudaError_t e = cudaGetLastError();
@@ -828,6 +829,11 @@ cudaError_t launch_d(const BwdParams& p, int num_sms, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t configure_bwd() {
+  const cudaError_t e = configure_d<64>();
+  return e != cudaSuccess ? e : configure_d<128>();
+}
 
 cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t s) {
   if (p.d == 64) return launch_d<64>(p, num_sms, s);

@@ -361,17 +361,22 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(const __grid_constant__
 
 template <int D, int NQ>
 cudaError_t configure() {
-  static cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<D, NQ>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              DCfg<D>::kSmemBytes);
+  return cudaFuncSetAttribute(decode_stream_kernel<D, NQ>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, DCfg<D>::kSmemBytes);
+}
+
+template <int D>
+cudaError_t configure_d() {
+  cudaError_t e = configure<D, 1>();
+  if (e == cudaSuccess) e = configure<D, 2>();
+  if (e == cudaSuccess) e = configure<D, 4>();
+  if (e == cudaSuccess) e = configure<D, 8>();
   return e;
 }
 
 // Kernel instances for at most 1, 2, 4 and 8 query rows (registers scale with the bound).
 template <int D, int NQ>
 cudaError_t launch_nq(const DecodeParams& p, cudaStream_t s) {
-  cudaError_t e = configure<D, NQ>();
-  if (e != cudaSuccess) return e;
   decode_stream_kernel<D, NQ><<<p.n_ctas, kThreads, DCfg<D>::kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
@@ -398,8 +403,7 @@ cudaError_t launch(const DecodeParams& p_in, cudaStream_t s) {
 template <int D>
 int resident_ctas() {
   int n = 0;
-  if (configure<D, kDecodeMaxNq>() != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_stream_kernel<D, kDecodeMaxNq>,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_stream_kernel<D, kDecodeMaxNq>,
                                                     kThreads, DCfg<D>::kSmemBytes) != cudaSuccess) {
     cudaGetLastError();
     return 1;
@@ -408,6 +412,11 @@ int resident_ctas() {
 }
 
 }  // namespace
+
+cudaError_t configure_decode() {
+  const cudaError_t e = configure_d<64>();
+  return e != cudaSuccess ? e : configure_d<128>();
+}
 
 int decode_ctas_per_sm(int d) { return d == 128 ? resident_ctas<128>() : resident_ctas<64>(); }
 

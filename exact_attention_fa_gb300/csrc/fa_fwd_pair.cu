@@ -542,20 +542,24 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_pair_kernel(const __grid_cons
 }
 
 template <int D>
+cudaError_t configure() {
+  return cudaFuncSetAttribute(fwd_pair_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<D>::kSmemBytes);
+}
+
+template <int D>
 cudaError_t launch(const FwdParams& p, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        fwd_pair_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
   const unsigned grid = static_cast<unsigned>((p.n_tiles + 1) / 2) * static_cast<unsigned>(p.BH);
   fwd_pair_kernel<D><<<grid, kThreads, Cfg<D>::kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+cudaError_t configure_fwd_pair() {
+  const cudaError_t e = configure<64>();
+  return e != cudaSuccess ? e : configure<128>();
+}
 
 cudaError_t launch_fwd_pair(const FwdParams& p, int d, cudaStream_t s) {
   if (d == 64) return launch<64>(p, s);

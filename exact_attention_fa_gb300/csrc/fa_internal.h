@@ -98,5 +98,10 @@ cudaError_t launch_fwd_fp32(const Fp32FwdParams& p, cudaStream_t s);
 cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t s);
 int decode_ctas_per_sm(int d);  // resident split-kernel CTAs per SM (shared-memory bound)
+// Opt the kernels that use more than 48 KB of dynamic shared memory in to their size. Function
+// attributes belong to a device's context, so these run once per device, with it current.
+cudaError_t configure_fwd_pair();
+cudaError_t configure_bwd();
+cudaError_t configure_decode();
 
 }  // namespace fa
