@@ -32,6 +32,14 @@ def test_bench_line(cuda, workload):
     assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
     assert d["roofline"]["peak"] > 0 and 0 < d["roofline"]["frac"]
     assert d["config"]["workload"] == workload
+    # the fp32 path runs on the FMA pipes; bf16 on the tensor cores, also against the sustained
+    # and datasheet peaks; decoding against HBM
+    want = {"single_head_fp32": "alu", "mha_N2048_d64": "tensor", "decode_N32768_d128_h8": "hbm"}
+    assert d["roofline"]["bound"] == want[workload]
+    if want[workload] != "alu":
+        assert 0 < d["roofline"]["frac_of_nominal"] < d["roofline"]["frac"]
+    if want[workload] == "tensor":
+        assert d["roofline"]["frac_of_sustained"] > d["roofline"]["frac"]
 
 
 @pytest.mark.gpu
