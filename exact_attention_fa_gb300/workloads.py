@@ -98,8 +98,11 @@ WORKLOADS = {
                                       backward=True, seed=5),
     # decoding ("3 · FlashAttention", 3.6): one new query row per head against a 32k-key cache
     "decode_N32768_d128": Workload("decode_N32768_d128", 8, 32, 32768, 128, nq=1, seed=6),
-    # the same per-head problem on 8 heads (268 MB of K, V: larger than L2, small enough for ncu)
+    # the same per-head problem on 8 heads (134 MB of K, V: larger than L2, small enough for ncu)
     "decode_N32768_d128_h8": Workload("decode_N32768_d128_h8", 1, 8, 32768, 128, nq=1, seed=7),
+    # the same at d = 64 (64-key blocks), and its profile case on 16 heads (134 MB of K, V)
+    "decode_N32768_d64": Workload("decode_N32768_d64", 8, 32, 32768, 64, nq=1, seed=8),
+    "decode_N32768_d64_h16": Workload("decode_N32768_d64_h16", 1, 16, 32768, 64, nq=1, seed=9),
 }
 
 
