@@ -88,11 +88,13 @@ def _ptr(t: torch.Tensor | None):
 def _bhnd(q: torch.Tensor, *others: torch.Tensor, dtype=torch.bfloat16):
     if q.dim() != 4:
         raise ValueError("expected [B, H, N, d] tensors")
-    for t in (q,) + others:
+    tensors = (q,) + others
+    for t in tensors:
         if t.shape != q.shape:
             raise ValueError(f"shape mismatch: {tuple(t.shape)} vs {tuple(q.shape)}")
         if t.dtype != dtype:
             raise TypeError(f"expected {dtype}, got {t.dtype}")
+    for t in tensors:
         if not t.is_cuda or t.device != q.device:
             raise ValueError("all tensors must be on the same CUDA device")
         if not t.is_contiguous():
