@@ -77,6 +77,14 @@ def _check(fn: str, status: int):
         raise FAError(fn, status, load().fa_status_string(status).decode())
 
 
+def _call(fn: str, device: torch.device, *args):
+    """Calls entry point `fn` with `device` current: the library works on the current CUDA device
+    (its per-device state, the stream's device), which must be the tensors' own."""
+    with torch.cuda.device(device):
+        status = getattr(load(), fn)(*args)
+    _check(fn, status)
+
+
 def _stream(t: torch.Tensor):
     return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
 
@@ -111,25 +119,24 @@ def fa_fwd(q, k, v, o, lse, scale: float, causal: bool = False):
     """bf16 forward into preallocated o [B,H,N,d] bf16 and lse [B,H,N] fp32."""
     B, H, N, d = _bhnd(q, k, v, o)
     _rows(lse, q.shape)
-    _check("fa_fwd", load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
-                                   float(scale), int(bool(causal)), _stream(q)))
+    _call("fa_fwd", q.device, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+          float(scale), int(bool(causal)), _stream(q))
 
 
 def fa_fwd_fp32(q, k, v, o, lse, scale: float, causal: bool = False):
     """fp32 forward (FMA pipes) into preallocated o [B,H,N,d] fp32 and lse [B,H,N] fp32."""
     B, H, N, d = _bhnd(q, k, v, o, dtype=torch.float32)
     _rows(lse, q.shape)
-    _check("fa_fwd_fp32", load().fa_fwd_fp32(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
-                                             N, d, float(scale), int(bool(causal)), _stream(q)))
+    _call("fa_fwd_fp32", q.device, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+          float(scale), int(bool(causal)), _stream(q))
 
 
 def fa_fwd_fp32_fa1(q, k, v, o, lse, scale: float, causal: bool = False):
     """fa_fwd_fp32 with the FlashAttention-1 per-block normalised update (same result)."""
     B, H, N, d = _bhnd(q, k, v, o, dtype=torch.float32)
     _rows(lse, q.shape)
-    _check("fa_fwd_fp32_fa1", load().fa_fwd_fp32_fa1(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-                                                     B, H, N, d, float(scale), int(bool(causal)),
-                                                     _stream(q)))
+    _call("fa_fwd_fp32_fa1", q.device, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+          float(scale), int(bool(causal)), _stream(q))
 
 
 def fa_fwd_blocksparse(q, k, v, o, lse, scale: float, block_mask, causal: bool = False):
@@ -141,10 +148,8 @@ def fa_fwd_blocksparse(q, k, v, o, lse, scale: float, block_mask, causal: bool =
     if (block_mask.dtype != torch.uint8 or tuple(block_mask.shape) != (nt, nt)
             or not block_mask.is_cuda or not block_mask.is_contiguous()):
         raise ValueError(f"block_mask must be a contiguous uint8 CUDA tensor [{nt}, {nt}]")
-    _check("fa_fwd_blocksparse",
-           load().fa_fwd_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
-                                     float(scale), int(bool(causal)), _ptr(block_mask),
-                                     _stream(q)))
+    _call("fa_fwd_blocksparse", q.device, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N,
+          d, float(scale), int(bool(causal)), _ptr(block_mask), _stream(q))
 
 
 def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
@@ -161,9 +166,9 @@ def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool, workspac
     need = fa_bwd_workspace_bytes(B, H, N, d)
     if workspace.numel() * workspace.element_size() < need or not workspace.is_cuda:
         raise ValueError(f"workspace must hold at least {need} bytes on the device")
-    _check("fa_bwd", load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
-                                   _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
-                                   int(bool(causal)), _ptr(workspace), _stream(q)))
+    _call("fa_bwd", q.device, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+          _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)), _ptr(workspace),
+          _stream(q))
 
 
 def fa_bwd_blocksparse(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool, block_mask,
@@ -181,11 +186,9 @@ def fa_bwd_blocksparse(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bo
     need = fa_bwd_workspace_bytes(B, H, N, d)
     if workspace.numel() * workspace.element_size() < need or not workspace.is_cuda:
         raise ValueError(f"workspace must hold at least {need} bytes on the device")
-    _check("fa_bwd_blocksparse",
-           load().fa_bwd_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
-                                     _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
-                                     int(bool(causal)), _ptr(block_mask), _ptr(workspace),
-                                     _stream(q)))
+    _call("fa_bwd_blocksparse", q.device, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+          _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+          _ptr(block_mask), _ptr(workspace), _stream(q))
 
 
 def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool):
@@ -196,10 +199,8 @@ def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool):
     if tuple(dq.shape) != tuple(q.shape):
         raise ValueError("dq must have the shape of q")
     _rows(lse, q.shape)
-    _check("fa_bwd_noalloc",
-           load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
-                                 _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
-                                 _stream(q)))
+    _call("fa_bwd_noalloc", q.device, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+          _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)), _stream(q))
 
 
 def fa_decode_ctas(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
@@ -226,23 +227,22 @@ def fa_decode(q, k, v, o, lse, scale: float, n_ctas: int = 0, workspace=None):
     if (workspace is None or not workspace.is_cuda or not workspace.is_contiguous()
             or workspace.numel() * workspace.element_size() < need):
         raise ValueError(f"workspace must be a contiguous CUDA tensor of at least {need} bytes")
-    _check("fa_decode", load().fa_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq,
-                                         Nk, d, float(scale), int(n_ctas), _ptr(workspace),
-                                         _stream(q)))
+    _call("fa_decode", q.device, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
+          float(scale), int(n_ctas), _ptr(workspace), _stream(q))
 
 
 def fa_selftest_wait_timeout(timeout_us: int = 20000, device=None):
     """Runs the library's bounded-wait self-test kernel (a wait that can only time out)."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     s = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
-    _check("fa_selftest_wait_timeout", load().fa_selftest_wait_timeout(int(timeout_us), s))
+    _call("fa_selftest_wait_timeout", dev, int(timeout_us), s)
 
 
 def fa_check_device_error(device=None):
     """Synchronises the current stream and raises if a kernel recorded a device-side error."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     s = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
-    _check("fa_check_device_error", load().fa_check_device_error(s))
+    _call("fa_check_device_error", dev, s)
 
 
 # ------------------------------------------------------------------------------- conveniences
@@ -284,7 +284,8 @@ def attention_backward(q, k, v, o, lse, do, scale: float | None = None, causal: 
     dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
-    ws = torch.empty(fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=q.device)
+    ws = torch.empty(max(16, fa_bwd_workspace_bytes(B, H, N, d)), dtype=torch.uint8,
+                     device=q.device)
     if block_mask is not None:
         fa_bwd_blocksparse(q, k, v, o, do, lse, dq, dk, dv, scale, causal, block_mask, ws)
     else:

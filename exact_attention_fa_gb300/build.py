@@ -37,9 +37,15 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
+def _portable_flags() -> list:
+    """The build flags with the include directory written relative to the repository, so that
+    the digest of the same sources is the same in every checkout."""
+    return ["include" if f == INCLUDE else f for f in NVCC_FLAGS]
+
+
 def _digest() -> str:
     h = hashlib.sha256()
-    h.update(" ".join(NVCC_FLAGS).encode())
+    h.update(" ".join(_portable_flags()).encode())
     for d in (CSRC, INCLUDE):
         for f in sorted(os.listdir(d)):
             if f.endswith((".cu", ".cuh", ".h")):

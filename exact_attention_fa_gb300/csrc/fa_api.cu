@@ -80,6 +80,14 @@ int device_state(DeviceState** out) {
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
       }
     }
+    if (st.status != FA_OK) {
+      // keep only a successful set-up; a failed one is tried again on the next call
+      st.ready = false;
+      *out = &st;
+      const int failed = st.status;
+      st.status = FA_OK;
+      return failed;
+    }
   }
   *out = &st;
   return st.status;
@@ -201,17 +209,9 @@ int bwd_bf16(const void* q, const void* k, const void* v, const void* o, const v
              const float* lse, float* dq, void* dk, void* dv, int B, int H, int N, int d,
              float scale, int causal, bool sparse, const uint8_t* block_mask, void* workspace,
              fa_stream_t stream) {
-  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace)
-    return FA_ERR_INVALID_ARG;
-  if (sparse && !block_mask) return FA_ERR_INVALID_ARG;
-  int st = check_common(B, H, N, scale);
+  int st = fa::check_bwd_args(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, sparse,
+                              block_mask, workspace, true);
   if (st != FA_OK) return st;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (sparse && (N + 127) / 128 > fa::kBwdMaxMaskTiles) return FA_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
-      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
-      !aligned16(workspace))
-    return FA_ERR_MISALIGNED;
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != FA_OK) return st;
   fa::BwdParams p{};
@@ -229,7 +229,7 @@ int bwd_bf16(const void* q, const void* k, const void* v, const void* o, const v
   const size_t rows = static_cast<size_t>(BH) * ((static_cast<size_t>(N) + 127) / 128) * 128;
   p.lse2 = static_cast<float*>(workspace);
   p.Dsum = static_cast<float*>(workspace) + rows;
-  p.aug = static_cast<uint8_t*>(workspace) + rows * 2 * sizeof(float);
+  p.aug = d == 64 ? static_cast<uint8_t*>(workspace) + rows * 2 * sizeof(float) : nullptr;
   p.BH = BH;
   p.N = N;
   p.d = d;
@@ -245,9 +245,28 @@ int bwd_bf16(const void* q, const void* k, const void* v, const void* o, const v
 
 }  // namespace
 
+// Argument checks of the backward entry points, in the order every one of them applies them.
+int fa::check_bwd_args(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                       const float* lse, const float* dq, const void* dk, const void* dv, int B,
+                       int H, int N, int d, float scale, bool sparse, const uint8_t* block_mask,
+                       const void* workspace, bool needs_workspace) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || (needs_workspace && !workspace))
+    return FA_ERR_INVALID_ARG;
+  if (sparse && !block_mask) return FA_ERR_INVALID_ARG;
+  const int st = check_common(B, H, N, scale);
+  if (st != FA_OK) return st;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (sparse && (N + 127) / 128 > fa::kBwdMaxMaskTiles) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (needs_workspace && !aligned16(workspace)))
+    return FA_ERR_MISALIGNED;
+  return FA_OK;
+}
+
 extern "C" {
 
-int fa_abi_version(void) { return (2 << 16) | 3; }
+int fa_abi_version(void) { return (2 << 16) | 4; }
 
 const char* fa_status_string(int status) {
   switch (status) {
@@ -260,7 +279,8 @@ const char* fa_status_string(int status) {
     case FA_ERR_NO_DEVICE: return "no current sm_103 CUDA device";
     case FA_ERR_TOO_LARGE: return "problem too large for the kernels' indexing";
     case FA_ERR_SCRATCH_LIMIT:
-      return "problem needs more scratch than fa_bwd_noalloc's static buffer (4 MiB) holds";
+      return "problem needs more scratch than fa_bwd_noalloc's static buffer "
+             "(FA_NOALLOC_SCRATCH_BYTES) holds";
     default: return "unknown status";
   }
 }
@@ -305,10 +325,10 @@ int fa_fwd_fp32_fa1(const float* q, const float* k, const float* v, float* o, fl
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
-  (void)d;
-  if (B < 1 || H < 1 || N < 1) return 0;
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
   const size_t rows = static_cast<size_t>(B) * H * ((static_cast<size_t>(N) + 127) / 128) * 128;
-  return rows * (2 * sizeof(float) + 64);  // lse2, D; their two 32-byte operand rows
+  // lse2 and D; at d = 64 also their two 32-byte operand rows
+  return rows * (2 * sizeof(float) + (d == 64 ? 64 : 0));
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,

@@ -92,6 +92,16 @@ struct DecodeParams {
   unsigned long long timeout_ns;
 };
 
+// Argument checks shared by the backward entry points (fa_bwd, fa_bwd_blocksparse,
+// fa_bwd_noalloc), so that all of them report the same status for the same bad argument: null
+// pointers and sizes (FA_ERR_INVALID_ARG), FA_ERR_TOO_LARGE, d or the mask size
+// (FA_ERR_UNSUPPORTED), alignment (FA_ERR_MISALIGNED), in that order. The workspace pointer is
+// checked only when needs_workspace is set.
+int check_bwd_args(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                   const float* lse, const float* dq, const void* dk, const void* dv, int B, int H,
+                   int N, int d, float scale, bool sparse, const uint8_t* block_mask,
+                   const void* workspace, bool needs_workspace);
+
 // Launchers; return a cudaError_t (cudaSuccess on success).
 cudaError_t launch_fwd_pair(const FwdParams& p, int d, cudaStream_t s);               // 2 tiles/CTA
 cudaError_t launch_fwd_fp32(const Fp32FwdParams& p, cudaStream_t s);

@@ -9,12 +9,15 @@
 // The array is a file-scope __device__ object: every device that loads the library holds
 // FA_NOALLOC_SCRATCH_BYTES of it until the process exits. In host code its name is only a host
 // stand-in, so its device address is looked up once per device with cudaGetSymbolAddress (with
-// that device current, on the first call) and that address is what the kernels receive.
+// that device current, on the first call) and that address is what the kernels receive. Only a
+// successful lookup is kept; a failed one is tried again on the next call. The kept address
+// belongs to the device's current context: calls after cudaDeviceReset are not supported.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "fa.h"
+#include "fa_internal.h"
 
 namespace {
 
@@ -25,9 +28,7 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
 
 struct ScratchSlot {
-  bool looked_up = false;
-  int status = FA_OK;
-  void* ptr = nullptr;
+  void* ptr = nullptr;  // device address of g_noalloc_scratch once looked up
 };
 ScratchSlot g_slots[kMaxDevices];
 std::mutex g_slots_mu;
@@ -40,22 +41,23 @@ int scratch_on_current_device(void** out) {
   }
   std::lock_guard<std::mutex> lock(g_slots_mu);
   ScratchSlot& s = g_slots[dev];
-  if (!s.looked_up) {
-    s.looked_up = true;
+  if (s.ptr == nullptr) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
         major != 10 || minor != 3) {
       cudaGetLastError();
-      s.status = FA_ERR_NO_DEVICE;
-    } else if (cudaGetSymbolAddress(&s.ptr, g_noalloc_scratch) != cudaSuccess || s.ptr == nullptr) {
-      cudaGetLastError();
-      s.status = FA_ERR_CUDA;
-      s.ptr = nullptr;
+      return FA_ERR_NO_DEVICE;
     }
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return FA_ERR_CUDA;
+    }
+    s.ptr = ptr;
   }
   *out = s.ptr;
-  return s.status;
+  return FA_OK;
 }
 
 }  // namespace
@@ -64,10 +66,13 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
                               const void* dO, const float* lse, float* dq, void* dk, void* dv,
                               int B, int H, int N, int d, float scale, int causal,
                               fa_stream_t stream) {
-  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
-  const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
-  if (need == 0) return FA_ERR_INVALID_ARG;
-  if (need > static_cast<size_t>(FA_NOALLOC_SCRATCH_BYTES)) return FA_ERR_SCRATCH_LIMIT;
+  // fa_bwd's argument checks first, in its order, so both report the same status for the same
+  // bad argument; only then the size limit of the static scratch.
+  const int bad = fa::check_bwd_args(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, false,
+                                     nullptr, nullptr, false);
+  if (bad != FA_OK) return bad;
+  if (fa_bwd_workspace_bytes(B, H, N, d) > static_cast<size_t>(FA_NOALLOC_SCRATCH_BYTES))
+    return FA_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   const int st = scratch_on_current_device(&scratch);
   if (st != FA_OK) return st;

@@ -46,6 +46,42 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+# OCP 8-bit float E4M3 ("e4m3fn"): sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0
+# holds the subnormals m/8 * 2^-6; the all-ones pattern S.1111.111 is NaN and there is no
+# infinity, so the largest finite value is 1.75 * 2^8 = 448.
+def _e4m3_table() -> np.ndarray:
+    codes = np.arange(256)
+    sign = np.where(codes & 0x80, -1.0, 1.0)
+    e = (codes >> 3) & 0xF
+    m = codes & 0x7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7.0))
+    vals = sign * mag
+    vals[(codes & 0x7F) == 0x7F] = np.nan
+    return vals
+
+
+E4M3_VALUES = _e4m3_table()
+E4M3_MAX = 448.0
+
+
+def e4m3_bits_from_f32(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest E4M3 value, ties to even (the even code has a 0 last mantissa bit),
+    saturating at +-448; returns the uint8 codes. Inputs must be finite."""
+    x = np.asarray(x, dtype=np.float64)
+    pos = E4M3_VALUES[:0x7F]  # codes 0x00 .. 0x7E: 0, the subnormals, the normals, ascending
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    hi = np.clip(np.searchsorted(pos, a, side="left"), 1, 0x7E)
+    lo = hi - 1
+    d_lo, d_hi = a - pos[lo], pos[hi] - a
+    code = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = np.where(a >= pos[hi], hi, code)  # exact hits of the upper candidate
+    return (code | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)  # -0 keeps its sign
+
+
+def e4m3_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    return E4M3_VALUES[np.asarray(bits, dtype=np.uint8)]
+
+
 def block_mask(n_tiles: int, seed: int, p: float = 0.25) -> np.ndarray:
     """Bernoulli(p) tile mask [n_tiles, n_tiles] (row = query tile, column = key tile), diagonal on."""
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, STREAM_MASK])))
@@ -63,7 +99,7 @@ class Workload:
     H: int
     N: int
     d: int
-    dtype: str = "bf16"  # "bf16" or "fp32" (Q, K, V, dO and O)
+    dtype: str = "bf16"  # "bf16", "fp32" or "e4m3" (Q, K, V, dO; O is bf16 for e4m3 inputs)
     causal: bool = False
     block_sparse: bool = False
     backward: bool = False
@@ -103,7 +139,17 @@ WORKLOADS = {
     # the same at d = 64 (64-key blocks), and its profile case on 16 heads (134 MB of K, V)
     "decode_N32768_d64": Workload("decode_N32768_d64", 8, 32, 32768, 64, nq=1, seed=8),
     "decode_N32768_d64_h16": Workload("decode_N32768_d64_h16", 1, 16, 32768, 64, nq=1, seed=9),
+    # the long-sequence causal forward's per-head problem on 8 heads, at N = 8192 and N = 4096
+    # (a device footprint small enough for counter captures; DRAM bytes should grow with N)
+    "causal_N8192_d128_h8": Workload("causal_N8192_d128_h8", 1, 8, 8192, 128, causal=True,
+                                     seed=10),
+    "causal_N4096_d128_h8": Workload("causal_N4096_d128_h8", 1, 8, 4096, 128, causal=True,
+                                     seed=11),
 }
+
+# The five specified workloads in their order (the seed of each is its position).
+SPECIFIED = ["single_head_fp32", "mha_N2048_d64", "causal_N8192_d128", "blocksparse_N16384_d64",
+             "bwd_causal_N4096_d128"]
 
 
 @dataclasses.dataclass
@@ -117,11 +163,19 @@ class Inputs:
     w: Workload
     arrays: dict
 
-    def f64(self, name: str) -> np.ndarray:
-        a = self.arrays[name]
+    def _decode(self, name: str, a: np.ndarray) -> np.ndarray:
         if a.dtype == np.uint16:
             return bf16_bits_to_f64(a)
+        if a.dtype == np.uint8 and name != "mask":
+            return e4m3_bits_to_f64(a)
         return a.astype(np.float64)
+
+    def f64(self, name: str) -> np.ndarray:
+        return self._decode(name, self.arrays[name])
+
+    def f64_head(self, name: str, b: int, h: int) -> np.ndarray:
+        """f64(name)[b, h] without converting the whole tensor."""
+        return self._decode(name, self.arrays[name][b, h])
 
     def raw(self, name: str) -> np.ndarray:
         return self.arrays[name]
@@ -136,7 +190,12 @@ def make_inputs(w: Workload, with_do: bool | None = None) -> Inputs:
     arrays = {}
     for nm, st in names:
         x = normal_f32(qshape if nm in ("q", "do") else shape, w.seed, st)
-        arrays[nm] = bf16_bits_from_f32(x) if w.dtype == "bf16" else x
+        if w.dtype == "bf16":
+            arrays[nm] = bf16_bits_from_f32(x)
+        elif w.dtype == "e4m3":
+            arrays[nm] = e4m3_bits_from_f32(x)
+        else:
+            arrays[nm] = x
         del x
     if w.block_sparse:
         arrays["mask"] = block_mask(-(-w.N // TILE), w.seed)

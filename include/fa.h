@@ -24,6 +24,9 @@
  *     was launched (except FA_ERR_CUDA from a failed launch).
  *   - Kernels never spin forever: every wait on an on-chip barrier gives up after a bounded time
  *     and records FA_ERR_DEVICE_TIMEOUT in a device error word, read by fa_check_device_error.
+ *   - The library sets itself up once per device, on the first call with that device current
+ *     (kernel attributes, device addresses of its own __device__ objects); a failed set-up is
+ *     retried on the next call. Calls after cudaDeviceReset on that device are not supported.
  *   - Masked rows: a query row with no allowed key gets O = 0 and lse = -inf.
  */
 #ifndef FA_GB300_H_
@@ -85,9 +88,9 @@ int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, flo
                        int H, int N, int d, float scale, int causal, const uint8_t* block_mask,
                        fa_stream_t stream);
 
-/* Bytes of device workspace fa_bwd needs: 72 bytes per row of B*H*ceil(N/128)*128 rows (rows
- * padded to whole 128-row tiles): two fp32 row statistics and two 32-byte bf16 operand rows made
- * from them. */
+/* Bytes of device workspace fa_bwd needs, per row of B*H*ceil(N/128)*128 rows (rows padded to
+ * whole 128-row tiles): two fp32 row statistics (8 bytes) and, at d = 64, two 32-byte bf16
+ * operand rows made from them (72 bytes in all). 0 for B, H, N < 1 or d not in {64, 128}. */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
 /* Backward by recomputation ("3 · FlashAttention", 3.4; "FlashAttention：在线 softmax 与
@@ -121,9 +124,11 @@ int fa_bwd_blocksparse(const void* q, const void* k, const void* v, const void* 
  * while it serves). The pages have no counterpart of this entry point.
  * Same arguments, results and errors as fa_bwd, minus `workspace`: the scratch comes from a
  * FA_NOALLOC_SCRATCH_BYTES array of device memory that every device holds from the moment the
- * library's module is loaded on it until the process exits. Problems whose
- * fa_bwd_workspace_bytes(B, H, N, d) exceeds that size are rejected with FA_ERR_SCRATCH_LIMIT
- * before anything is enqueued (4 MiB covers B*H*ceil(N/128)*128 <= 58240 rows).
+ * library's module is loaded on it until the process exits. fa_bwd's argument checks run first,
+ * in its order (so a bad argument gets the same status from both); then problems whose
+ * fa_bwd_workspace_bytes(B, H, N, d) exceeds the array are rejected with FA_ERR_SCRATCH_LIMIT,
+ * before anything is enqueued. 4 MiB covers B*H*ceil(N/128)*128 <= 58240 rows at d = 64 and
+ * <= 524288 rows at d = 128.
  * Allocates nothing: no cudaMalloc/cudaFree or allocating library call. The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress, with that device current);
  * make that first call before any stream capture. All calls on a device share the one array and
@@ -176,7 +181,8 @@ int fa_check_device_error(fa_stream_t stream);
 const char* fa_status_string(int status);
 
 /* ABI version: (major << 16) | minor. Major 2: fa_fwd_blocksparse takes a causal flag; minor 1:
- * fa_decode; minor 2: fa_bwd_blocksparse; minor 3: fa_fwd_fp32_fa1. */
+ * fa_decode; minor 2: fa_bwd_blocksparse; minor 3: fa_fwd_fp32_fa1; minor 4:
+ * fa_bwd_workspace_bytes depends on d (8 bytes per row at d = 128). */
 int fa_abi_version(void);
 
 #ifdef __cplusplus

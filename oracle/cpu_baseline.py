@@ -1,8 +1,8 @@
 """Runs the fp64 oracle on one (b, h) head for the CPU-baseline timing of bench.py.
 
 Test/benchmark infrastructure only (imported by bench.py's cpu_baseline leg and its reference
-arm). It holds no arithmetic of its own: it decodes the seeded bf16 inputs and calls the oracle's
-forward and backward as they stand.
+arm). It holds no arithmetic of its own: it decodes the seeded inputs (bf16 bit patterns or fp32)
+and calls the oracle's forward and backward as they stand.
 """
 from __future__ import annotations
 
@@ -11,8 +11,10 @@ import numpy as np
 from . import attention as orc
 
 
-def _f64(bits: np.ndarray) -> np.ndarray:
-    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+def _f64(a: np.ndarray) -> np.ndarray:
+    if a.dtype == np.uint16:  # bf16 bit patterns
+        return (a.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
 
 
 def warm(_: int) -> int:
@@ -22,12 +24,15 @@ def warm(_: int) -> int:
 
 
 def run_head(task) -> float:
-    """task = (q, k, v, do bf16 bit arrays [N, d] (do may be None), scale, causal, block_mask).
+    """task = (q, k, v, do [N, d] arrays (bf16 bits or fp32; do may be None), scale, causal,
+    block_mask, rows). rows: the query rows to compute (None: all of them); the forward of a row
+    subset is the same computation restricted to those rows. The backward always takes the whole
+    head.
 
     Returns the checksum of the outputs (so the work cannot be skipped)."""
-    q, k, v, do, scale, causal, block_mask = task
+    q, k, v, do, scale, causal, block_mask, rows = task
     qf, kf, vf = _f64(q), _f64(k), _f64(v)
-    O, lse = orc.forward_head(qf, kf, vf, scale, causal=causal, block_mask=block_mask)
+    O, lse = orc.forward_head(qf, kf, vf, scale, causal=causal, block_mask=block_mask, rows=rows)
     total = float(O.sum())
     if do is not None:
         dq, dk, dv = orc.backward_head(qf, kf, vf, _f64(do), scale, causal=causal,

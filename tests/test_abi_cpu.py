@@ -124,10 +124,11 @@ def test_fp32_validation(lib):
 
 
 def test_bwd_validation_and_workspace(lib):
-    # 72 bytes per padded row: lse2 and D (fp32) plus their two 32-byte bf16 operand rows
+    # per padded row: lse2 and D (fp32), and at d = 64 their two 32-byte bf16 operand rows
     assert lib.fa_bwd_workspace_bytes(2, 3, 100, 64) == 2 * 3 * 128 * 72
-    assert lib.fa_bwd_workspace_bytes(1, 1, 256, 128) == 256 * 72
+    assert lib.fa_bwd_workspace_bytes(1, 1, 256, 128) == 256 * 8
     assert lib.fa_bwd_workspace_bytes(0, 3, 100, 64) == 0
+    assert lib.fa_bwd_workspace_bytes(1, 1, 256, 96) == 0
     ptrs = [fake()] * 9
     assert lib.fa_bwd(*ptrs, 1, 1, 128, 64, 0.125, 1, P(0), None) == 1
     assert lib.fa_bwd(*ptrs, 1, 1, 128, 80, 0.125, 1, fake(), None) == 2
@@ -143,3 +144,41 @@ def test_no_device_here_is_reported_not_crashed(lib):
 def test_selftest_validation(lib):
     assert lib.fa_selftest_wait_timeout(0, None) == 1
     assert lib.fa_selftest_wait_timeout(20000001, None) == 1
+
+
+# (pointers, B, H, N, d, scale) cases that fa_bwd rejects before anything touches a GPU
+BAD_BWD_ARGS = [
+    ([P(0)] + [fake()] * 8, 1, 1, 128, 64, 0.125),             # null q
+    ([fake()] * 8 + [P(0)], 1, 1, 128, 64, 0.125),             # null dv
+    ([fake()] * 9, 0, 1, 128, 64, 0.125),                      # B = 0
+    ([fake()] * 9, 1, 1, 0, 64, 0.125),                        # N = 0
+    ([fake()] * 9, 1, 1, 128, 64, float("nan")),               # scale
+    ([fake()] * 9, 1, 1, 128, 96, 0.125),                      # head dim
+    ([fake()] * 9, 8, 32, 8192, 96, 0.125),                    # head dim of a large problem
+    ([fake(0x10008)] + [fake()] * 8, 1, 1, 128, 64, 0.125),    # misaligned q
+    ([fake(0x10008)] + [fake()] * 8, 8, 32, 8192, 64, 0.125),  # misaligned, large problem
+    ([P(0)] + [fake()] * 8, 8, 32, 8192, 128, 0.125),          # null q, large problem
+    ([fake()] * 9, 1 << 16, 1 << 16, 1024, 64, 0.125),         # too large to index
+]
+
+
+@pytest.mark.parametrize("case", range(len(BAD_BWD_ARGS)))
+def test_bwd_noalloc_reports_fa_bwds_status(lib, case):
+    """fa_bwd_noalloc runs fa_bwd's argument checks first and in the same order, so a bad
+    argument gets the same status from both, whatever the problem's size."""
+    ptrs, B, Hh, N, d, scale = BAD_BWD_ARGS[case]
+    want = lib.fa_bwd(*ptrs, B, Hh, N, d, scale, 1, fake(), None)
+    assert want in (1, 2, 3, 7)
+    assert lib.fa_bwd_noalloc(*ptrs, B, Hh, N, d, scale, 1, None) == want
+
+
+def test_bwd_noalloc_scratch_limit_after_argument_checks(lib):
+    ptrs = [fake()] * 9
+    # 4 MiB: 58240 padded rows at d = 64 (72 bytes each), 524288 at d = 128 (8 bytes each)
+    assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 58241, 64, 0.125, 0, None) == 8
+    assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 524289, 128, 0.125, 0, None) == 8
+    # within the limit the call goes on to the device, which this machine does not have
+    import torch
+    if not torch.cuda.is_available():
+        assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 58240, 64, 0.125, 0, None) == 6
+        assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 524288, 128, 0.125, 0, None) == 6

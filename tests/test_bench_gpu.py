@@ -26,7 +26,10 @@ def run_bench(*args):
 @pytest.mark.gpu
 @pytest.mark.parametrize("workload", ["single_head_fp32", "mha_N2048_d64", "decode_N32768_d128_h8"])
 def test_bench_line(cuda, workload):
-    d = run_bench("--workload", workload, "--steps", "3", "--warmup", "3", "--no-cpu-baseline")
+    args = ["--workload", workload, "--steps", "3", "--warmup", "3", "--no-cpu-baseline"]
+    if workload == "mha_N2048_d64":
+        args.append("--backward")
+    d = run_bench(*args)
     assert KEYS <= set(d), KEYS - set(d)
     assert d["value"] > 0 and d["e2e"]["value"] > 0 and d["gpu_launches"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
@@ -48,3 +51,26 @@ def test_bench_decode_reports_bandwidth(cuda):
                   "--no-cpu-baseline", "--no-e2e")
     assert d["unit"] == "GB/s" and d["roofline"]["bound"] == "hbm" and d["roofline"]["unit"] == "GB/s"
     assert 0 < d["roofline"]["frac"] < 1.2
+
+
+@pytest.mark.gpu
+def test_bench_default_line_has_per_config_entries(cuda):
+    """The default line: the long-sequence causal forward, with one entry per other specified
+    workload (CUDA-event ms, TFLOPS, roofline fraction, dominant kernel, clocks, oracle baseline
+    for every one of them, the fp32 one included)."""
+    d = run_bench("--steps", "3", "--warmup", "3")
+    assert KEYS <= set(d), KEYS - set(d)
+    assert d["config"]["workload"] == "causal_N8192_d128" and d["config"]["step"] == "forward"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 3 * 8 * 32 * 8192 * 128 * 2
+    pc = d["per_config"]
+    assert sorted(pc) == sorted(["single_head_fp32", "mha_N2048_d64", "blocksparse_N16384_d64",
+                                 "bwd_causal_N4096_d128"])
+    for name, e in pc.items():
+        assert e["ms_per_step"] > 0 and e["tflops"] > 0, name
+        assert 0 < e["roofline"]["frac"] < 1.2 and e["roofline"]["kernel"], name
+        assert e["cpu_baseline"]["value"] > 0 and e["cpu_baseline"]["kind"] == "oracle", name
+        assert "clocks" in e and e["gpu_launches"] > 0, name
+    assert pc["single_head_fp32"]["roofline"]["bound"] == "alu"
+    assert pc["bwd_causal_N4096_d128"]["roofline"]["kernel"].startswith("bwd_tc_kernel<128>")
+    assert "bwd" in pc["bwd_causal_N4096_d128"]["parts"]

@@ -16,8 +16,18 @@ from oracle import attention as orc
 pytestmark = pytest.mark.gpu
 
 
-def run_and_compare(w: wl.Workload, device, rows_per_head=None, heads=None, relative_above_one=False):
-    """Runs the forward of workload w on the GPU; compares every row (or sampled rows/heads)."""
+def tile_rows(N, rng):
+    """Rows that put a sample in every CTA and every warp of it: in each 128-row query tile one
+    random row from each 32-row group (one softmax warp's TMEM lanes), plus the head's first and
+    last rows and the rows around the first tile boundary."""
+    picks = [np.arange(g, min(g + 32, N)) for g in range(0, N, 32)]
+    rows = [rng.choice(p) for p in picks]
+    return np.unique(np.concatenate([rows, [0, N - 1, min(N - 1, 127), min(N - 1, 128)]]))
+
+
+def run_and_compare(w: wl.Workload, device, rows="all", heads=None, relative_above_one=False):
+    """Runs the forward of workload w on the GPU and compares it with the oracle on every head
+    (or `heads` sampled ones): every row (rows="all") or the tile_rows sample (rows="tiles")."""
     inp = wl.make_inputs(w)
     q, k, v = (H.to_device(inp, n, device) for n in ("q", "k", "v"))
     mask_np = inp.raw("mask") if w.block_sparse else None
@@ -26,7 +36,6 @@ def run_and_compare(w: wl.Workload, device, rows_per_head=None, heads=None, rela
     fa.fa_check_device_error()
     o = o.float().cpu().numpy()
     lse = lse.cpu().numpy()
-    qf, kf, vf = inp.f64("q"), inp.f64("k"), inp.f64("v")
     rng = np.random.default_rng(1234)
     all_heads = [(b, h) for b in range(w.B) for h in range(w.H)]
     if heads is not None:
@@ -34,17 +43,13 @@ def run_and_compare(w: wl.Workload, device, rows_per_head=None, heads=None, rela
         all_heads = [all_heads[i] for i in sorted(sel)]
     worst = 0.0
     for b, h in all_heads:
-        if rows_per_head is None:
-            rows = np.arange(w.N)
-        else:
-            rows = np.unique(np.concatenate([
-                rng.choice(w.N, size=rows_per_head, replace=False),
-                [0, w.N - 1, min(w.N - 1, 127), min(w.N - 1, 128)]]))
-        O_ref, lse_ref = orc.forward_head(qf[b, h], kf[b, h], vf[b, h], w.softmax_scale,
-                                          causal=w.causal, block_mask=mask_np, rows=rows)
-        mx, _ = H.compare_o(o[b, h, rows], O_ref, bf16=(w.dtype == "bf16"),
+        sel_rows = np.arange(w.N) if rows == "all" else tile_rows(w.N, rng)
+        qf, kf, vf = (inp.f64_head(n, b, h) for n in ("q", "k", "v"))
+        O_ref, lse_ref = orc.forward_head(qf, kf, vf, w.softmax_scale, causal=w.causal,
+                                          block_mask=mask_np, rows=sel_rows)
+        mx, _ = H.compare_o(o[b, h, sel_rows], O_ref, bf16=(w.dtype == "bf16"),
                             relative_above_one=relative_above_one)
-        H.compare_lse(lse[b, h, rows], lse_ref)
+        H.compare_lse(lse[b, h, sel_rows], lse_ref)
         worst = max(worst, mx)
     return worst, o, lse
 
@@ -129,8 +134,21 @@ def test_mha_N2048_d64_full(cuda):
     run_and_compare(wl.WORKLOADS["mha_N2048_d64"], cuda)
 
 
-def test_causal_N8192_d128_sampled(cuda):
-    run_and_compare(wl.WORKLOADS["causal_N8192_d128"], cuda, rows_per_head=48, heads=6)
+def test_causal_N8192_d128_every_cta(cuda):
+    """The long-sequence causal workload at full size, in the bench's launch configuration: every
+    head, a row of every warp of every query tile (so every CTA of the launch)."""
+    run_and_compare(wl.WORKLOADS["causal_N8192_d128"], cuda, rows="tiles")
+
+
+@pytest.mark.parametrize("B,Hh,N,d,causal", [
+    (1, 9, 8192, 128, True),    # K/V of 8 heads fill the 32 MB head group: groups of 8 + 1
+    (3, 11, 2048, 128, False),  # groups of 32 + 1
+    (1, 35, 4096, 64, True),    # groups of 32 + 3
+])
+def test_partial_last_head_group(cuda, B, Hh, N, d, causal):
+    """CTAs walk heads in groups whose K/V fit in L2; here the last group is a partial one."""
+    w = wl.Workload("partial_group", B, Hh, N, d, causal=causal, seed=71)
+    run_and_compare(w, cuda, rows="tiles")
 
 
 # ------------------------------------------------------------------------- block-sparse
@@ -180,8 +198,14 @@ def test_causal_mask_above_diagonal_only_gives_empty_rows(cuda):
     H.compare_lse(lse[0, 0].cpu().numpy(), lse_ref)
 
 
-def test_blocksparse_N16384_d64_sampled(cuda):
-    run_and_compare(wl.WORKLOADS["blocksparse_N16384_d64"], cuda, rows_per_head=32, heads=4)
+def test_blocksparse_N16384_d64_every_cta(cuda):
+    run_and_compare(wl.WORKLOADS["blocksparse_N16384_d64"], cuda, rows="tiles")
+
+
+def test_blocksparse_partial_last_head_group(cuda):
+    # N = 16384, d = 64: 8 heads per L2 group, 10 heads -> groups of 8 + 2
+    w = wl.Workload("bs_partial_group", 1, 10, 16384, 64, block_sparse=True, seed=72)
+    run_and_compare(w, cuda, rows="tiles")
 
 
 def test_all_ones_mask_equals_dense_bitwise(cuda):

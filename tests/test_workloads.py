@@ -51,3 +51,31 @@ def test_make_inputs_shapes():
     w32 = wl.WORKLOADS["single_head_fp32"]
     inp32 = wl.make_inputs(w32)
     assert inp32.raw("k").dtype == np.float32 and inp32.f64("k").dtype == np.float64
+
+
+def test_e4m3_table_follows_the_format_definition():
+    v = wl.E4M3_VALUES
+    assert v[0x00] == 0.0 and v[0x01] == 2.0 ** -9 and v[0x07] == 7 * 2.0 ** -9  # subnormals
+    assert v[0x08] == 2.0 ** -6 and v[0x38] == 1.0 and v[0x7E] == 448.0
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF]) and v[0xB8] == -1.0
+    assert np.all(np.diff(v[:0x7F]) > 0)
+
+
+def test_e4m3_rounding_matches_torch_round_to_nearest_even():
+    x = wl.normal_f32((50000,), seed=8, stream=1) * np.float32(5.0)
+    mids = (wl.E4M3_VALUES[1:0x7E] + wl.E4M3_VALUES[2:0x7F]) / 2  # exact ties
+    x = np.concatenate([x, mids, -mids, wl.E4M3_VALUES[:0x7F], [2.0 ** -10, 3 * 2.0 ** -11]])
+    ours = wl.e4m3_bits_from_f32(x)
+    theirs = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert np.array_equal(ours, theirs.numpy())
+    assert np.all(wl.e4m3_bits_from_f32(np.array([500.0, -1e4])) == [0x7E, 0xFE])  # saturates
+
+
+def test_e4m3_inputs_decode_exactly():
+    w = wl.Workload("f8", 1, 2, 100, 128, dtype="e4m3", seed=3)
+    inp = wl.make_inputs(w)
+    assert inp.raw("q").dtype == np.uint8
+    x = wl.normal_f32((1, 2, 100, 128), 3, wl.STREAM_Q)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(inp.f64("q"), want)
+    assert np.array_equal(inp.f64_head("q", 0, 1), want[0, 1])
