@@ -46,6 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # Datasheet figures for one GB300 (dense, no sparsity), reported beside the measured peaks.
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_HBM_GBS = 7900.0
+FP8_OVER_BF16 = 4.5 / 2.25  # datasheet dense fp8 / bf16 tensor rates
 FP32_FMA_PER_CLK_PER_SM = 128  # fp32 FMA lanes per SM (four sub-partitions of 32)
 FLUSH_BYTES = 512 << 20        # > the 129 MB L2
 # Oracle rows per CPU task for forward-only workloads (a strided subset of one head's query rows).
@@ -332,9 +333,11 @@ class ClockSampler:
 
 def forward_kernel_name(w):
     """Name of the forward kernel the library runs for this workload (the two-query-tile kernel
-    for every bf16 forward)."""
+    for every bf16 and e4m3 forward)."""
     if w.dtype == "fp32":
         return f"fwd_fp32_kernel<{w.d}>"
+    if w.dtype == "e4m3":
+        return f"fwd_pair_kernel<{w.d}, true>"
     return f"fwd_pair_kernel<{w.d}>"
 
 
@@ -366,12 +369,15 @@ class Problem:
             a = inp.raw(name)
             if a.dtype == np.uint16:
                 return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+            if a.dtype == np.uint8 and name != "mask":  # e4m3 codes
+                return torch.from_numpy(a).to(dev).view(torch.float8_e4m3fn)
             return torch.from_numpy(a).to(dev)
 
         self.q, self.k, self.v = dev_tensor("q"), dev_tensor("k"), dev_tensor("v")
         self.do = dev_tensor("do") if w.backward else None
         self.mask = dev_tensor("mask") if w.block_sparse else None
-        self.o = torch.empty_like(self.q)
+        self.o = (torch.empty(self.q.shape, dtype=torch.bfloat16, device=dev)
+                  if w.dtype == "e4m3" else torch.empty_like(self.q))
         self.lse = torch.empty(self.q.shape[:3], dtype=torch.float32, device=dev)
         if w.backward:
             self.dq = torch.empty(self.q.shape, dtype=torch.float32, device=dev)
@@ -387,6 +393,8 @@ class Problem:
         o, lse = (self.o if o is None else o), (self.lse if lse is None else lse)
         if w.dtype == "fp32":
             fa.fa_fwd_fp32(q, k, v, o, lse, w.softmax_scale, w.causal)
+        elif w.dtype == "e4m3":
+            fa.fa_fwd_fp8(q, k, v, o, lse, w.softmax_scale, 1.0, w.causal)
         elif w.block_sparse:
             fa.fa_fwd_blocksparse(q, k, v, o, lse, w.softmax_scale, self.mask, w.causal)
         else:
@@ -466,11 +474,15 @@ def roofline_of(pr, kname, kflops, kms, peaks, peak_src):
     peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     src = "MEASURED_PEAKS.json" if peak_src == "measured" else "fallback"
+    nominal, what = NOMINAL_BF16_TFLOPS, f"{peak_src} bf16 dense (burst) {src}"
+    if pr.w.dtype == "e4m3":
+        # an fp8 contraction: the measured bf16 peak times the datasheet fp8 / bf16 ratio (2)
+        peak, sustained, nominal = (FP8_OVER_BF16 * x for x in (peak, sustained, nominal))
+        what = f"{peak_src} bf16 dense (burst) {src} x {FP8_OVER_BF16:g} (datasheet fp8 / bf16)"
     return {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": peak,
-            "unit": "TFLOP/s", "frac": achieved / peak,
-            "peak_source": f"{peak_src} bf16 dense (burst) {src}",
+            "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": what,
             "frac_of_sustained": achieved / sustained,
-            "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS, "nominal": NOMINAL_BF16_TFLOPS,
+            "frac_of_nominal": achieved / nominal, "nominal": nominal,
             "traffic": traffic}
 
 
@@ -645,9 +657,9 @@ def run_ours(args):
         "metric": metric_name(w), "value": job_tflops(world, pr.f_fwd + pr.f_bwd, t["step_ms"]),
         "unit": "TFLOPS", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": t["step_ms"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp32" if w.dtype == "fp32" else "bf16",
+        "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic: i.i.d. N(0,1) inputs, seeded"
-                + (", rounded to bf16" if w.dtype == "bf16" else ""),
+                + {"bf16": ", rounded to bf16", "e4m3": ", rounded to e4m3"}.get(w.dtype, ""),
         "config": config_of(w, world),
         "parts": parts_of(pr, t, peak),
         "roofline": roofline_of(pr, kname, kflops, kms, peaks, peak_src),

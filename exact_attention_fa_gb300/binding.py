@@ -31,6 +31,7 @@ SIGNATURES = [
     ("fa_fwd_fp32", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     ("fa_fwd_fp32_fa1", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     ("fa_fwd_blocksparse", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
+    ("fa_fwd_fp8", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _F, _I, _P]),
     ("fa_bwd_workspace_bytes", ctypes.c_size_t, [_I, _I, _I, _I]),
     ("fa_bwd", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
     ("fa_bwd_noalloc", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
@@ -152,6 +153,18 @@ def fa_fwd_blocksparse(q, k, v, o, lse, scale: float, block_mask, causal: bool =
           d, float(scale), int(bool(causal)), _ptr(block_mask), _stream(q))
 
 
+def fa_fwd_fp8(q, k, v, o, lse, scale: float, v_scale: float = 1.0, causal: bool = False):
+    """e4m3 forward: q, k, v torch.float8_e4m3fn [B,H,N,d] (d = 128); o bf16 and lse fp32
+    preallocated; o = v_scale * softmax(scale * q k^T) v."""
+    B, H, N, d = _bhnd(q, k, v, dtype=torch.float8_e4m3fn)
+    _bhnd(o)
+    if tuple(o.shape) != tuple(q.shape) or o.device != q.device:
+        raise ValueError("o must be a bf16 tensor of q's shape on q's device")
+    _rows(lse, q.shape)
+    _call("fa_fwd_fp8", q.device, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+          float(scale), float(v_scale), int(bool(causal)), _stream(q))
+
+
 def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return int(load().fa_bwd_workspace_bytes(B, H, N, d))
 
@@ -248,10 +261,17 @@ def fa_check_device_error(device=None):
 # ------------------------------------------------------------------------------- conveniences
 
 def attention_forward(q, k, v, scale: float | None = None, causal: bool = False, block_mask=None):
-    """Allocates O and lse with torch and runs the matching entry point (bf16 or fp32)."""
+    """Allocates O and lse with torch and runs the matching entry point (bf16, fp32 or e4m3;
+    e4m3 inputs give a bf16 O)."""
     scale = q.shape[-1] ** -0.5 if scale is None else scale
-    o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    if q.dtype == torch.float8_e4m3fn:
+        if block_mask is not None:
+            raise ValueError("the e4m3 forward takes no block mask")
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+        fa_fwd_fp8(q, k, v, o, lse, scale, 1.0, causal)
+        return o, lse
+    o = torch.empty_like(q)
     if q.dtype == torch.float32:
         if block_mask is not None:
             raise ValueError("block-sparse attention is bf16 only")

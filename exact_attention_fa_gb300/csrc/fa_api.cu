@@ -131,6 +131,20 @@ bool encode_f32_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view [B*H][N][d] of an 8-bit (e4m3) tensor, box 128 x rows x 1 (128-byte rows), 128-byte
+// swizzle, zero fill outside.
+bool encode_u8_map(CUtensorMap* map, const void* base, int BH, int N, int d, int rows = 128) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N) * d};
+  const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int to_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
 // One thread waits, with the kernels' bounded wait, on a barrier nobody arrives at.
@@ -176,6 +190,7 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.heads_per_group = static_cast<int>(g < 1 ? 1 : (g > BH ? BH : g));
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.o_scale = 1.f;
   p.err = ds->err;
   p.timeout_ns = kWaitTimeoutNs;
   if (static_cast<long long>(p.n_tiles) * BH > 0x7fffffffll) return FA_ERR_TOO_LARGE;
@@ -186,6 +201,41 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
   // causal N = 4096 1251 / 1125, dense B16 N = 512 593 / 554; d = 64 dense N = 2048 702-728 /
   // ~600; block-sparse d = 64 at 25% density 678 / 632.
   return to_status(fa::launch_fwd_pair(p, d, cs));
+}
+
+// The e4m3 forward: the bf16 forward's kernel with 8-bit tiles (d = 128); O stays bf16.
+int fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+            int d, float scale, float v_scale, int causal, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  int st = check_common(B, H, N, scale);
+  if (st != FA_OK) return st;
+  if (!isfinite(v_scale)) return FA_ERR_INVALID_ARG;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != FA_OK) return st;
+  fa::FwdParams p{};
+  const int BH = B * H;
+  if (!encode_u8_map(&p.tm_q, q, BH, N, d) || !encode_u8_map(&p.tm_k, k, BH, N, d) ||
+      !encode_u8_map(&p.tm_v, v, BH, N, d) || !encode_bf16_map(&p.tm_o, o, BH, N, d))
+    return FA_ERR_CUDA;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.block_mask = nullptr;
+  p.BH = BH;
+  p.N = N;
+  p.n_tiles = (N + 127) / 128;
+  const long long kv_bytes_per_head = 2ll * N * d;
+  long long g = (32ll << 20) / kv_bytes_per_head;
+  p.heads_per_group = static_cast<int>(g < 1 ? 1 : (g > BH ? BH : g));
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.o_scale = v_scale;
+  p.err = ds->err;
+  p.timeout_ns = kWaitTimeoutNs;
+  if (static_cast<long long>(p.n_tiles) * BH > 0x7fffffffll) return FA_ERR_TOO_LARGE;
+  return to_status(fa::launch_fwd_fp8(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 // CTAs for decoding: as many as the SMs hold at once, never more than there are key blocks.
@@ -266,7 +316,7 @@ int fa::check_bwd_args(const void* q, const void* k, const void* v, const void* 
 
 extern "C" {
 
-int fa_abi_version(void) { return (2 << 16) | 4; }
+int fa_abi_version(void) { return (2 << 16) | 5; }
 
 const char* fa_status_string(int status) {
   switch (status) {
@@ -294,6 +344,11 @@ int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, flo
                        int H, int N, int d, float scale, int causal, const uint8_t* block_mask,
                        fa_stream_t stream) {
   return fwd_bf16(q, k, v, o, lse, B, H, N, d, scale, causal, true, block_mask, stream);
+}
+
+int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int N, int d, float scale, float v_scale, int causal, fa_stream_t stream) {
+  return fwd_fp8(q, k, v, o, lse, B, H, N, d, scale, v_scale, causal, stream);
 }
 
 namespace {

@@ -19,12 +19,16 @@
 //   * warps 0-3 / 4-7 are the softmax warpgroups of tile 0 / 1: thread r owns query row r (TMEM
 //     lane r). It loads its 128 scores, applies the scale (log2(e) folded in, exp2 on the SFU),
 //     the causal / tail mask, updates m and l, rescales its O row only when the reference max
-//     moves (conditional rescaling), writes P as bf16 into TMEM, and finally normalises O and
-//     writes O and lse.
+//     moves (conditional rescaling), writes P as bf16 (e4m3 for e4m3 inputs) into TMEM, and
+//     finally normalises O and writes O and lse.
 //   * causal / block-sparse: key tiles a query tile does not need are never loaded nor multiplied
 //     ("3 · FlashAttention", question on the causal mask; "拡張: Block-Sparse FlashAttention").
-// TMEM columns: d = 128: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512), P_t over S_t;
-// d = 64: S_0, S_1 as above, P_0 [256,320), P_1 [320,384), O_0 [384,448), O_1 [448,512).
+// TMEM columns: d = 128: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512), P_t over S_t
+// (e4m3 P: the first 32 columns of S_t); d = 64: S_0, S_1 as above, P_0 [256,320), P_1 [320,384),
+// O_0 [384,448), O_1 [448,512).
+// The same kernel serves e4m3 inputs at d = 128 ("3 · FlashAttention", 3.5, the FP8 support of
+// FlashAttention-3): both products run as tcgen05.mma kind::f8f6f4 on e4m3 operands with fp32
+// accumulation; P is rounded to e4m3 for the P V product, l sums the unrounded fp32 P.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -48,13 +52,22 @@ static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsLoadMma <= kThreads * 168,
 constexpr int kBoxBytes = 128 * 64 * 2;  // one TMA box: 128 rows x 64 bf16 (128 B rows)
 constexpr float kRescaleSlack = 8.f;     // log2 units: P stays <= 256
 
-template <int D>
+// F8: e4m3 Q, K, V (d = 128 only): a tile row is 128 bytes, one TMA box; the products are
+// tcgen05.mma kind::f8f6f4 and P goes to TMEM as e4m3. O is still written as bf16, through a
+// staging area of its own (the 16 KB e4m3 Q tile is too small for the 32 KB bf16 O tile).
+template <int D, bool F8 = false>
 struct Cfg {
-  static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kStages = D == 128 ? 4 : 8;  // K/V ring (K and V tiles alternate)
+  static_assert(!F8 || D == 128, "the e4m3 forward is built for d = 128");
+  static constexpr int kElemBytes = F8 ? 1 : 2;
+  static constexpr int kTileBytes = 128 * D * kElemBytes;
+  static constexpr int kBoxCols = 128 / kElemBytes;  // elements per 128-byte TMA box row
+  static constexpr int kBoxes = D / kBoxCols;        // TMA boxes per tile
+  static constexpr int kStages = F8 ? 8 : (D == 128 ? 4 : 8);  // K/V ring (K, V alternate)
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
-  static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
+  static constexpr int kOTileBytes = 128 * D * 2;  // one bf16 O tile
+  static constexpr int kOffOStage = kOffKV + kStages * kTileBytes;  // F8 only
+  static constexpr int kOffBar = kOffOStage + (F8 ? 2 * kOTileBytes : 0);
   // barriers: Q, full[S], empty[S], s_full[2], p_full[2], o_full[2], pv_done[2], s_free[2],
   // drain[2]
   static constexpr int kBarQ = 0;
@@ -129,10 +142,10 @@ __device__ __forceinline__ void decode_work(const FwdParams& p, int& bh, int& pa
 }
 
 // ---------------------------------------------------------------------------------------------
-template <int D>
+template <int D, bool F8>
 __device__ void producer(const FwdParams& p, uint32_t sbase, const Ctl& ctl, int bh, int qt0,
                          int qt1) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
   tma_prefetch_desc(&p.tm_q);
   tma_prefetch_desc(&p.tm_k);
@@ -140,9 +153,9 @@ __device__ void producer(const FwdParams& p, uint32_t sbase, const Ctl& ctl, int
 
   mbar_arrive_expect_tx(bar(C::kBarQ), 2 * C::kTileBytes);
   for (int t = 0; t < 2; ++t)
-    for (int b = 0; b < D / 64; ++b)
+    for (int b = 0; b < C::kBoxes; ++b)
       tma_load_3d(sbase + C::kOffQ + t * C::kTileBytes + b * kBoxBytes, &p.tm_q, bar(C::kBarQ),
-                  b * 64, (t ? qt1 : qt0) * BM, bh);
+                  b * C::kBoxCols, (t ? qt1 : qt0) * BM, bh);
 
   int issued[C::kStages];
 #pragma unroll
@@ -156,9 +169,9 @@ __device__ void producer(const FwdParams& p, uint32_t sbase, const Ctl& ctl, int
     const int round = pos / C::kStages;
     if (!mbar_wait_warp(bar(C::kBarEmpty + s), (round & 1) ^ 1, ctl)) return false;
     mbar_arrive_expect_tx(bar(C::kBarFull + s), C::kTileBytes);
-    for (int b = 0; b < D / 64; ++b)
+    for (int b = 0; b < C::kBoxes; ++b)
       tma_load_3d(sbase + C::kOffKV + s * C::kTileBytes + b * kBoxBytes, map, bar(C::kBarFull + s),
-                  b * 64, j * BN, bh);
+                  b * C::kBoxCols, j * BN, bh);
     issued[s] = round;
     ++pos;
     return true;
@@ -190,32 +203,45 @@ __device__ void producer(const FwdParams& p, uint32_t sbase, const Ctl& ctl, int
 // every ring position in the producer's order and release each one (the empty barriers count
 // both); a warp waits for a position to be full before releasing it even when its tile skips
 // that key tile, so neither can release a stage ahead of the other's use of it.
-template <int D>
+template <int D, bool F8>
 __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, const Ctl& ctl,
                            int qt0, int qt1, int t) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
-  constexpr uint32_t kIdescQK = idesc_bf16(128, BN, 0, 0);  // A = Q (K-major), B = K (K-major)
-  constexpr uint32_t kIdescPV = idesc_bf16(128, D, 0, 1);   // A = P (TMEM), B = V (MN-major)
+  // A = Q (K-major), B = K (K-major); PV: A = P (TMEM), B = V (MN-major)
+  constexpr uint32_t kIdescQK = F8 ? idesc_e4m3(128, BN, 0, 0) : idesc_bf16(128, BN, 0, 0);
+  constexpr uint32_t kIdescPV = F8 ? idesc_e4m3(128, D, 0, 1) : idesc_bf16(128, D, 0, 1);
 
   // Descriptors precomputed once (Q_t per K-step, first K and V stage); a stage is a constant
-  // offset away, so each MMA costs the issuing thread one add.
+  // offset away, so each MMA costs the issuing thread one add. A K-step covers 32 bytes of a
+  // 128-byte swizzle row (16 bf16 or 32 e4m3), four steps per TMA box.
   constexpr uint32_t kHi = sdesc_hi_sw128(1024);
   constexpr uint64_t kStageStep = C::kTileBytes >> 4;
-  uint64_t qd[D / 16];
+  constexpr int kSteps = D * C::kElemBytes / 32;
+  uint64_t qd[kSteps];
 #pragma unroll
-  for (int k = 0; k < D / 16; ++k)
+  for (int k = 0; k < kSteps; ++k)
     qd[k] = sdesc64(
         sdesc_lo(sbase + C::kOffQ + t * C::kTileBytes + (k / 4) * kBoxBytes + (k % 4) * 32, 16), kHi);
   const uint64_t kd0 = sdesc64(sdesc_lo(sbase + C::kOffKV, 16), kHi);
   const uint64_t vd0 = sdesc64(sdesc_lo(sbase + C::kOffKV, kBoxBytes), kHi);
   const uint32_t tS = tmem + C::col_s(t);
   auto issue_s = [&](int stage) {
-    if constexpr (D == 128)
+    if constexpr (F8)
+      mma_qk_f8_d128(tS, qd, kd0 + stage * kStageStep, kIdescQK);
+    else if constexpr (D == 128)
       mma_qk_d128(tS, qd, kd0 + stage * kStageStep, kIdescQK);
     else
       mma_qk_d64(tS, qd, kd0 + stage * kStageStep, kIdescQK);
     mma_commit(bar(C::kBarS + t));
+  };
+  auto issue_pv = [&](int stage, bool accumulate) {
+    if constexpr (F8)
+      mma_pv_f8_k128(tmem + C::col_o(t), tmem + C::col_p(t), vd0 + stage * kStageStep, kIdescPV,
+                     accumulate ? 1u : 0u);
+    else
+      mma_pv_k128(tmem + C::col_o(t), tmem + C::col_p(t), vd0 + stage * kStageStep, kIdescPV,
+                  accumulate ? 1u : 0u);
   };
 
   bool ok = mbar_wait_warp(bar(C::kBarQ), 0, ctl);
@@ -267,8 +293,7 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
         if (!(ok = mbar_wait_warp(bar(C::kBarP + t), pphase, ctl))) break;
         pphase ^= 1;
         tc_fence_after();
-        mma_pv_k128(tmem + C::col_o(t), tmem + C::col_p(t), vd0 + sv * kStageStep, kIdescPV,
-                    acc ? 1u : 0u);
+        issue_pv(sv, acc);
         mma_commit(bar(C::kBarPV + t));
         acc = true;
       }
@@ -278,8 +303,7 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
         if (!(ok = mbar_wait_warp(bar(C::kBarP + t), pphase, ctl))) break;
         pphase ^= 1;
         tc_fence_after();
-        mma_pv_k128(tmem + C::col_o(t), tmem + C::col_p(t), vd0 + sv * kStageStep, kIdescPV,
-                    acc ? 1u : 0u);
+        issue_pv(sv, acc);
         acc = true;
       }
       // S_t of the next tile overwrites P_t of this one: one thread's MMAs run in issue order,
@@ -304,10 +328,10 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
 }
 
 // ---------------------------------------------------------------------------------------------
-template <int D>
+template <int D, bool F8>
 __device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, uint32_t tmem,
                            const Ctl& ctl, int bh, int qt0, int qt1) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int t = warp / 4;
@@ -407,6 +431,7 @@ __device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, ui
 #pragma unroll
     for (int c = 0; c < 128; c += 32) {
       uint32_t pk[16];
+      float q0 = 0.f, q1 = 0.f;  // e4m3: the pair of an even i, packed with the next pair
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const unsigned long long x = f2_fma(
@@ -415,10 +440,23 @@ __device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, ui
         f2_unpack(x, x0, x1);
         const float p0 = ex2(x0), p1 = ex2(x1);
         rs[i & 3] = f2_add(rs[i & 3], f2_pack(p0, p1));
-        pk[i] = pack_bf16(p0, p1);
+        if constexpr (F8) {
+          // four e4m3 per TMEM column (keys 4u .. 4u + 3 of this chunk in bytes 0 .. 3)
+          if (i & 1) {
+            pk[i / 2] = pack_e4m3x4(q0, q1, p0, p1);
+          } else {
+            q0 = p0;
+            q1 = p1;
+          }
+        } else {
+          pk[i] = pack_bf16(p0, p1);
+        }
       }
       if (c == 0 && !wait_pv()) fail = true;
-      tmem_st16(tP + c / 2, pk);
+      if constexpr (F8)
+        tmem_st8(tP + c / 4, pk);
+      else
+        tmem_st16(tP + c / 2, pk);
     }
     if (fail) { ok = false; break; }
     float rs0, rs1;
@@ -439,10 +477,14 @@ __device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, ui
     const bool bad = !mbar_wait(bar(C::kBarO + t), 0, ctl);
     if (bar_red_or(1 + t, 128, bad)) return;
     tc_fence_after();
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    // O / l as bf16 into this tile's Q buffer (free: every MMA has completed), 128-byte swizzled
-    // like the TMA boxes; one thread then stores the tile with the TMA (rows past N are clipped).
-    uint8_t* srow = smem + C::kOffQ + t * C::kTileBytes + r * 128;
+    float inv = l > 0.f ? 1.f / l : 0.f;
+    if constexpr (F8) inv *= p.o_scale;
+    // O / l as bf16 into this tile's Q buffer (free: every MMA has completed; e4m3: the staging
+    // area), 128-byte swizzled like the TMA boxes; one thread then stores the tile with the TMA
+    // (rows past N are clipped).
+    constexpr int kOStage = F8 ? C::kOffOStage : C::kOffQ;
+    constexpr int kOTile = F8 ? C::kOTileBytes : C::kTileBytes;
+    uint8_t* srow = smem + kOStage + t * kOTile + r * 128;
 #pragma unroll 1
     for (int c = 0; c < D; c += 32) {
       uint32_t o[32];
@@ -463,7 +505,7 @@ __device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, ui
     bar_sync(1 + t, 128);
     if (threadIdx.x == 128 * t) {
       for (int b = 0; b < D / 64; ++b)
-        tma_store_3d(&p.tm_o, sbase + C::kOffQ + t * C::kTileBytes + b * kBoxBytes, b * 64, qt * BM, bh);
+        tma_store_3d(&p.tm_o, sbase + kOStage + t * kOTile + b * kBoxBytes, b * 64, qt * BM, bh);
       bulk_commit();
       bulk_wait_all();
     }
@@ -477,9 +519,9 @@ __device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, ui
 }
 
 // ---------------------------------------------------------------------------------------------
-template <int D>
+template <int D, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1) fwd_pair_kernel(const __grid_constant__ FwdParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -524,13 +566,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_pair_kernel(const __grid_cons
   if (warp >= kLoadWarp) {
     regs_dec<kRegsLoadMma>();
     if (warp == kLoadWarp)
-      producer<D>(p, sbase, ctl, bh, qt0, qt1);  // whole warp: one elected lane issues
+      producer<D, F8>(p, sbase, ctl, bh, qt0, qt1);  // whole warp: one elected lane issues
     else if (warp == kMmaWarp || warp == kMmaWarp + 1)
-      mma_issuer<D>(p, sbase, tmem, ctl, qt0, qt1, warp - kMmaWarp);  // one elected lane issues
+      mma_issuer<D, F8>(p, sbase, tmem, ctl, qt0, qt1, warp - kMmaWarp);  // one elected lane
     __syncwarp();
   } else {
     regs_inc<kRegsSoftmax>();
-    softmax_wg<D>(p, smem, sbase, tmem, ctl, bh, qt0, qt1);
+    softmax_wg<D, F8>(p, smem, sbase, tmem, ctl, bh, qt0, qt1);
   }
 
   tc_fence_before();
@@ -541,25 +583,28 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_pair_kernel(const __grid_cons
   }
 }
 
-template <int D>
+template <int D, bool F8 = false>
 cudaError_t configure() {
-  return cudaFuncSetAttribute(fwd_pair_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Cfg<D>::kSmemBytes);
+  return cudaFuncSetAttribute(fwd_pair_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<D, F8>::kSmemBytes);
 }
 
-template <int D>
+template <int D, bool F8 = false>
 cudaError_t launch(const FwdParams& p, cudaStream_t s) {
   const unsigned grid = static_cast<unsigned>((p.n_tiles + 1) / 2) * static_cast<unsigned>(p.BH);
-  fwd_pair_kernel<D><<<grid, kThreads, Cfg<D>::kSmemBytes, s>>>(p);
+  fwd_pair_kernel<D, F8><<<grid, kThreads, Cfg<D, F8>::kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t configure_fwd_pair() {
-  const cudaError_t e = configure<64>();
-  return e != cudaSuccess ? e : configure<128>();
+  cudaError_t e = configure<64>();
+  if (e == cudaSuccess) e = configure<128>();
+  return e != cudaSuccess ? e : configure<128, true>();
 }
+
+cudaError_t launch_fwd_fp8(const FwdParams& p, cudaStream_t s) { return launch<128, true>(p, s); }
 
 cudaError_t launch_fwd_pair(const FwdParams& p, int d, cudaStream_t s) {
   if (d == 64) return launch<64>(p, s);

@@ -24,6 +24,7 @@ struct FwdParams {
   int heads_per_group;        // CTA order: groups of heads whose K/V fit in L2
   int causal;                 // key j > query i masked (combines with a tile mask)
   float scale_log2;           // scale * log2(e)
+  float o_scale;              // e4m3 inputs: O is multiplied by this (the scale of V)
   unsigned* err;
   unsigned long long timeout_ns;
 };
@@ -104,6 +105,8 @@ int check_bwd_args(const void* q, const void* k, const void* v, const void* o, c
 
 // Launchers; return a cudaError_t (cudaSuccess on success).
 cudaError_t launch_fwd_pair(const FwdParams& p, int d, cudaStream_t s);               // 2 tiles/CTA
+// The same kernel on e4m3 Q, K, V at d = 128 (tm_q, tm_k, tm_v: 8-bit maps, box 128 x 128 x 1).
+cudaError_t launch_fwd_fp8(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_fwd_fp32(const Fp32FwdParams& p, cudaStream_t s);
 cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t s);

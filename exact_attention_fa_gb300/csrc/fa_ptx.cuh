@@ -366,6 +366,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       FA_W8(0), FA_W8(8)
       : "memory");
 }
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+                   taddr),
+               FA_W8(0)
+               : "memory");
+}
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -489,6 +495,38 @@ __device__ __forceinline__ void mma_ss_k128_mn(uint32_t d_tmem, uint64_t a, uint
       "l"(a), "l"(b), "r"(idesc)
       : "memory");
 }
+// 8-bit operands (tcgen05.mma kind::f8f6f4, e4m3 A and B, fp32 accumulate): one K-step is 32
+// elements = 32 bytes, the same byte width as a 16-bit K-step, so a K-major 128-byte-swizzled
+// tile (rows of 128 e4m3) advances its descriptor by 2 (16-byte units) per step.
+// S = Q K^T at d = 128: four K-steps inside one swizzle atom row, A and B both K-major.
+__device__ __forceinline__ void mma_qk_f8_d128(uint32_t d_tmem, const uint64_t (&a)[4], uint64_t b,
+                                               uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .b64 tb;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %5, %6, 0;\n\t"
+      "add.s64 tb, %5, 2;\n\t@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %2, tb, %6, 1;\n\t"
+      "add.s64 tb, %5, 4;\n\t@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, tb, %6, 1;\n\t"
+      "add.s64 tb, %5, 6;\n\t@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %4, tb, %6, 1;\n\t"
+      "}\n" ::"r"(d_tmem),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b), "r"(idesc)
+      : "memory");
+}
+// O (+)= P V over 128 keys with e4m3 operands: A = P in TMEM (four e4m3 per 32-bit column, so a
+// 32-key K-step is 8 columns), B = V MN-major (rows of 128 e4m3; 32 keys = four 8-row groups =
+// 4 KB per K-step, i.e. +256 in 16-byte units).
+__device__ __forceinline__ void mma_pv_f8_k128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .pred p;\n\t.reg .b64 tb;\n\t.reg .b32 ta;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t"
+      "add.s32 ta, %1, 8;\n\tadd.s64 tb, %2, 256;\n\t@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 16;\n\tadd.s64 tb, %2, 512;\n\t@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ta], tb, %3, 1;\n\t"
+      "add.s32 ta, %1, 24;\n\tadd.s64 tb, %2, 768;\n\t@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ta], tb, %3, 1;\n\t"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __host__ __device__ constexpr uint64_t sdesc64(uint32_t lo, uint32_t hi) {
   return (static_cast<uint64_t>(hi) << 32) | lo;
 }
@@ -498,6 +536,14 @@ __host__ __device__ constexpr uint64_t sdesc64(uint32_t lo, uint32_t hi) {
 //   15 A major (0 = K, 1 = MN), 16 B major, 17-22 N >> 3, 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, int b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
+         (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f8f6f4 with e4m3 A and B (format code 0 in bits
+// 7-9 and 10-12), fp32 D, dense; the other fields as in idesc_bf16.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, int a_mn_major, int b_mn_major) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
          (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
@@ -539,6 +585,18 @@ __device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsig
   unsigned long long d;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
+}
+// Four fp32 values rounded to e4m3 (nearest, ties to even, saturating at +-448), packed with the
+// first in the lowest byte. cvt's first source goes to the upper byte of each pair.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float p0, float p1, float p2, float p3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(p0), "f"(p1), "f"(p2), "f"(p3));
+  return r;
 }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);

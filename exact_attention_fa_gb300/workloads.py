@@ -147,6 +147,10 @@ WORKLOADS = {
                                      seed=11),
 }
 
+# The long-sequence causal problem with e4m3 inputs (the FP8 forward; O bf16).
+WORKLOADS["causal_N8192_d128_fp8"] = Workload("causal_N8192_d128_fp8", 8, 32, 8192, 128,
+                                              dtype="e4m3", causal=True, seed=12)
+
 # The five specified workloads in their order (the seed of each is its position).
 SPECIFIED = ["single_head_fp32", "mha_N2048_d64", "causal_N8192_d128", "blocksparse_N16384_d64",
              "bwd_causal_N4096_d128"]

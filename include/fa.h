@@ -88,6 +88,19 @@ int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, flo
                        int H, int N, int d, float scale, int causal, const uint8_t* block_mask,
                        fa_stream_t stream);
 
+/* Forward with e4m3 (8-bit float: 4 exponent bits, 3 mantissa bits, OCP "e4m3fn") inputs, the
+ * FP8 support the FlashAttention-3 row of "3 · FlashAttention" (mkdocs.reaper.mx), 3.5, lists.
+ * q, k, v : [B,H,N,d] e4m3 bytes (read);  o : [B,H,N,d] bf16 (written);  lse : [B,H,N] fp32
+ * (written), as fa_fwd. Both products run on the tensor cores with e4m3 operands and fp32
+ * accumulation: S = scale * Q K^T, and P (the exponentials, at most 2^8 against the running max)
+ * is rounded to e4m3 for the product with V, while the row sum l adds the unrounded fp32 values.
+ * The result is o = v_scale * softmax(S) V and lse = log-sum-exp of S: for tensors quantised as
+ * x = s_x * x8, pass scale * s_q * s_k as `scale` and s_v as `v_scale`. d = 128 only
+ * (FA_ERR_UNSUPPORTED otherwise); any N >= 1; causal as fa_fwd. Errors as fa_fwd, plus
+ * FA_ERR_INVALID_ARG for a non-finite v_scale. */
+int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int N, int d, float scale, float v_scale, int causal, fa_stream_t stream);
+
 /* Bytes of device workspace fa_bwd needs, per row of B*H*ceil(N/128)*128 rows (rows padded to
  * whole 128-row tiles): two fp32 row statistics (8 bytes) and, at d = 64, two 32-byte bf16
  * operand rows made from them (72 bytes in all). 0 for B, H, N < 1 or d not in {64, 128}. */
@@ -182,7 +195,7 @@ const char* fa_status_string(int status);
 
 /* ABI version: (major << 16) | minor. Major 2: fa_fwd_blocksparse takes a causal flag; minor 1:
  * fa_decode; minor 2: fa_bwd_blocksparse; minor 3: fa_fwd_fp32_fa1; minor 4:
- * fa_bwd_workspace_bytes depends on d (8 bytes per row at d = 128). */
+ * fa_bwd_workspace_bytes depends on d (8 bytes per row at d = 128); minor 5: fa_fwd_fp8. */
 int fa_abi_version(void);
 
 #ifdef __cplusplus

@@ -1,8 +1,8 @@
 """Runs the fp64 oracle on one (b, h) head for the CPU-baseline timing of bench.py.
 
 Test/benchmark infrastructure only (imported by bench.py's cpu_baseline leg and its reference
-arm). It holds no arithmetic of its own: it decodes the seeded inputs (bf16 bit patterns or fp32)
-and calls the oracle's forward and backward as they stand.
+arm). It holds no arithmetic of its own: it decodes the seeded inputs (bf16 bit patterns, e4m3
+codes or fp32) and calls the oracle's forward and backward as they stand.
 """
 from __future__ import annotations
 
@@ -14,6 +14,9 @@ from . import attention as orc
 def _f64(a: np.ndarray) -> np.ndarray:
     if a.dtype == np.uint16:  # bf16 bit patterns
         return (a.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    if a.dtype == np.uint8:  # e4m3 codes, decoded by the input generator's table
+        from exact_attention_fa_gb300.workloads import e4m3_bits_to_f64
+        return e4m3_bits_to_f64(a)
     return a.astype(np.float64)
 
 

@@ -18,8 +18,8 @@ def to_device(inp: wl.Inputs, name: str, device) -> torch.Tensor:
     a = inp.raw(name)
     if a.dtype == np.uint16:
         return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
-    if a.dtype == np.uint8:
-        return torch.from_numpy(a).to(device)
+    if a.dtype == np.uint8 and name != "mask":  # e4m3 codes
+        return torch.from_numpy(a).to(device).view(torch.float8_e4m3fn)
     return torch.from_numpy(a).to(device)
 
 

@@ -20,7 +20,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for want in ("fa_fwd", "fa_fwd_fp32", "fa_fwd_fp32_fa1", "fa_fwd_blocksparse", "fa_bwd", "fa_bwd_workspace_bytes",
+    for want in ("fa_fwd", "fa_fwd_fp32", "fa_fwd_fp32_fa1", "fa_fwd_blocksparse", "fa_fwd_fp8",
+                 "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_noalloc",
                  "fa_decode", "fa_decode_ctas", "fa_decode_workspace_bytes",
                  "fa_check_device_error", "fa_status_string", "fa_abi_version"):
         assert want in names
@@ -182,3 +183,15 @@ def test_bwd_noalloc_scratch_limit_after_argument_checks(lib):
     if not torch.cuda.is_available():
         assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 58240, 64, 0.125, 0, None) == 6
         assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 524288, 128, 0.125, 0, None) == 6
+
+
+def test_fp8_validation(lib):
+    import torch
+    base = (fake(), fake(), fake(), fake(), fake(), 1, 1, 256)
+    if not torch.cuda.is_available():
+        assert lib.fa_fwd_fp8(*base, 128, 0.088, 1.0, 0, None) == 6  # valid: no device here
+    assert lib.fa_fwd_fp8(*base, 64, 0.088, 1.0, 0, None) == 2      # d = 128 only
+    assert lib.fa_fwd_fp8(*base, 128, 0.088, float("inf"), 0, None) == 1
+    assert lib.fa_fwd_fp8(*base, 128, -1.0, 1.0, 0, None) == 1
+    assert lib.fa_fwd_fp8(P(0), *base[1:], 128, 0.088, 1.0, 0, None) == 1
+    assert lib.fa_fwd_fp8(fake(0x10001), *base[1:], 128, 0.088, 1.0, 0, None) == 3

@@ -51,3 +51,23 @@ def test_missing_library_raises(monkeypatch, tmp_path):
     monkeypatch.setattr(fa, "_lib", None)
     with pytest.raises(fa.FAError, match="missing"):
         fa.load(str(tmp_path / "libfa_gb300.so"))
+
+
+def test_oracle_side_loads_no_product_code():
+    """The oracle and the input generator import neither the binding nor the library."""
+    import subprocess
+    import sys
+    code = ("import sys, oracle.cpu_baseline, oracle.attention; "
+            "import exact_attention_fa_gb300.workloads; "
+            "bad = [m for m in ('exact_attention_fa_gb300.binding', 'exact_attention_fa_gb300.build',"
+            " 'torch') if m in sys.modules]; print(bad); assert not bad")
+    root = __import__("os").path.dirname(__import__("os").path.dirname(__file__))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+
+
+def test_package_exports_resolve_lazily():
+    import exact_attention_fa_gb300 as pkg
+    assert pkg.fa_fwd is fa.fa_fwd and pkg.fa_fwd_fp8 is fa.fa_fwd_fp8
+    with pytest.raises(AttributeError):
+        pkg.no_such_entry_point
