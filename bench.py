@@ -7,7 +7,8 @@ C ABI of libfa_gb300.so. The default workload is the long-sequence causal forwar
 N=8192, d=128, bf16 (the largest specified problem); the same line carries a `per_config` object
 with one entry for each of the other specified workloads (the fp32 single head, the multi-head
 N=2048 forward, the block-sparse N=16384 forward and the causal N=4096 backward), each timed
-the same way, with its own roofline fraction, clocks and oracle baseline.
+the same way, with its own roofline fraction, clocks and oracle baseline, and a `next_rows` object
+with the FP8 (e4m3) forward on the long-sequence shape, measured against the fp8 peak.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--backward]
                   [--no-per-config] [--impl ours|reference]
@@ -82,6 +83,11 @@ def per_config_names(main_name: str):
     """The specified workloads other than the line's own, in their specified order."""
     from exact_attention_fa_gb300 import workloads as wl
     return [n for n in wl.SPECIFIED if n != main_name]
+
+
+# Workloads of rows past the specified ones, measured beside them on the default line: the FP8
+# forward on the long-sequence causal shape.
+NEXT_ROWS = ["causal_N8192_d128_fp8"]
 
 
 def flops(w, mask=None):
@@ -590,9 +596,10 @@ def run_ours(args):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     w = bench_workload(args.workload, args.backward)
     from exact_attention_fa_gb300 import workloads as wl
-    others = ([] if args.no_per_config or w.decode or args.workload != DEFAULT_WORKLOAD
-              else per_config_names(w.name))
-    cfg_w = {n: wl.WORKLOADS[n] for n in others}
+    default_line = not args.no_per_config and not w.decode and args.workload == DEFAULT_WORKLOAD
+    others = per_config_names(w.name) if default_line else []
+    nexts = list(NEXT_ROWS) if default_line else []
+    cfg_w = {n: wl.WORKLOADS[n] for n in others + nexts}
 
     # host inputs first; the oracle's worker pool (spawned) runs before CUDA is touched
     inp = wl.make_inputs(w, with_do=w.backward)
@@ -627,7 +634,7 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
     peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
 
-    per_config = {}
+    per_config, next_rows = {}, {}
     for n, cw in cfg_w.items():
         cpr = Problem(cw, cfg_inp[n], fa, dev)
         # a short probe sets the step count, then the timed run
@@ -635,7 +642,7 @@ def run_ours(args):
         steps = per_config_steps(probe["step_ms"], K)
         ct = time_problem(cpr, steps, max(3, args.warmup), flush_buf, world, dev, local)
         kname, kflops, kms = cpr.dominant(ct["fwd_ms"], ct["bwd_ms"])
-        per_config[n] = {
+        (next_rows if n in nexts else per_config)[n] = {
             "config": config_of(cw, world),
             "ms_per_step": ct["step_ms"], "steps": steps,
             "tflops": job_tflops(world, cpr.f_fwd + cpr.f_bwd, ct["step_ms"]),
@@ -671,6 +678,8 @@ def run_ours(args):
     }
     if per_config:
         line["per_config"] = per_config
+    if next_rows:
+        line["next_rows"] = next_rows
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

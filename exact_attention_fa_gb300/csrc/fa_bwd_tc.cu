@@ -731,27 +731,56 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   }
 }
 
+// L2 cache policies: O and dO are read once here (evict first); the zeroed dQ rows are written
+// to be kept (evict last), so that the main kernel's reductions find them in L2.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint4 ld_evict_first(const __nv_bfloat16* ptr, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void st_zero_evict_last(float* ptr, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %1, %1, %1}, %2;" ::"l"(ptr), "f"(0.f),
+               "l"(pol)
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------------------------
 // prep: D_i = sum_k dO_ik O_ik, lse2_i = lse_i * log2(e) (padding rows: D = 0, lse2 = +inf),
-// dQ rows zeroed. D / 8 threads per row, 8 elements each.
+// dQ rows zeroed. D / 8 threads per row, 8 elements each. The rows are walked from the last head
+// to the first: the main kernel starts with the first heads, whose zeroed dQ rows (and D, lse2)
+// are then the ones most recently written, still in L2, instead of being read back from DRAM.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ BwdParams p, int npad) {
   constexpr int kTpr = D / 8;
-  const long long total = static_cast<long long>(p.BH) * npad * kTpr;
+  const long long rows_total = static_cast<long long>(p.BH) * npad;
+  const long long total = rows_total * kTpr;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   const int lane = threadIdx.x % 32;
+  const uint64_t pol_first = l2_policy_evict_first(), pol_last = l2_policy_evict_last();
   for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t - lane < total;
        t += stride) {
     const bool valid = t < total;
-    const long long row = t / kTpr;
+    const long long row = rows_total - 1 - t / kTpr;
     const int part = static_cast<int>(t % kTpr);
     const int bh = static_cast<int>(row / npad);
     const int q = static_cast<int>(row % npad);
     float acc = 0.f;
     if (valid && q < p.N) {
       const size_t off = (static_cast<size_t>(bh) * p.N + q) * D + part * 8;
-      const uint4 a = *reinterpret_cast<const uint4*>(p.dO + off);
-      const uint4 b = *reinterpret_cast<const uint4*>(p.o + off);
+      const uint4 a = ld_evict_first(p.dO + off, pol_first);
+      const uint4 b = ld_evict_first(p.o + off, pol_first);
       const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
       const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
@@ -761,9 +790,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ B
         acc = fmaf(x.x, y.x, acc);
         acc = fmaf(x.y, y.y, acc);
       }
-      float4* dq = reinterpret_cast<float4*>(p.dq + off);
-      dq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      dq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      st_zero_evict_last(p.dq + off, pol_last);
+      st_zero_evict_last(p.dq + off + 4, pol_last);
     }
 #pragma unroll
     for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(~0u, acc, off);

@@ -72,5 +72,9 @@ def test_bench_default_line_has_per_config_entries(cuda):
         assert e["cpu_baseline"]["value"] > 0 and e["cpu_baseline"]["kind"] == "oracle", name
         assert "clocks" in e and e["gpu_launches"] > 0, name
     assert pc["single_head_fp32"]["roofline"]["bound"] == "alu"
+    f8 = d["next_rows"]["causal_N8192_d128_fp8"]
+    assert f8["config"]["dtype"] == "e4m3" and 0 < f8["roofline"]["frac"] < 1.2
+    assert f8["roofline"]["kernel"] == "fwd_pair_kernel<128, true>"
+    assert f8["roofline"]["peak"] > 1.9 * d["roofline"]["peak"]  # the fp8 peak
     assert pc["bwd_causal_N4096_d128"]["roofline"]["kernel"].startswith("bwd_tc_kernel<128>")
     assert "bwd" in pc["bwd_causal_N4096_d128"]["parts"]

@@ -79,3 +79,14 @@ def test_e4m3_inputs_decode_exactly():
     want = torch.from_numpy(x).to(torch.float8_e4m3fn).double().numpy()
     assert np.array_equal(inp.f64("q"), want)
     assert np.array_equal(inp.f64_head("q", 0, 1), want[0, 1])
+
+
+def test_e4m3_fast_rounding_equals_the_table_search():
+    """The integer-arithmetic rounding used for large inputs equals the table search."""
+    x = np.concatenate([wl.normal_f32((200000,), 1, 1) * np.float32(s)
+                        for s in (0.001, 0.02, 1.0, 30.0, 200.0)])
+    mids = (wl.E4M3_VALUES[1:0x7E] + wl.E4M3_VALUES[2:0x7F]) / 2
+    x = np.concatenate([x, mids, -mids, wl.E4M3_VALUES[:0x7F],
+                        [500.0, -1e4, 448.0, 464.0, 463.9, 2.0 ** -10, -2.0 ** -10, 0.0, -0.0]])
+    x = x.astype(np.float32)
+    assert np.array_equal(wl.e4m3_bits_from_f32_fast(x), wl.e4m3_bits_from_f32(x))
