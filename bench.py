@@ -357,7 +357,7 @@ def recorded_traffic(kname, w):
     except (OSError, ValueError):
         return None
     from exact_attention_fa_gb300 import build
-    entry = rec.get(f"{w.name}:{kname.split(' ')[0]}")
+    entry = rec.get(f"{w.name}:{kname.split(' (')[0]}")
     if not entry or entry.get("source_digest") != build.source_digest():
         return None
     return entry.get("dram_bytes_per_launch")

@@ -28,12 +28,13 @@ namespace {
 
 constexpr int kRows = 8;   // query rows (warps) per CTA
 constexpr int kKeys = 32;  // keys per shared-memory block
+constexpr int kThreads = kRows * 32;
 
 template <int D, bool kFA1>
 __global__ void __launch_bounds__(kRows * 32) fwd_fp32_kernel(const Fp32FwdParams p) {
   constexpr int C = D / 32;
   __shared__ float ks[kKeys][D + 1];  // +1: lane j reads row j without bank conflicts
-  __shared__ float vs[kKeys][D];
+  __shared__ __align__(16) float vs[kKeys][D];
   __shared__ float qs[kRows][D];
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -44,7 +45,8 @@ __global__ void __launch_bounds__(kRows * 32) fwd_fp32_kernel(const Fp32FwdParam
   const float* k = p.k + head;
   const float* v = p.v + head;
 
-  for (int i = threadIdx.x; i < kRows * D; i += blockDim.x) {
+#pragma unroll
+  for (int i = threadIdx.x; i < kRows * D; i += kThreads) {
     const int r = row0 + i / D;
     qs[i / D][i % D] = r < p.N ? q[static_cast<size_t>(r) * D + i % D] : 0.f;
   }
@@ -54,22 +56,52 @@ __global__ void __launch_bounds__(kRows * 32) fwd_fp32_kernel(const Fp32FwdParam
 #pragma unroll
   for (int c = 0; c < C; ++c) acc[c] = 0.f;
 
-  const int kend = p.causal ? min(p.N, row0 + kRows) : p.N;
-  for (int kb = 0; kb < kend; kb += kKeys) {
-    __syncthreads();
-    for (int i = threadIdx.x; i < kKeys * D; i += blockDim.x) {
-      const int j = kb + i / D, c = i % D;
+  // A key/value block is kKeys x D floats of each; thread t holds float4 number t + u * kThreads
+  // of both. The next block's loads are issued before this block's arithmetic, so the latency of
+  // global memory overlaps the work instead of adding to it once per block.
+  constexpr int kVec = kKeys * D / 4 / kThreads;  // D / 32
+  float4 kr[kVec], vr[kVec];
+  auto fetch = [&](int kb) {
+#pragma unroll
+    for (int u = 0; u < kVec; ++u) {
+      const int e = (threadIdx.x + u * kThreads) * 4;
+      const int j = kb + e / D;
+      const size_t off = static_cast<size_t>(j) * D + e % D;
       const bool in = j < p.N;
-      ks[i / D][c] = in ? k[static_cast<size_t>(j) * D + c] : 0.f;
-      vs[i / D][c] = in ? v[static_cast<size_t>(j) * D + c] : 0.f;
+      kr[u] = in ? *reinterpret_cast<const float4*>(k + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+      vr[u] = in ? *reinterpret_cast<const float4*>(v + off) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+  };
+  auto stash = [&]() {
+#pragma unroll
+    for (int u = 0; u < kVec; ++u) {
+      const int e = (threadIdx.x + u * kThreads) * 4;
+      const int r = e / D, c = e % D;
+      ks[r][c] = kr[u].x;
+      ks[r][c + 1] = kr[u].y;
+      ks[r][c + 2] = kr[u].z;
+      ks[r][c + 3] = kr[u].w;
+      *reinterpret_cast<float4*>(&vs[r][c]) = vr[u];
+    }
+  };
+
+  const int kend = p.causal ? min(p.N, row0 + kRows) : p.N;
+  if (kend > 0) fetch(0);
+  for (int kb = 0; kb < kend; kb += kKeys) {
+    __syncthreads();  // every warp is done with the previous block
+    stash();
     __syncthreads();
+    if (kb + kKeys < kend) fetch(kb + kKeys);
     if (row >= p.N) continue;
 
     const int j = kb + lane;
-    float s = 0.f;
-#pragma unroll 16
-    for (int c = 0; c < D; ++c) s = fmaf(qs[warp][c], ks[lane][c], s);
+    // the d-long dot product in four independent chains
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < D; c += 4)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) s4[u] = fmaf(qs[warp][c + u], ks[lane][c + u], s4[u]);
+    float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
     const bool ok = j < p.N && (!p.causal || j <= row);
     s = ok ? s * p.scale_log2 : -INFINITY;
 

@@ -169,6 +169,12 @@ WORKLOADS = {
 WORKLOADS["causal_N8192_d128_fp8"] = Workload("causal_N8192_d128_fp8", 8, 32, 8192, 128,
                                               dtype="e4m3", causal=True, seed=12)
 
+# Counter-capture cases of the e4m3 forward and of the backward on 8 heads (small device footprint).
+WORKLOADS["causal_N4096_d128_fp8_h8"] = Workload("causal_N4096_d128_fp8_h8", 1, 8, 4096, 128,
+                                                 dtype="e4m3", causal=True, seed=13)
+WORKLOADS["bwd_causal_N4096_d128_h8"] = Workload("bwd_causal_N4096_d128_h8", 1, 8, 4096, 128,
+                                                 causal=True, backward=True, seed=14)
+
 # The five specified workloads in their order (the seed of each is its position).
 SPECIFIED = ["single_head_fp32", "mha_N2048_d64", "causal_N8192_d128", "blocksparse_N16384_d64",
              "bwd_causal_N4096_d128"]
