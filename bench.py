@@ -8,7 +8,9 @@ N=8192, d=128, bf16 (the largest specified problem); the same line carries a `pe
 with one entry for each of the other specified workloads (the fp32 single head, the multi-head
 N=2048 forward, the block-sparse N=16384 forward and the causal N=4096 backward), each timed
 the same way, with its own roofline fraction, clocks and oracle baseline, and a `next_rows` object
-with the FP8 (e4m3) forward on the long-sequence shape, measured against the fp8 peak.
+with the FP8 (e4m3) forward on the long-sequence shape, measured against the fp8 peak, and the
+bf16 forwards of the long-sequence and multi-head workloads with part of the exponentials computed
+in software (fa_set_exp2_emulation), which is off by default.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--backward]
                   [--no-per-config] [--impl ours|reference]
@@ -88,6 +90,7 @@ def per_config_names(main_name: str):
 # Workloads of rows past the specified ones, measured beside them on the default line: the FP8
 # forward on the long-sequence causal shape.
 NEXT_ROWS = ["causal_N8192_d128_fp8"]
+EXP2_EMULATION_PER32 = 4  # fa_set_exp2_emulation's setting measured on the default line
 
 
 def flops(w, mask=None):
@@ -634,16 +637,14 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
     peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
 
-    per_config, next_rows = {}, {}
-    for n, cw in cfg_w.items():
-        cpr = Problem(cw, cfg_inp[n], fa, dev)
+    def measure(cpr, n):
         # a short probe sets the step count, then the timed run
         probe = time_problem(cpr, 3, max(3, min(args.warmup, 5)), flush_buf, world, dev, local)
         steps = per_config_steps(probe["step_ms"], K)
         ct = time_problem(cpr, steps, max(3, args.warmup), flush_buf, world, dev, local)
         kname, kflops, kms = cpr.dominant(ct["fwd_ms"], ct["bwd_ms"])
-        (next_rows if n in nexts else per_config)[n] = {
-            "config": config_of(cw, world),
+        return {
+            "config": config_of(cpr.w, world),
             "ms_per_step": ct["step_ms"], "steps": steps,
             "tflops": job_tflops(world, cpr.f_fwd + cpr.f_bwd, ct["step_ms"]),
             "parts": parts_of(cpr, ct, peak),
@@ -652,7 +653,27 @@ def run_ours(args):
             "gpu_launches": cpr.launches * steps,
             "clocks": ct["clocks"],
         }
+
+    per_config, next_rows = {}, {}
+    for n, cw in cfg_w.items():
+        cpr = Problem(cw, cfg_inp[n], fa, dev)
+        (next_rows if n in nexts else per_config)[n] = measure(cpr, n)
         del cpr
+    if default_line:
+        # the partial software exponential (4 of every 32 exponentials per row on the FMA
+        # pipes), off by default, measured beside the default on the same problems
+        for n, cpr in ((w.name, pr),
+                       ("mha_N2048_d64", Problem(cfg_w["mha_N2048_d64"],
+                                                 cfg_inp["mha_N2048_d64"], fa, dev))):
+            fa.fa_set_exp2_emulation(EXP2_EMULATION_PER32)
+            try:
+                e = measure(cpr, n)
+            finally:
+                fa.fa_set_exp2_emulation(0)
+            e["exp2_emulation_per32"] = EXP2_EMULATION_PER32
+            e["roofline"]["kernel"] += f" ({EXP2_EMULATION_PER32} of 32 exponentials in software)"
+            e["roofline"]["traffic"] = None  # the traffic record is the default instance's
+            next_rows[f"{n}+exp2_emulation"] = e
 
     if rank != 0:
         if world > 1:

@@ -9,7 +9,7 @@ _EXPORTS = ("FAError", "attention_backward", "attention_decode", "attention_forw
             "fa_bwd_blocksparse", "fa_bwd_noalloc", "fa_bwd_workspace_bytes",
             "fa_check_device_error", "fa_decode", "fa_decode_ctas", "fa_decode_workspace_bytes",
             "fa_fwd", "fa_fwd_blocksparse", "fa_fwd_fp8", "fa_fwd_fp32", "fa_fwd_fp32_fa1",
-            "load")
+            "fa_get_exp2_emulation", "fa_set_exp2_emulation", "load")
 
 __all__ = list(_EXPORTS)
 

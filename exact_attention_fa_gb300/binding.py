@@ -40,6 +40,8 @@ SIGNATURES = [
     ("fa_decode", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P]),
     ("fa_decode_ctas", _I, [_I, _I, _I, _I, _I]),
     ("fa_decode_workspace_bytes", ctypes.c_size_t, [_I, _I, _I, _I, _I]),
+    ("fa_set_exp2_emulation", _I, [_I]),
+    ("fa_get_exp2_emulation", _I, []),
     ("fa_selftest_wait_timeout", _I, [ctypes.c_uint, _P]),
     ("fa_check_device_error", _I, [_P]),
     ("fa_status_string", ctypes.c_char_p, [_I]),
@@ -242,6 +244,16 @@ def fa_decode(q, k, v, o, lse, scale: float, n_ctas: int = 0, workspace=None):
         raise ValueError(f"workspace must be a contiguous CUDA tensor of at least {need} bytes")
     _call("fa_decode", q.device, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
           float(scale), int(n_ctas), _ptr(workspace), _stream(q))
+
+
+def fa_set_exp2_emulation(per32: int):
+    """Exponentials out of every 32 per row that the bf16 forward computes on the FMA pipes
+    (0, the default, or 4); process-wide, for the forward calls enqueued afterwards."""
+    _check("fa_set_exp2_emulation", load().fa_set_exp2_emulation(int(per32)))
+
+
+def fa_get_exp2_emulation() -> int:
+    return int(load().fa_get_exp2_emulation())
 
 
 def fa_selftest_wait_timeout(timeout_us: int = 20000, device=None):

@@ -6,6 +6,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "fa.h"
@@ -30,6 +31,7 @@ struct DeviceState {
 
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
+std::atomic<int> g_exp2_per32{0};  // fa_set_exp2_emulation
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 // Per-device set-up, once, with that device current: check it is an sm_103 part, look up the
@@ -191,6 +193,7 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.o_scale = 1.f;
+  p.exp2_poly = g_exp2_per32.load(std::memory_order_relaxed) != 0 ? 1 : 0;
   p.err = ds->err;
   p.timeout_ns = kWaitTimeoutNs;
   if (static_cast<long long>(p.n_tiles) * BH > 0x7fffffffll) return FA_ERR_TOO_LARGE;
@@ -316,7 +319,7 @@ int fa::check_bwd_args(const void* q, const void* k, const void* v, const void* 
 
 extern "C" {
 
-int fa_abi_version(void) { return (2 << 16) | 5; }
+int fa_abi_version(void) { return (2 << 16) | 6; }
 
 const char* fa_status_string(int status) {
   switch (status) {
@@ -334,6 +337,14 @@ const char* fa_status_string(int status) {
     default: return "unknown status";
   }
 }
+
+int fa_set_exp2_emulation(int per32) {
+  if (per32 != 0 && per32 != fa::kExp2EmulationPer32) return FA_ERR_INVALID_ARG;
+  g_exp2_per32.store(per32, std::memory_order_relaxed);
+  return FA_OK;
+}
+
+int fa_get_exp2_emulation(void) { return g_exp2_per32.load(std::memory_order_relaxed); }
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
            int d, float scale, int causal, fa_stream_t stream) {

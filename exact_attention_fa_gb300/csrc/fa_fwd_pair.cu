@@ -328,9 +328,12 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t sbase, uint32_t tmem, co
 }
 
 // ---------------------------------------------------------------------------------------------
-template <int D, bool F8>
+// POLY: scores out of every 32 of a row whose exponential is computed on the FMA pipes
+// (exp2_poly2) instead of the SFU; 0 in the default instances.
+template <int D, bool F8, int POLY>
 __device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, uint32_t tmem,
                            const Ctl& ctl, int bh, int qt0, int qt1) {
+  static_assert(POLY == 0 || (32 % POLY == 0 && POLY % 2 == 0), "POLY: pairs spread evenly");
   using C = Cfg<D, F8>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -438,7 +441,18 @@ __device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, ui
             f2_pack(__uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1])), k2, nm2);
         float x0, x1;
         f2_unpack(x, x0, x1);
-        const float p0 = ex2(x0), p1 = ex2(x1);
+        float p0, p1;
+        if constexpr (POLY > 0) {
+          if (i % (32 / POLY) == 0) {  // POLY / 2 pairs of every 16, spread out
+            exp2_poly2(x0, x1, p0, p1);
+          } else {
+            p0 = ex2(x0);
+            p1 = ex2(x1);
+          }
+        } else {
+          p0 = ex2(x0);
+          p1 = ex2(x1);
+        }
         rs[i & 3] = f2_add(rs[i & 3], f2_pack(p0, p1));
         if constexpr (F8) {
           // four e4m3 per TMEM column (keys 4u .. 4u + 3 of this chunk in bytes 0 .. 3)
@@ -519,7 +533,7 @@ __device__ void softmax_wg(const FwdParams& p, uint8_t* smem, uint32_t sbase, ui
 }
 
 // ---------------------------------------------------------------------------------------------
-template <int D, bool F8 = false>
+template <int D, bool F8 = false, int POLY = 0>
 __global__ void __launch_bounds__(kThreads, 1) fwd_pair_kernel(const __grid_constant__ FwdParams p) {
   using C = Cfg<D, F8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -572,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_pair_kernel(const __grid_cons
     __syncwarp();
   } else {
     regs_inc<kRegsSoftmax>();
-    softmax_wg<D, F8>(p, smem, sbase, tmem, ctl, bh, qt0, qt1);
+    softmax_wg<D, F8, POLY>(p, smem, sbase, tmem, ctl, bh, qt0, qt1);
   }
 
   tc_fence_before();
@@ -583,16 +597,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_pair_kernel(const __grid_cons
   }
 }
 
-template <int D, bool F8 = false>
+template <int D, bool F8 = false, int POLY = 0>
 cudaError_t configure() {
-  return cudaFuncSetAttribute(fwd_pair_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Cfg<D, F8>::kSmemBytes);
+  return cudaFuncSetAttribute(fwd_pair_kernel<D, F8, POLY>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, F8>::kSmemBytes);
 }
 
-template <int D, bool F8 = false>
+template <int D, bool F8 = false, int POLY = 0>
 cudaError_t launch(const FwdParams& p, cudaStream_t s) {
   const unsigned grid = static_cast<unsigned>((p.n_tiles + 1) / 2) * static_cast<unsigned>(p.BH);
-  fwd_pair_kernel<D, F8><<<grid, kThreads, Cfg<D, F8>::kSmemBytes, s>>>(p);
+  fwd_pair_kernel<D, F8, POLY><<<grid, kThreads, Cfg<D, F8>::kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -601,12 +615,19 @@ cudaError_t launch(const FwdParams& p, cudaStream_t s) {
 cudaError_t configure_fwd_pair() {
   cudaError_t e = configure<64>();
   if (e == cudaSuccess) e = configure<128>();
-  return e != cudaSuccess ? e : configure<128, true>();
+  if (e == cudaSuccess) e = configure<128, true>();
+  if (e == cudaSuccess) e = configure<64, false, kExp2EmulationPer32>();
+  return e != cudaSuccess ? e : configure<128, false, kExp2EmulationPer32>();
 }
 
 cudaError_t launch_fwd_fp8(const FwdParams& p, cudaStream_t s) { return launch<128, true>(p, s); }
 
 cudaError_t launch_fwd_pair(const FwdParams& p, int d, cudaStream_t s) {
+  if (p.exp2_poly) {
+    if (d == 64) return launch<64, false, kExp2EmulationPer32>(p, s);
+    if (d == 128) return launch<128, false, kExp2EmulationPer32>(p, s);
+    return cudaErrorInvalidValue;
+  }
   if (d == 64) return launch<64>(p, s);
   if (d == 128) return launch<128>(p, s);
   return cudaErrorInvalidValue;

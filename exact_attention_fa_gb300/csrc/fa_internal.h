@@ -25,6 +25,7 @@ struct FwdParams {
   int causal;                 // key j > query i masked (combines with a tile mask)
   float scale_log2;           // scale * log2(e)
   float o_scale;              // e4m3 inputs: O is multiplied by this (the scale of V)
+  int exp2_poly;              // bf16: 1 = kExp2EmulationPer32 of every 32 exponentials on the FMA pipes
   unsigned* err;
   unsigned long long timeout_ns;
 };
@@ -102,6 +103,10 @@ int check_bwd_args(const void* q, const void* k, const void* v, const void* o, c
                    const float* lse, const float* dq, const void* dk, const void* dv, int B, int H,
                    int N, int d, float scale, bool sparse, const uint8_t* block_mask,
                    const void* workspace, bool needs_workspace);
+
+// Exponentials out of every 32 per row that the bf16 forward computes with a polynomial on the
+// FMA pipes when that mode is on (fa_set_exp2_emulation).
+constexpr int kExp2EmulationPer32 = 4;
 
 // Launchers; return a cudaError_t (cudaSuccess on success).
 cudaError_t launch_fwd_pair(const FwdParams& p, int d, cudaStream_t s);               // 2 tiles/CTA

@@ -586,6 +586,35 @@ __device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsig
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+// 2^x for two values on the FMA pipes instead of the SFU (the FA4 idea of "3 · FlashAttention",
+// 3.5: a share of the exponentials computed in software). x = j + f with j = rint(x), f in
+// [-1/2, 1/2]: adding 1.5 * 2^23 leaves j in the low mantissa bits; 2^f comes from a degree-3
+// polynomial fitted to 2^f in relative error on [-1/2, 1/2] by the Remez exchange algorithm
+// (coefficients from exact_attention_fa_gb300/exp2_poly_fit.py, max relative error 7.5e-5 in fp32,
+// far below the bf16 rounding of P); j is then added into the exponent field. x below -126
+// (masked keys, -inf) gives exactly 0, as the SFU's flush-to-zero ex2 does.
+constexpr float kExp2C0 = 0.9999280571937561f;
+constexpr float kExp2C1 = 0.6932609677314758f;
+constexpr float kExp2C2 = 0.2426111251115799f;
+constexpr float kExp2C3 = 0.0551716685295105f;
+__device__ __forceinline__ void exp2_poly2(float x0, float x1, float& p0, float& p1) {
+  constexpr float kRound = 12582912.f;  // 1.5 * 2^23
+  const unsigned long long x = f2_pack(fmaxf(x0, -127.f), fmaxf(x1, -127.f));
+  const unsigned long long t = f2_add(x, f2_pack(kRound, kRound));
+  const unsigned long long jf = f2_add(t, f2_pack(-kRound, -kRound));  // rint(x) as a float
+  const unsigned long long f = f2_fma(jf, f2_pack(-1.f, -1.f), x);      // x - rint(x)
+  unsigned long long q = f2_fma(f2_pack(kExp2C3, kExp2C3), f, f2_pack(kExp2C2, kExp2C2));
+  q = f2_fma(q, f, f2_pack(kExp2C1, kExp2C1));
+  q = f2_fma(q, f, f2_pack(kExp2C0, kExp2C0));
+  float t0, t1, q0, q1;
+  f2_unpack(t, t0, t1);
+  f2_unpack(q, q0, q1);
+  const int j0 = static_cast<int>(__float_as_uint(t0)) - static_cast<int>(__float_as_uint(kRound));
+  const int j1 = static_cast<int>(__float_as_uint(t1)) - static_cast<int>(__float_as_uint(kRound));
+  p0 = x0 < -126.f ? 0.f : __int_as_float(__float_as_int(q0) + (j0 << 23));
+  p1 = x1 < -126.f ? 0.f : __int_as_float(__float_as_int(q1) + (j1 << 23));
+}
+
 // Four fp32 values rounded to e4m3 (nearest, ties to even, saturating at +-448), packed with the
 // first in the lowest byte. cvt's first source goes to the upper byte of each pair.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float p0, float p1, float p2, float p3) {

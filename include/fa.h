@@ -101,6 +101,20 @@ int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, flo
 int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                int N, int d, float scale, float v_scale, int causal, fa_stream_t stream);
 
+/* The partial software exponential of FlashAttention-4 ("3 · FlashAttention" (mkdocs.reaper.mx),
+ * 3.5: some of the softmax's exponentials computed on the FMA units instead of the special
+ * function unit). per32 = 4: the bf16 forward (fa_fwd, fa_fwd_blocksparse) computes 4 of every 32
+ * exponentials of a row with a degree-3 polynomial (relative error below 7.5e-5, under the bf16
+ * rounding of P) on the FMA pipes; per32 = 0 (the default): all on the SFU. The results agree
+ * within the bf16 tolerances either way. It is off by default because on GB300 it measures slower
+ * (the softmax is limited by its dependency chain and instruction issue, not by the SFU). The
+ * setting is process-wide and applies to forward calls enqueued after it; it does not affect
+ * fa_fwd_fp8, fa_fwd_fp32 or fa_decode. Returns FA_ERR_INVALID_ARG for other values. */
+int fa_set_exp2_emulation(int per32);
+
+/* The current per32 setting of fa_set_exp2_emulation (0 or 4). */
+int fa_get_exp2_emulation(void);
+
 /* Bytes of device workspace fa_bwd needs, per row of B*H*ceil(N/128)*128 rows (rows padded to
  * whole 128-row tiles): two fp32 row statistics (8 bytes) and, at d = 64, two 32-byte bf16
  * operand rows made from them (72 bytes in all). 0 for B, H, N < 1 or d not in {64, 128}. */
@@ -195,7 +209,8 @@ const char* fa_status_string(int status);
 
 /* ABI version: (major << 16) | minor. Major 2: fa_fwd_blocksparse takes a causal flag; minor 1:
  * fa_decode; minor 2: fa_bwd_blocksparse; minor 3: fa_fwd_fp32_fa1; minor 4:
- * fa_bwd_workspace_bytes depends on d (8 bytes per row at d = 128); minor 5: fa_fwd_fp8. */
+ * fa_bwd_workspace_bytes depends on d (8 bytes per row at d = 128); minor 5: fa_fwd_fp8;
+ * minor 6: fa_set_exp2_emulation, fa_get_exp2_emulation. */
 int fa_abi_version(void);
 
 #ifdef __cplusplus

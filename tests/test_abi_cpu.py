@@ -195,3 +195,10 @@ def test_fp8_validation(lib):
     assert lib.fa_fwd_fp8(*base, 128, -1.0, 1.0, 0, None) == 1
     assert lib.fa_fwd_fp8(P(0), *base[1:], 128, 0.088, 1.0, 0, None) == 1
     assert lib.fa_fwd_fp8(fake(0x10001), *base[1:], 128, 0.088, 1.0, 0, None) == 3
+
+
+def test_exp2_emulation_setting(lib):
+    assert lib.fa_get_exp2_emulation() == 0  # the default: every exponential on the SFU
+    assert lib.fa_set_exp2_emulation(3) == 1 and lib.fa_set_exp2_emulation(-4) == 1
+    assert lib.fa_set_exp2_emulation(4) == 0 and lib.fa_get_exp2_emulation() == 4
+    assert lib.fa_set_exp2_emulation(0) == 0 and lib.fa_get_exp2_emulation() == 0
