@@ -169,6 +169,12 @@ WORKLOADS = {
 WORKLOADS["causal_N8192_d128_fp8"] = Workload("causal_N8192_d128_fp8", 8, 32, 8192, 128,
                                               dtype="e4m3", causal=True, seed=12)
 
+# Decoding with 8 new query rows per head (the tensor-core decoding path), same cache sizes.
+WORKLOADS["decode_N32768_d128_q8"] = Workload("decode_N32768_d128_q8", 8, 32, 32768, 128, nq=8,
+                                              seed=15)
+WORKLOADS["decode_N32768_d64_q8"] = Workload("decode_N32768_d64_q8", 8, 32, 32768, 64, nq=8,
+                                             seed=16)
+
 # Counter-capture cases of the e4m3 forward and of the backward on 8 heads (small device footprint).
 WORKLOADS["causal_N4096_d128_fp8_h8"] = Workload("causal_N4096_d128_fp8_h8", 1, 8, 4096, 128,
                                                  dtype="e4m3", causal=True, seed=13)

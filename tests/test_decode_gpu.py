@@ -44,17 +44,21 @@ def run_decode(w, device, n_ctas=0, heads=None):
     (1, 129, 128, 18),   # one block per CTA
     (5, 300, 128, 1024), # more CTAs asked for than there are blocks (capped)
     (4, 2048, 64, 0),
+    # one query row at d = 64 runs on the CUDA cores, everything else on the tensor cores
+    (1, 4097, 64, 0),
+    (1, 1000, 64, 7),
+    (1, 129, 64, 1024),
 ])
 def test_decode_small(cuda, nq, nk, d, ctas):
     w = wl.Workload("decode_small", 2, 3, nk, d, nq=nq, seed=40 + nq)
     run_decode(w, cuda, ctas)
 
 
-@pytest.mark.parametrize("d", [64, 128])
-def test_decode_long_ranges(cuda, d):
-    """Eight CTAs, each streaming about 500 blocks through its warps' rings and across a head
-    boundary (ragged last block per head)."""
-    w = wl.Workload("decode_long", 2, 4, 16384 + 7, d, nq=2, seed=50 + d)
+@pytest.mark.parametrize("d,nq", [(64, 2), (128, 2), (64, 1), (128, 1)])
+def test_decode_long_ranges(cuda, d, nq):
+    """Eight CTAs, each streaming hundreds of blocks through its ring and across a head boundary
+    (ragged last block per head), on either kernel."""
+    w = wl.Workload("decode_long", 2, 4, 16384 + 7, d, nq=nq, seed=50 + d + nq)
     run_decode(w, cuda, 8)
 
 
@@ -87,3 +91,25 @@ def test_decode_N32768_launch_configuration(cuda):
     assert n >= 1
     w = full.with_(B=1, H=4)
     run_decode(w, cuda, n)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_eight_rows_long_cache_every_head(cuda, d):
+    """Eight query rows against 32768 keys on 32 heads (the tensor-core decoding path at the bench's
+    cache length, 152 CTAs cutting heads mid-way), every head against the oracle."""
+    w = wl.Workload("decode_q8_long", 2, 16, 32768, d, nq=8, seed=56 + d)
+    run_decode(w, cuda)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_one_and_eight_rows_agree(cuda, d):
+    """The one-row results equal the first row of an eight-row call on the same cache (within the
+    bf16 tolerance; at d = 64 the two come from different kernels)."""
+    w8 = wl.Workload("decode_rows8", 1, 4, 5000, d, nq=8, seed=57)
+    inp = wl.make_inputs(w8)
+    q, k, v = (H.to_device(inp, n, cuda) for n in ("q", "k", "v"))
+    o8, l8 = fa.attention_decode(q, k, v, w8.softmax_scale)
+    o1, l1 = fa.attention_decode(q[:, :, :1].contiguous(), k, v, w8.softmax_scale)
+    torch.cuda.synchronize()
+    assert (o1.float() - o8[:, :, :1].float()).abs().max().item() <= H.BF16_O_MAX_ABS
+    assert (l1 - l8[:, :, :1]).abs().max().item() <= H.LSE_MAX_ABS
