@@ -628,12 +628,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
         mbar_arrive(bar(C::kBarX + b));
         if (!(ok = mbar_wait(bar(C::kBarX + b), (i >> 1) & 1, ctl))) break;
         const float mx = fmaxf(mh, xm[(b * 2 + (hf ^ 1)) * 32 + r]);
-        // P V of the previous block has to be done before P is rewritten and before O is rescaled
+        const float m_new = fmaxf(m, mx);  // finite: a block holds at least one key
+        // the exponentials first, into registers: they overlap the previous block's P V, which
+        // has to be done only before P is rewritten and O rescaled
+        const unsigned long long k2 = f2_pack(sl2, sl2);
+        const unsigned long long nm2 = f2_pack(-m_new, -m_new);
+        unsigned long long rs[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) rs[u] = f2_pack(0.f, 0.f);
+        uint32_t pk[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const unsigned long long x = f2_fma(
+              f2_pack(__uint_as_float(sc[2 * u]), __uint_as_float(sc[2 * u + 1])), k2, nm2);
+          float x0, x1;
+          f2_unpack(x, x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          rs[u & 3] = f2_add(rs[u & 3], f2_pack(p0, p1));
+          pk[u] = pack_bf16(p0, p1);
+        }
         if (i > 0) {
           if (!(ok = mbar_wait(bar(C::kBarPVDone), (i - 1) & 1, ctl))) break;
           tc_fence_after();
         }
-        const float m_new = fmaxf(m, mx);  // finite: a block holds at least one key
         if (i > i0 && __any_sync(~0u, m_new > m)) {  // the same decision in both warps
           const float alpha = ex2(m - m_new);
 #pragma unroll 1
@@ -647,26 +664,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
           l *= alpha;
         }
         m = m_new;
-        const unsigned long long k2 = f2_pack(sl2, sl2);
-        const unsigned long long nm2 = f2_pack(-m, -m);
-        unsigned long long rs[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) rs[u] = f2_pack(0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < 64; k += 32) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const unsigned long long x = f2_fma(
-                f2_pack(__uint_as_float(sc[k + 2 * u]), __uint_as_float(sc[k + 2 * u + 1])), k2, nm2);
-            float x0, x1;
-            f2_unpack(x, x0, x1);
-            const float p0 = ex2(x0), p1 = ex2(x1);
-            rs[u & 3] = f2_add(rs[u & 3], f2_pack(p0, p1));
-            pk[u] = pack_bf16(p0, p1);
-          }
-          tmem_st16(trow + C::kColP + 32u * hf + k / 2, pk);
-        }
+        tmem_st16(trow + C::kColP + 32u * hf, pk);
+        tmem_st16(trow + C::kColP + 32u * hf + 16, pk + 16);
         float rs0, rs1;
         f2_unpack(f2_add(f2_add(rs[0], rs[1]), f2_add(rs[2], rs[3])), rs0, rs1);
         l += rs0 + rs1;
