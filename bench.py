@@ -789,10 +789,7 @@ def run_decode(args, w, fa, inp, cpu, world, rank, local, dev, flush_buf):
     peaks, peak_src = load_peaks()
     peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     achieved = algo_bytes / (t_step * 1e-3) / 1e9
-    # the library decodes on the tensor cores at d = 128 and with several query rows, on the CUDA
-    # cores for one row at d = 64
-    split = "decode_tc_kernel" if (w.d == 128 or w.nq > 1) else "decode_stream_kernel"
-    kname = f"{split}<{w.d}> (+ decode_merge_kernel<{w.d}>)"
+    kname = f"decode_tc_kernel<{w.d}> (+ decode_merge_kernel<{w.d}>)"
     line = {
         "metric": metric_name(w), "value": world * achieved, "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True,

@@ -25,7 +25,6 @@ struct DeviceState {
   bool ready = false;
   int status = FA_OK;
   int num_sms = 0;
-  int decode_resident = 1;          // CUDA-core decoding CTAs per SM (d = 64, one query row)
   unsigned* err = nullptr;          // device address of g_error_word on this device
 };
 
@@ -65,8 +64,6 @@ int device_state(DeviceState** out) {
           fa::configure_decode() != cudaSuccess) {
         cudaGetLastError();
         st.status = FA_ERR_CUDA;
-      } else {
-        st.decode_resident = fa::decode_ctas_per_sm();
       }
     }
     if (st.status == FA_OK && g_encode == nullptr) {
@@ -240,18 +237,12 @@ int fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, in
   return to_status(fa::launch_fwd_fp8(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-// Which decoding kernel runs: the tensor-core one for d = 128 and for several query rows (measured
-// at B8 H32, 32768 keys: d = 128, one row 7094 GB/s against 6091 on the CUDA cores; eight rows
-// 7072 against 1132), the CUDA-core one for one query row at d = 64 (6177 against 5461).
-bool decode_on_tensor_cores(int Nq, int d) { return d == 128 || Nq > 1; }
-
-// CTAs for decoding: as many as the SMs hold at once, never more than there are key blocks
-// (the tensor-core kernel: 128-key blocks, one CTA per SM).
-int decode_auto_ctas(int BH, int Nq, int Nk, int d, const DeviceState& ds) {
-  const bool tc = decode_on_tensor_cores(Nq, d);
-  const int kB = tc ? fa::kDecodeTcBlockKeys : fa::kDecodeMinBlockKeys;
+// CTAs for decoding: one per SM (the kernel holds 192 KB of keys and values in flight), never
+// more than there are key blocks.
+int decode_auto_ctas(int BH, int Nk, int d, const DeviceState& ds) {
+  const int kB = fa::decode_tc_block_keys(d);
   const long long blocks = static_cast<long long>(BH) * ((Nk + kB - 1) / kB);
-  long long n = static_cast<long long>(ds.num_sms) * (tc ? 1 : ds.decode_resident);
+  long long n = ds.num_sms;
   if (n > fa::kDecodeMaxCtas) n = fa::kDecodeMaxCtas;
   return static_cast<int>(n < blocks ? n : blocks);
 }
@@ -325,7 +316,7 @@ int fa::check_bwd_args(const void* q, const void* k, const void* v, const void* 
 
 extern "C" {
 
-int fa_abi_version(void) { return (2 << 16) | 6; }
+int fa_abi_version(void) { return (2 << 16) | 7; }
 
 const char* fa_status_string(int status) {
   switch (status) {
@@ -422,13 +413,14 @@ int fa_decode_ctas(int B, int H, int Nq, int Nk, int d) {
   if (check_decode(B, H, Nq, Nk, d, 1.f) != FA_OK) return 0;
   DeviceState* ds = nullptr;
   if (device_state(&ds) != FA_OK) return 0;
-  return decode_auto_ctas(B * H, Nq, Nk, d, *ds);
+  return decode_auto_ctas(B * H, Nk, d, *ds);
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
   if (check_decode(B, H, Nq, Nk, d, 1.f) != FA_OK) return 0;
   const long long BH = static_cast<long long>(B) * H;
-  long long ctas = BH * ((Nk + fa::kDecodeMinBlockKeys - 1) / fa::kDecodeMinBlockKeys);
+  const int kB = fa::decode_tc_block_keys(d);
+  long long ctas = BH * ((Nk + kB - 1) / kB);
   if (ctas > fa::kDecodeMaxCtas) ctas = fa::kDecodeMaxCtas;
   return static_cast<size_t>((ctas + BH) * Nq * (d + 1)) * sizeof(float);
 }
@@ -446,7 +438,7 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != FA_OK) return st;
   const int BH = B * H;
-  if (n_ctas == 0) n_ctas = decode_auto_ctas(BH, Nq, Nk, d, *ds);
+  if (n_ctas == 0) n_ctas = decode_auto_ctas(BH, Nk, d, *ds);
   fa::DecodeParams p{};  // the launcher sets the block count and caps n_ctas at it
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);
@@ -461,16 +453,11 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.scale_log2 = scale * 1.4426950408889634f;
   p.err = ds->err;
   p.timeout_ns = kWaitTimeoutNs;
-  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (decode_on_tensor_cores(Nq, d)) {
-    // the products on the tensor cores (rows past Nq of the 128-row Q tile and keys past Nk
-    // read as zero through the tensor maps)
-    if (!encode_bf16_map(&p.tm_q, q, BH, Nq, d) || !encode_bf16_map(&p.tm_k, k, BH, Nk, d) ||
-        !encode_bf16_map(&p.tm_v, v, BH, Nk, d))
-      return FA_ERR_CUDA;
-    return to_status(fa::launch_decode_tc(p, d, cs));
-  }
-  return to_status(fa::launch_decode(p, d, cs));
+  // rows past Nq of the 128-row Q tile and keys past Nk read as zero through the tensor maps
+  if (!encode_bf16_map(&p.tm_q, q, BH, Nq, d) || !encode_bf16_map(&p.tm_k, k, BH, Nk, d) ||
+      !encode_bf16_map(&p.tm_v, v, BH, Nk, d))
+    return FA_ERR_CUDA;
+  return to_status(fa::launch_decode(p, d, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int fa_selftest_wait_timeout(unsigned timeout_us, fa_stream_t stream) {

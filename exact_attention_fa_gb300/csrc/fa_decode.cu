@@ -1,29 +1,19 @@
 // Decoding attention: a few query rows against a long key/value sequence ("3 · FlashAttention",
 // 3.6 "L'attention en décodage" and the Flash-Decoding row of 3.7).
 //
-// With Nq <= 8 query rows per head the work is a matrix-vector product: every key and value row
-// is used Nq times, so decoding is bound by HBM bandwidth. Two kernels, chosen by measurement
-// (fa_api.cu): decode_tc_kernel (further below: the products on the tensor cores, 128-key blocks)
-// for d = 128 and for several query rows, and decode_stream_kernel (the CUDA cores) for one query
-// row at d = 64, where it keeps up with HBM and the tensor-core kernel's per-block costs do not.
-// decode_stream_kernel, GB300 mapping (its template covers more shapes than the one it runs for):
-//   * Flash-Decoding's split of the keys, balanced for a fixed grid: the key blocks (32 keys at
-//     d = 128, 64 at d = 64: 16 KB of K and V either way) of all heads, head after head, are
-//     dealt out as G equal contiguous ranges, one per CTA, with G = the CTAs the SMs hold at
-//     once (persistent: no tail wave, every SM streams until the end). A range may start or end
-//     inside a head and may span several heads;
-//   * one warp of the CTA streams its range with 1-D bulk copies (cp.async.bulk) into per-warp
-//     shared-memory rings of (K block, V block) pairs (128 KB in flight per CTA), across head
-//     boundaries, guarded by full / empty mbarriers;
-//   * eight compute warps take the blocks in turn, each with an online softmax state of its own
-//     ("3 · FlashAttention", 3.3): lane = key (two keys at d = 64) for the scores q.k (16-byte
-//     loads rotated by lane, so no bank conflicts), warp shuffles for the block's max and sum,
-//     lane = 4 output columns for O += P V (at d = 64 the two half-warps take alternate keys).
-//     No CTA-wide barrier per block: the warps meet only where a head ends inside the range, to
-//     merge their states into that (CTA, head) piece;
-//   * each piece holds O_c / l_c and its log-sum-exp lse_c; a second kernel merges the pieces of
-//     each head with the same statistics merge as the blockwise forward (lse = log Σ exp lse_c,
-//     O = Σ exp(lse_c - lse) O_c).
+// With Nq <= 8 query rows per head every key and value row is used Nq times: the work is a
+// matrix-vector product bound by HBM bandwidth. Flash-Decoding's split of the keys, balanced for a
+// fixed grid: the key blocks of all heads, head after head, are dealt out as G equal contiguous
+// ranges, one per CTA, with G = the SM count (persistent: no tail wave, every SM streams until the
+// end). A range may start or end inside a head and may span several heads. Each CTA turns each
+// head's stretch of its range into a piece (O_c / l_c and its log-sum-exp lse_c); a second kernel
+// merges the pieces of each head with the same statistics merge as the blockwise forward
+// (lse = log sum_c exp lse_c, O = sum_c exp(lse_c - lse) O_c).
+//
+// The products run on the tensor cores (decode_tc_kernel below). A CUDA-core kernel (lane = key
+// for the scores, lane = output columns for P V) did 2 Nq d FMAs per key against 4 d bytes of K
+// and V: it reached 6091 GB/s (d = 128) and 6177 (d = 64) with one query row but only 1132 with
+// eight; the tensor-core kernel streams 6977 / 6556 GB/s with one row and 7061 / 6508 with eight.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -33,280 +23,12 @@
 namespace fa {
 namespace {
 
-constexpr int kWarps = 8;              // compute warps; warp kWarps streams the blocks in
-constexpr int kThreads = 32 * (kWarps + 1);
 constexpr float kLn2 = 0.6931471805599453f;
-
-template <int D>
-struct DCfg {
-  // Each compute warp has a ring of its own (one consumer per stage, so the phase parity of a
-  // stage's barrier always refers to the block the warp expects): one 16 KB stage per warp,
-  // 128 KB in flight per CTA.
-  static constexpr int kStagesPerWarp = 1;
-  static constexpr int kStages = kWarps * kStagesPerWarp;
-  // keys per block: 16 KB per (K, V) block pair either way, so one key per lane at d = 128 and two
-  // at d = 64 (lanes l and l + 32)
-  static constexpr int kBK = D == 128 ? 32 : 64;
-  static constexpr int kKeysPerLane = kBK / 32;
-  static constexpr int kBlockBytes = kBK * D * 2;  // one K or V block, bf16
-  static constexpr int kStageBytes = 2 * kBlockBytes;
-  static constexpr int kOffQ = kStages * kStageBytes;                // fp32 [kDecodeMaxNq][D]
-  static constexpr int kOffO = kOffQ + kDecodeMaxNq * D * 4;         // fp32 [kWarps][Nq][D]
-  static constexpr int kOffML = kOffO + kWarps * kDecodeMaxNq * D * 4;  // fp32 [kWarps][Nq][2]
-  static constexpr int kOffBar = kOffML + kWarps * kDecodeMaxNq * 8;
-  static constexpr int kOffAbort = kOffBar + 16 * kStages;         // full[S], empty[S]
-  static constexpr int kSmemBytes = kOffAbort + 16;
-  static constexpr int kLanesPerRow = D / 4;   // lanes covering one V row, 4 columns each
-  static constexpr int kKeySplit = 32 / kLanesPerRow;  // keys a warp takes at once in O += P V
-};
-
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
 
 // CTA of global key block g (blocks of all heads in a row, head-major): blocks are dealt out as
 // G contiguous ranges [c*T/G, (c+1)*T/G).
 __device__ __forceinline__ int cta_of_block(long long g, long long T, int G) {
   return static_cast<int>(((g + 1) * G - 1) / T);
-}
-
-// CTA c streams its range of key blocks. Warp kWarps copies them in order into the rings;
-// compute warp w takes the CTA-local blocks i = w (mod kWarps) (lane = key) with an online
-// softmax state of its own per head, and at the end of each head's stretch of the range the
-// warps' states are merged into the piece (c, head h) at slot c + h: O_piece / l_piece and
-// lse_piece (log2 units). Along the ranges (c, h) only ever steps forward, so c + h is unique.
-template <int D, int NQ>
-__global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const __grid_constant__ DecodeParams p) {
-  using C = DCfg<D>;
-  constexpr int S = C::kStages;
-  constexpr int R = C::kStagesPerWarp;
-  // CTA-local block i belongs to compute warp i % kWarps, as that warp's k-th block
-  // (k = i / kWarps): stage (i % kWarps) * R + k % R, phase k / R of that stage.
-  auto stage_of = [&](int i) { return (i % kWarps) * R + (i / kWarps) % R; };
-  auto parity_of = [&](int i) { return static_cast<uint32_t>((i / kWarps / R) & 1); };
-  constexpr int kKS = C::kKeySplit;
-  constexpr int kBK = C::kBK;
-  constexpr int kKPL = C::kKeysPerLane;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const uint32_t sbase = smem_u32(smem);
-  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int Nq = p.Nq;
-  const int nb = p.blocks_per_head;
-  const long long T = static_cast<long long>(p.BH) * nb;
-  const int G = gridDim.x, c = blockIdx.x;
-  const long long g0 = c * T / G;
-  const int nblk = static_cast<int>((c + 1) * T / G - g0);
-  float* qs = reinterpret_cast<float*>(smem + C::kOffQ);
-  float* wo = reinterpret_cast<float*>(smem + C::kOffO);
-  float* wml = reinterpret_cast<float*>(smem + C::kOffML);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
-  const Ctl ctl{abort_flag, p.err, p.timeout_ns};
-  auto full = [&](int s) { return sbase + C::kOffBar + 8u * s; };
-  auto empty = [&](int s) { return sbase + C::kOffBar + 8u * (S + s); };
-  auto keys_in = [&](long long g) {
-    const int jb = static_cast<int>(g % nb);
-    return min(kBK, p.Nk - jb * kBK);
-  };
-
-  if (tid == 0) {
-    *abort_flag = 0;
-    for (int s = 0; s < S; ++s) {
-      mbar_init(full(s), 1);
-      mbar_init(empty(s), 1);
-    }
-    fence_barrier_init();
-  }
-  __syncthreads();
-
-  if (warp == kWarps) {
-    // ---------------------------------------------------------------- producer (whole warp)
-    int i = 0;
-    bool ok = true;
-    for (; i < nblk; ++i) {
-      const int s = stage_of(i);
-      if (!mbar_wait_warp(empty(s), parity_of(i) ^ 1u, ctl)) { ok = false; break; }
-      const long long g = g0 + i;
-      const int h = static_cast<int>(g / nb), jb = static_cast<int>(g % nb);
-      const uint32_t bytes = static_cast<uint32_t>(keys_in(g)) * D * 2;
-      const size_t off = (static_cast<size_t>(h) * p.Nk + static_cast<size_t>(jb) * kBK) * D;
-      mbar_arrive_expect_tx(full(s), 2 * bytes);
-      tma_bulk_g2s(sbase + s * C::kStageBytes, p.k + off, bytes, full(s));
-      tma_bulk_g2s(sbase + s * C::kStageBytes + C::kBlockBytes, p.v + off, bytes, full(s));
-    }
-    if (!ok) {
-      // Give the copies in flight a bounded time to land before the CTA exits.
-      Ctl drain = ctl;
-      int zero = 0;
-      drain.abort_flag = &zero;
-      for (int b = max(0, i - S); b < i; ++b) mbar_wait_warp(full(stage_of(b)), parity_of(b), drain);
-    }
-    return;
-  }
-
-  // ------------------------------------------------------------------ compute warps
-  constexpr int kChunks = D / 8;  // 16-byte chunks per key row
-  const int sub = lane / C::kLanesPerRow, col4 = (lane % C::kLanesPerRow) * 4;
-  bool ok = true;
-  long long g = g0;
-  const long long g_end = g0 + nblk;
-  while (g < g_end) {
-    const int h = static_cast<int>(g / nb);
-    const long long seg_end = min(g_end, static_cast<long long>(h + 1) * nb);
-    // q of head h, pre-multiplied by scale * log2(e) so that scores come out in log2 units
-    const __nv_bfloat16* qg = p.q + static_cast<size_t>(h) * Nq * D;
-    for (int e = tid; e < Nq * D; e += 32 * kWarps) qs[e] = __bfloat162float(qg[e]) * p.scale_log2;
-    bar_sync(1, 32 * kWarps);
-
-    float m[NQ], l[NQ], acc[NQ][4];
-#pragma unroll
-    for (int j = 0; j < NQ; ++j) {
-      m[j] = -INFINITY;
-      l[j] = 0.f;
-#pragma unroll
-      for (int t = 0; t < 4; ++t) acc[j][t] = 0.f;
-    }
-    // this warp's blocks of the stretch: CTA-local indices congruent to warp mod kWarps
-    const int first = static_cast<int>(g - g0);
-    for (int i = first + (warp - first % kWarps + kWarps) % kWarps; ok && g0 + i < seg_end;
-         i += kWarps) {
-      const long long gb = g0 + i;
-      const int s = stage_of(i);
-      if (!mbar_wait_warp(full(s), parity_of(i), ctl)) { ok = false; break; }
-      const int n = keys_in(gb);
-      const __nv_bfloat16* Ks = reinterpret_cast<const __nv_bfloat16*>(smem + s * C::kStageBytes);
-      const __nv_bfloat16* Vs = Ks + kBK * D;
-
-      // scores of keys lane + 32 u (16-byte chunks in an order rotated by lane: no bank
-      // conflicts), two partial sums per key and query row for short dependency chains
-      float sc[NQ][kKPL][2];
-#pragma unroll
-      for (int j = 0; j < NQ; ++j)
-#pragma unroll
-        for (int u = 0; u < kKPL; ++u) sc[j][u][0] = sc[j][u][1] = 0.f;
-#pragma unroll
-      for (int u = 0; u < kKPL; ++u) {
-        const int key = lane + 32 * u;
-        if (key < n) {
-#pragma unroll
-          for (int cc = 0; cc < kChunks; ++cc) {
-            const int ch = (cc + lane) % kChunks;
-            float kf[8];
-            bf16x8_to_f32(*reinterpret_cast<const uint4*>(Ks + key * D + ch * 8), kf);
-#pragma unroll
-            for (int j = 0; j < NQ; ++j) {
-              if (j < Nq) {
-                const float4 qa = *reinterpret_cast<const float4*>(qs + j * D + ch * 8);
-                const float4 qb = *reinterpret_cast<const float4*>(qs + j * D + ch * 8 + 4);
-                float a = sc[j][u][cc % 2];
-                a = fmaf(qa.x, kf[0], a); a = fmaf(qa.y, kf[1], a);
-                a = fmaf(qa.z, kf[2], a); a = fmaf(qa.w, kf[3], a);
-                a = fmaf(qb.x, kf[4], a); a = fmaf(qb.y, kf[5], a);
-                a = fmaf(qb.z, kf[6], a); a = fmaf(qb.w, kf[7], a);
-                sc[j][u][cc % 2] = a;
-              }
-            }
-          }
-        }
-      }
-      // online softmax per query row (the block's scores sit kKPL per lane)
-      float pj[NQ][kKPL];
-#pragma unroll
-      for (int j = 0; j < NQ; ++j) {
-        if (j < Nq) {
-          float sj[kKPL];
-          float mx = -INFINITY;
-#pragma unroll
-          for (int u = 0; u < kKPL; ++u) {
-            sj[u] = lane + 32 * u < n ? sc[j][u][0] + sc[j][u][1] : -INFINITY;
-            mx = fmaxf(mx, sj[u]);
-          }
-#pragma unroll
-          for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, o));
-          const float m_new = fmaxf(m[j], mx);  // finite: the block has at least one key
-          float ps = 0.f;
-#pragma unroll
-          for (int u = 0; u < kKPL; ++u) {
-            pj[j][u] = ex2(sj[u] - m_new);
-            ps += pj[j][u];
-          }
-#pragma unroll
-          for (int o = 16; o; o >>= 1) ps += __shfl_xor_sync(~0u, ps, o);
-          const float alpha = ex2(m[j] - m_new);  // 0 while nothing was accumulated
-          l[j] = l[j] * alpha + ps;
-          m[j] = m_new;
-#pragma unroll
-          for (int t = 0; t < 4; ++t) acc[j][t] *= alpha;
-        }
-      }
-      // O += P V: lane owns 4 columns of a V row; at d = 64 the two half-warps take alternate
-      // keys (kKS = 2) and are summed at the end. Keys past n contribute p = 0 and v = 0.
-      for (int k0 = 0; k0 < n; k0 += 8 * kKS) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int key = k0 + u * kKS + sub;
-          uint2 w = make_uint2(0u, 0u);
-          if (key < n) w = *reinterpret_cast<const uint2*>(Vs + key * D + col4);
-          const float vf[4] = {__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
-                               __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u)};
-#pragma unroll
-          for (int j = 0; j < NQ; ++j) {
-            if (j < Nq) {
-              // key's P sits in lane key % 32, slot key / 32 (the same slot for both
-              // half-warps: k0 + u * kKS is even)
-              const float pk = __shfl_sync(~0u, pj[j][(k0 + u * kKS) >> 5], key & 31);
-#pragma unroll
-              for (int t = 0; t < 4; ++t) acc[j][t] = fmaf(pk, vf[t], acc[j][t]);
-            }
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty(s));
-    }
-
-    // merge the warps' states into the piece (c, h)
-#pragma unroll
-    for (int j = 0; j < NQ; ++j) {
-      if (j < Nq) {
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          float a = acc[j][t];
-          if constexpr (kKS == 2) a += __shfl_xor_sync(~0u, a, 16);
-          if (sub == 0) wo[(warp * kDecodeMaxNq + j) * D + col4 + t] = a;
-        }
-        if (lane == 0) {
-          wml[(warp * kDecodeMaxNq + j) * 2] = m[j];
-          wml[(warp * kDecodeMaxNq + j) * 2 + 1] = l[j];
-        }
-      }
-    }
-    if (bar_red_or(1, 32 * kWarps, !ok)) return;
-    const size_t slot = static_cast<size_t>(c) + h;
-    for (int e = tid; e < Nq * D; e += 32 * kWarps) {
-      const int j = e / D, col = e % D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wml[(w * kDecodeMaxNq + j) * 2]);
-      float L = 0.f, a = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const float f = ex2(wml[(w * kDecodeMaxNq + j) * 2] - M);  // 0 for an idle warp
-          L = fmaf(f, wml[(w * kDecodeMaxNq + j) * 2 + 1], L);
-          a = fmaf(f, wo[(w * kDecodeMaxNq + j) * D + col], a);
-        }
-      }
-      p.ws_o[(slot * Nq + j) * D + col] = L > 0.f ? a / L : 0.f;
-      if (col == 0) p.ws_lse[slot * Nq + j] = L > 0.f ? M + __log2f(L) : -INFINITY;
-    }
-    bar_sync(1, 32 * kWarps);  // wo, wml and qs are free again
-    g = seg_end;
-  }
 }
 
 // One CTA of D threads per (head, query row): merges the pieces of the CTAs whose block ranges
@@ -363,33 +85,40 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(const __grid_constant__
 }
 
 // ---------------------------------------------------------------------------------------------
-// Decoding with several query rows (2 <= Nq <= kDecodeMaxNq) on the tensor cores. With Nq rows the
-// CUDA-core kernel above does 2 Nq d FMAs per key against 4 d bytes of K and V, which at Nq = 8
-// runs out of FMA throughput long before HBM runs out of bytes. Here each 128-key block is a small
-// forward tile: S = Q K^T and O += P V as tcgen05.mma with Q zero-padded to a 128-row tile by the
-// TMA (rows past Nq read as zero), so the tensor core does 128 / Nq times the useful work but
-// still needs far less time per block than HBM needs to deliver the block's K and V.
-//   * the key blocks of all heads are dealt out as in the kernel above (equal contiguous ranges,
-//     one per CTA, head-major), the stretch of one head inside a range being a segment;
+// The decoding kernel. Each key block is a small forward tile: S = Q K^T and O += P V as
+// tcgen05.mma with Q zero-padded to a 128-row tile by the TMA (rows past Nq read as zero), so the
+// tensor core does 128 / Nq times the useful work but still needs far less time per block than
+// HBM needs to deliver the block's K and V.
+//   * the stretch of one head inside a CTA's range is a segment;
 //   * warp 1 loads Q of each segment and the (K, V) blocks with TMA into a ring;
-//   * warp 2 issues the MMAs: S into one of two TMEM buffers, so that S of the next block is
-//     computed while the softmax works on this one, then P V into the segment's O;
+//   * warp 2 issues the MMAs: S of the next block as soon as the softmax has read this one (two
+//     TMEM buffers at d = 128, one of 256 keys at d = 64), then P V into the segment's O;
 //   * warps 0 and 4 are the softmax (both reach TMEM lanes 0-31): thread r of each owns query row
-//     r (rows >= Nq carry zeros and are never stored), warp 0 keys 0-63 of a block and warp 4 keys
-//     64-127; they exchange the block's row max through shared memory, so both use one reference
+//     r (rows >= Nq carry zeros and are never stored), warp 0 the first half of a block's keys and
+//     warp 4 the second; they exchange the block's row max through shared memory, so both use one reference
 //     max, and each keeps its own part of the running sum. Online softmax as in the forward, P as
 //     bf16 into TMEM; at the end of a segment O / l and the log-sum-exp are written as the piece
 //     (CTA, head), merged per head by decode_merge_kernel.
-// TMEM columns: S_0 [0, 128), S_1 [128, 256), P [256, 320), O [320, 320 + D).
+// Blocks of 256 keys at d = 64 and 128 at d = 128: 32 KB of K and of V per block either way, so
+// that the per-block costs (barrier round trips, MMA issue) weigh the same per byte.
+// TMEM columns: d = 128: S_0 [0, 128), S_1 [128, 256), P [256, 320), O [320, 448); d = 64:
+// S [0, 256), P [256, 384), O [384, 448).
 template <int D>
 struct TcCfg {
-  static constexpr int kBK = kDecodeTcBlockKeys;
-  static constexpr int kTile = 128 * D * 2;           // Q, a K block or a V block (bf16)
-  static constexpr int kBox = 128 * 64 * 2;           // one TMA box: 128 rows x 64 columns
-  static constexpr int kStages = D == 128 ? 3 : 6;    // (K, V) pairs in flight: 192 KB
+  static constexpr int kBK = decode_tc_block_keys(D);  // 32 KB of K and of V per block
+  static constexpr int kHalfKeys = kBK / 2;            // keys per softmax warp
+  static constexpr int kQTile = 128 * D * 2;           // the Q tile (bf16)
+  static constexpr int kKV = kBK * D * 2;              // a K or a V block
+  static constexpr int kBox = 128 * 64 * 2;            // one TMA box: 128 rows x 64 columns
+  static constexpr int kRowBoxes = kBK / 128;          // boxes along the keys of a block
+  static constexpr int kColBoxes = D / 64;             // boxes along d
+  static constexpr int kStages = 3;                    // (K, V) pairs in flight: 192 KB
   static constexpr int kOffQ = 0;
-  static constexpr int kOffRing = kTile;
-  static constexpr int kOffBar = kOffRing + kStages * 2 * kTile;
+  static constexpr int kOffRing = kQTile;
+  static constexpr int kOffBar = kOffRing + kStages * 2 * kKV;
+  // d = 128: two S buffers of 128 columns; d = 64: one of 256 (S of the next block is still
+  // issued as soon as both softmax warps have read this one)
+  static constexpr int kSBufs = D == 64 ? 1 : 2;
   // barriers: full[S], empty[S], q_full, q_empty, s_full[2], s_free[2], p_full, pv_done, o_done,
   // o_free, drain
   static constexpr int kBarFull = 0;
@@ -411,7 +140,10 @@ struct TcCfg {
   static constexpr int kOffTmemPtr = kOffX + (2 * 2 * 32 + 2 * 32) * 4;
   static constexpr int kOffAbort = kOffTmemPtr + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1 KB
-  static constexpr uint32_t kColS = 0, kColP = 256, kColO = 320;
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColP = kSBufs * kBK;    // kBK / 2 columns of bf16 pairs
+  static constexpr uint32_t kColO = kColP + kBK / 2;  // D columns; at most 448 in all
+  static_assert(kColO + D <= 512, "TMEM columns");
 };
 constexpr int kTcThreads = 160;  // warps: 0 and 4 softmax, 1 TMA, 2 MMA, 3 idle
 
@@ -490,20 +222,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
       const int h = rg.head(rg.g0 + i);
       const int e = rg.seg_end(i);
       if (seg > 0 && !(ok = mbar_wait_warp(bar(C::kBarQEmpty), (seg - 1) & 1, ctl))) break;
-      mbar_arrive_expect_tx(bar(C::kBarQFull), C::kTile);
-      for (int b = 0; b < D / 64; ++b)
+      mbar_arrive_expect_tx(bar(C::kBarQFull), C::kQTile);
+      for (int b = 0; b < C::kColBoxes; ++b)
         tma_load_3d(sbase + C::kOffQ + b * C::kBox, &p.tm_q, bar(C::kBarQFull), b * 64, 0, h);
       for (; i < e; ++i) {
         const int st = i % C::kStages, round = i / C::kStages;
         if (!(ok = mbar_wait_warp(bar(C::kBarEmpty + st), (round & 1) ^ 1, ctl))) break;
         const int jb = static_cast<int>((rg.g0 + i) % rg.nb);
-        const uint32_t dst = sbase + C::kOffRing + st * 2 * C::kTile;
-        mbar_arrive_expect_tx(bar(C::kBarFull + st), 2 * C::kTile);
-        for (int b = 0; b < D / 64; ++b) {
-          tma_load_3d(dst + b * C::kBox, &p.tm_k, bar(C::kBarFull + st), b * 64, jb * C::kBK, h);
-          tma_load_3d(dst + C::kTile + b * C::kBox, &p.tm_v, bar(C::kBarFull + st), b * 64,
-                      jb * C::kBK, h);
-        }
+        const uint32_t dst = sbase + C::kOffRing + st * 2 * C::kKV;
+        mbar_arrive_expect_tx(bar(C::kBarFull + st), 2 * C::kKV);
+        // column box b (64 of d) at b * kBK * 128 bytes, row box rb (128 keys) at rb * 16 KB
+        // inside it: the 128-byte-swizzled layout of the whole kBK x D tile
+        for (int rb = 0; rb < C::kRowBoxes; ++rb)
+          for (int b = 0; b < C::kColBoxes; ++b) {
+            const uint32_t off = b * C::kBK * 128 + rb * C::kBox;
+            const int row = jb * C::kBK + rb * 128;
+            tma_load_3d(dst + off, &p.tm_k, bar(C::kBarFull + st), b * 64, row, h);
+            tma_load_3d(dst + C::kKV + off, &p.tm_v, bar(C::kBarFull + st), b * 64, row, h);
+          }
         issued_last = i;
       }
       ++seg;
@@ -526,23 +262,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
     for (int k = 0; k < D / 16; ++k)
       qd[k] = sdesc64(sdesc_lo(sbase + C::kOffQ + (k / 4) * C::kBox + (k % 4) * 32, 16), kHi);
     const uint64_t kd0 = sdesc64(sdesc_lo(sbase + C::kOffRing, 16), kHi);
-    const uint64_t vd0 = sdesc64(sdesc_lo(sbase + C::kOffRing + C::kTile, C::kBox), kHi);
-    constexpr uint64_t kStageStep = (2 * C::kTile) >> 4;
+    const uint64_t vd0 = sdesc64(sdesc_lo(sbase + C::kOffRing + C::kKV, C::kBK * 128), kHi);
+    constexpr uint64_t kStageStep = (2 * C::kKV) >> 4;
     bool ok = true;
     int ns = 0;  // S products issued (buffer ns % 2)
     auto issue_s = [&](int i) {  // S of CTA-local block i (its K stage must be full)
-      const int b = ns & 1;
-      if (ns >= 2) {
-        if (!mbar_wait_warp(bar(C::kBarSFree + b), ((ns >> 1) - 1) & 1, ctl)) return false;
+      const int b = ns % C::kSBufs;
+      if (ns >= C::kSBufs) {
+        if (!mbar_wait_warp(bar(C::kBarSFree + b), (ns / C::kSBufs - 1) & 1, ctl)) return false;
         tc_fence_after();
       }
       const int st = i % C::kStages;
       if (!mbar_wait_warp(bar(C::kBarFull + st), (i / C::kStages) & 1, ctl)) return false;
       tc_fence_after();
       if constexpr (D == 128)
-        mma_qk_d128(tmem + C::kColS + 128u * b, qd, kd0 + st * kStageStep, kIdescS);
+        mma_qk_d128(tmem + C::kColS + C::kBK * b, qd, kd0 + st * kStageStep, kIdescS);
       else
-        mma_qk_d64(tmem + C::kColS + 128u * b, qd, kd0 + st * kStageStep, kIdescS);
+        mma_qk_d64(tmem + C::kColS + C::kBK * b, qd, kd0 + st * kStageStep, kIdescS);
       mma_commit(bar(C::kBarSFull + b));
       ++ns;
       return true;
@@ -565,8 +301,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
           if (!(ok = mbar_wait_warp(bar(C::kBarOFree), (seg - 1) & 1, ctl))) break;
           tc_fence_after();
         }
-        mma_pv_k128(tmem + C::kColO, tmem + C::kColP, vd0 + (i % C::kStages) * kStageStep,
-                    kIdescPV, i > i0 ? 1u : 0u);
+        // 128 keys per call: P columns 64 apart, V rows 16 KB apart (1024 in 16-byte units)
+#pragma unroll
+        for (int rb = 0; rb < C::kRowBoxes; ++rb)
+          mma_pv_k128(tmem + C::kColO, tmem + C::kColP + 64u * rb,
+                      vd0 + (i % C::kStages) * kStageStep + 1024u * rb, kIdescPV,
+                      (i > i0 || rb > 0) ? 1u : 0u);
         mma_commit(bar(C::kBarPVDone));
         mma_commit(bar(C::kBarEmpty + i % C::kStages));
         if (i + 1 == e) mma_commit(bar(C::kBarODone));
@@ -595,18 +335,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
       const int e = rg.seg_end(i);
       float m = -INFINITY, l = 0.f;  // l: this warp's part of the running sum
       for (int i0 = i; i < e; ++i) {
-        const int b = i & 1;
-        if (!(ok = mbar_wait(bar(C::kBarSFull + b), (i >> 1) & 1, ctl))) break;
+        constexpr int kH = C::kHalfKeys;
+        const int sb = i % C::kSBufs;
+        if (!(ok = mbar_wait(bar(C::kBarSFull + sb), (i / C::kSBufs) & 1, ctl))) break;
         tc_fence_after();
-        uint32_t sc[64];
-        tmem_ld64(trow + C::kColS + 128u * b + 64u * hf, sc);
+        uint32_t sc[kH];
+        if constexpr (kH == 128)
+          tmem_ld128(trow + C::kColS + C::kBK * sb + kH * hf, sc);
+        else
+          tmem_ld64(trow + C::kColS + C::kBK * sb + kH * hf, sc);
         tc_fence_before();
-        mbar_arrive(bar(C::kBarSFree + b));
+        mbar_arrive(bar(C::kBarSFree + sb));
+        const int b = i & 1;  // exchange slot
         const int jb = static_cast<int>((rg.g0 + i) % rg.nb);
-        const int n = min(C::kBK, p.Nk - jb * C::kBK) - 64 * hf;  // keys of this half
-        if (n < 64) {
+        const int n = min(C::kBK, p.Nk - jb * C::kBK) - kH * hf;  // keys of this half
+        if (n < kH) {
 #pragma unroll
-          for (int k = 0; k < 64; ++k)
+          for (int k = 0; k < kH; ++k)
             if (k >= n) sc[k] = __float_as_uint(-INFINITY);
         }
         float mxa[8];
@@ -614,7 +359,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
         for (int u = 0; u < 8; ++u)
           mxa[u] = max3(-INFINITY, __uint_as_float(sc[2 * u]), __uint_as_float(sc[2 * u + 1]));
 #pragma unroll
-        for (int k = 16; k < 64; k += 16)
+        for (int k = 16; k < kH; k += 16)
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             mxa[u] = max3(mxa[u], __uint_as_float(sc[k + 2 * u]), __uint_as_float(sc[k + 2 * u + 1]));
@@ -636,9 +381,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
         unsigned long long rs[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) rs[u] = f2_pack(0.f, 0.f);
-        uint32_t pk[32];
+        uint32_t pk[kH / 2];
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
+        for (int u = 0; u < kH / 2; ++u) {
           const unsigned long long x = f2_fma(
               f2_pack(__uint_as_float(sc[2 * u]), __uint_as_float(sc[2 * u + 1])), k2, nm2);
           float x0, x1;
@@ -664,8 +409,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
           l *= alpha;
         }
         m = m_new;
-        tmem_st16(trow + C::kColP + 32u * hf, pk);
-        tmem_st16(trow + C::kColP + 32u * hf + 16, pk + 16);
+#pragma unroll
+        for (int u = 0; u < kH / 32; ++u)
+          tmem_st16(trow + C::kColP + (kH / 2) * hf + 16u * u, pk + 16 * u);
         float rs0, rs1;
         f2_unpack(f2_add(f2_add(rs[0], rs[1]), f2_add(rs[2], rs[3])), rs0, rs1);
         l += rs0 + rs1;
@@ -712,62 +458,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
   }
 }
 
-template <int D, int NQ>
-cudaError_t configure() {
-  return cudaFuncSetAttribute(decode_stream_kernel<D, NQ>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, DCfg<D>::kSmemBytes);
-}
-
-// The CUDA-core kernel runs for one query row at d = 64 only (the tensor-core kernel below is
-// faster everywhere else): its single instance.
-cudaError_t launch_cuda_cores(const DecodeParams& p_in, cudaStream_t s) {
-  // the block size is the kernel's: blocks per head, the CTA count (at most one per block) and
-  // the pieces' layout in the workspace follow from it
-  DecodeParams p = p_in;
-  p.blocks_per_head = (p.Nk + DCfg<64>::kBK - 1) / DCfg<64>::kBK;
-  const long long blocks = static_cast<long long>(p.BH) * p.blocks_per_head;
-  if (p.n_ctas > blocks) p.n_ctas = static_cast<int>(blocks);
-  p.ws_lse = p.ws_o + static_cast<size_t>(p.n_ctas + p.BH) * p.Nq * 64;
-  decode_stream_kernel<64, 1><<<p.n_ctas, kThreads, DCfg<64>::kSmemBytes, s>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  decode_merge_kernel<64><<<static_cast<unsigned>(p.BH) * p.Nq, 64, 0, s>>>(p);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 cudaError_t configure_decode() {
-  cudaError_t e = configure<64, 1>();
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             TcCfg<64>::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<64>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       TcCfg<64>::kSmemBytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(decode_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              TcCfg<128>::kSmemBytes);
   return e;
 }
 
-int decode_ctas_per_sm() {
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_stream_kernel<64, 1>, kThreads,
-                                                    DCfg<64>::kSmemBytes) != cudaSuccess) {
-    cudaGetLastError();
-    return 1;
-  }
-  return n < 1 ? 1 : n;
-}
-
-cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t s) {
-  if (d != 64 || p.Nq != 1) return cudaErrorInvalidValue;
-  return launch_cuda_cores(p, s);
-}
-
 namespace {
 template <int D>
 cudaError_t launch_tc(const DecodeParams& p_in, cudaStream_t s) {
+  // the block size is the kernel's: blocks per head, the CTA count (at most one per block) and
+  // the pieces' layout in the workspace follow from it
   DecodeParams p = p_in;
-  p.blocks_per_head = (p.Nk + kDecodeTcBlockKeys - 1) / kDecodeTcBlockKeys;
+  p.blocks_per_head = (p.Nk + TcCfg<D>::kBK - 1) / TcCfg<D>::kBK;
   const long long blocks = static_cast<long long>(p.BH) * p.blocks_per_head;
   if (p.n_ctas > blocks) p.n_ctas = static_cast<int>(blocks);
   p.ws_lse = p.ws_o + static_cast<size_t>(p.n_ctas + p.BH) * p.Nq * D;
@@ -779,7 +488,7 @@ cudaError_t launch_tc(const DecodeParams& p_in, cudaStream_t s) {
 }
 }  // namespace
 
-cudaError_t launch_decode_tc(const DecodeParams& p, int d, cudaStream_t s) {
+cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t s) {
   if (d == 64) return launch_tc<64>(p, s);
   if (d == 128) return launch_tc<128>(p, s);
   return cudaErrorInvalidValue;

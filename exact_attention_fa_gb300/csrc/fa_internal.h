@@ -73,14 +73,15 @@ struct BwdParams {
 };
 
 // Decoding: Nq <= kDecodeMaxNq query rows per head against Nk keys. The key blocks of all heads
-// (kDecodeMinBlockKeys keys or more, by head dimension) are dealt out to n_ctas CTAs in
-// contiguous ranges; piece (CTA c, head h) is slot c + h.
+// (decode_tc_block_keys(d) keys each) are dealt out to n_ctas CTAs in contiguous ranges; piece
+// (CTA c, head h) is slot c + h.
 constexpr int kDecodeMaxNq = 8;
 constexpr int kDecodeMaxCtas = 1024;
-constexpr int kDecodeMinBlockKeys = 32;
+// Keys per block: 32 KB of K and of V per block at either head dimension.
+constexpr int decode_tc_block_keys(int d) { return d == 64 ? 256 : 128; }
 struct DecodeParams {
-  // tensor-core path (2 <= Nq): 3-D views [BH][rows][d] of q (rows Nq), k and v (rows Nk), box
-  // 64 x 128 x 1, 128-byte swizzle; rows past the extent read as zero
+  // 3-D views [BH][rows][d] of q (rows Nq), k and v (rows Nk), box 64 x 128 x 1, 128-byte
+  // swizzle; rows past the extent read as zero
   CUtensorMap tm_q;
   CUtensorMap tm_k;
   CUtensorMap tm_v;
@@ -119,13 +120,8 @@ cudaError_t launch_fwd_pair(const FwdParams& p, int d, cudaStream_t s);         
 cudaError_t launch_fwd_fp8(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_fwd_fp32(const Fp32FwdParams& p, cudaStream_t s);
 cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t s);
-// Decoding on the CUDA cores: one query row at d = 64 (the only case it is used for).
+// Decoding: the split kernel on the tensor cores (tensor maps in p), then the merge of the pieces.
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t s);
-// Decoding with the products on the tensor cores (d = 128, or several query rows): 128-key
-// blocks (tensor maps in p), the same pieces and merge as launch_decode.
-constexpr int kDecodeTcBlockKeys = 128;
-cudaError_t launch_decode_tc(const DecodeParams& p, int d, cudaStream_t s);
-int decode_ctas_per_sm();  // resident CUDA-core decoding CTAs per SM (d = 64, one query row)
 // Opt the kernels that use more than 48 KB of dynamic shared memory in to their size. Function
 // attributes belong to a device's context, so these run once per device, with it current.
 cudaError_t configure_fwd_pair();

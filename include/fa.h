@@ -170,9 +170,10 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
  *     o = softmax(scale * q K^T) V,   lse = log sum_j exp(scale * q.k_j).
  * q, o : bf16 [B,H,Nq,d];  k, v : bf16 [B,H,Nk,d];  lse : fp32 [B,H,Nq] (all DEVICE pointers,
  * 16-byte aligned, caller-owned; q, k, v read, o and lse written). d in {64, 128}; Nk >= 1.
- * The work is a matrix-vector product bound by HBM bandwidth. The key blocks of all heads (32
- * keys at d = 128, 64 at d = 64) are split into n_ctas equal contiguous ranges streamed by
- * separate CTAs (a range may cut a head and span several); the pieces of each head are merged
+ * The work is a matrix-vector product bound by HBM bandwidth. The key blocks of all heads (128
+ * keys at d = 128, 256 at d = 64) are split into n_ctas equal contiguous ranges streamed by
+ * separate CTAs (a range may cut a head and span several), each block's products on the tensor
+ * cores with the query rows zero-padded to a 128-row tile; the pieces of each head are merged
  * with the softmax statistics merge.
  * n_ctas = 0 takes as many CTAs as the device holds at once (fa_decode_ctas); 1 .. 1024 forces
  * the count (capped at the number of key blocks). `workspace`: fa_decode_workspace_bytes(...)
@@ -187,9 +188,9 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
  * without a usable device. */
 int fa_decode_ctas(int B, int H, int Nq, int Nk, int d);
 
-/* Bytes of workspace fa_decode needs for any n_ctas: (min(B*H*ceil(Nk/32), 1024) + B*H) pieces
- * of Nq rows, each row d + 1 floats (the piece's normalised output and log-sum-exp); 0 for
- * invalid sizes. */
+/* Bytes of workspace fa_decode needs for any n_ctas: (min(B*H*ceil(Nk/K), 1024) + B*H) pieces
+ * of Nq rows, K the keys per block (128 at d = 128, 256 at d = 64), each row d + 1 floats (the
+ * piece's normalised output and log-sum-exp); 0 for invalid sizes. */
 size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d);
 
 /* Diagnostic, with no counterpart on the pages: launches one CTA whose thread waits on an
@@ -210,7 +211,8 @@ const char* fa_status_string(int status);
 /* ABI version: (major << 16) | minor. Major 2: fa_fwd_blocksparse takes a causal flag; minor 1:
  * fa_decode; minor 2: fa_bwd_blocksparse; minor 3: fa_fwd_fp32_fa1; minor 4:
  * fa_bwd_workspace_bytes depends on d (8 bytes per row at d = 128); minor 5: fa_fwd_fp8;
- * minor 6: fa_set_exp2_emulation, fa_get_exp2_emulation. */
+ * minor 6: fa_set_exp2_emulation, fa_get_exp2_emulation; minor 7: fa_decode on the tensor cores,
+ * fa_decode_workspace_bytes counted with its blocks. */
 int fa_abi_version(void);
 
 #ifdef __cplusplus

@@ -100,8 +100,10 @@ def test_decode_validation(lib):
 
 
 def test_decode_workspace_and_ctas(lib):
-    # pieces: min(key blocks, 1024) CTAs + B*H heads, Nq rows of d + 1 floats each
-    assert lib.fa_decode_workspace_bytes(2, 3, 4, 1000, 128) == (6 * 32 + 6) * 4 * 129 * 4
+    # pieces: min(key blocks, 1024) CTAs + B*H heads, Nq rows of d + 1 floats each; blocks of 128
+    # keys at d = 128, 256 at d = 64
+    assert lib.fa_decode_workspace_bytes(2, 3, 4, 1000, 128) == (6 * 8 + 6) * 4 * 129 * 4
+    assert lib.fa_decode_workspace_bytes(2, 3, 4, 1000, 64) == (6 * 4 + 6) * 4 * 65 * 4
     assert lib.fa_decode_workspace_bytes(8, 32, 1, 32768, 128) == (1024 + 256) * 129 * 4
     assert lib.fa_decode_workspace_bytes(1, 1, 9, 100, 64) == 0  # unsupported sizes
     assert lib.fa_decode_ctas(1, 1, 9, 100, 64) == 0

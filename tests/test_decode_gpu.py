@@ -44,8 +44,7 @@ def run_decode(w, device, n_ctas=0, heads=None):
     (1, 129, 128, 18),   # one block per CTA
     (5, 300, 128, 1024), # more CTAs asked for than there are blocks (capped)
     (4, 2048, 64, 0),
-    # one query row at d = 64 runs on the CUDA cores, everything else on the tensor cores
-    (1, 4097, 64, 0),
+    (1, 4097, 64, 0),    # a key past a 256-key block boundary
     (1, 1000, 64, 7),
     (1, 129, 64, 1024),
 ])
@@ -56,8 +55,8 @@ def test_decode_small(cuda, nq, nk, d, ctas):
 
 @pytest.mark.parametrize("d,nq", [(64, 2), (128, 2), (64, 1), (128, 1)])
 def test_decode_long_ranges(cuda, d, nq):
-    """Eight CTAs, each streaming hundreds of blocks through its ring and across a head boundary
-    (ragged last block per head), on either kernel."""
+    """Eight CTAs, each streaming dozens of blocks through its ring and across a head boundary
+    (ragged last block per head)."""
     w = wl.Workload("decode_long", 2, 4, 16384 + 7, d, nq=nq, seed=50 + d + nq)
     run_decode(w, cuda, 8)
 
@@ -95,8 +94,8 @@ def test_decode_N32768_launch_configuration(cuda):
 
 @pytest.mark.parametrize("d", [64, 128])
 def test_decode_eight_rows_long_cache_every_head(cuda, d):
-    """Eight query rows against 32768 keys on 32 heads (the tensor-core decoding path at the bench's
-    cache length, 152 CTAs cutting heads mid-way), every head against the oracle."""
+    """Eight query rows against 32768 keys on 32 heads (the bench's cache length, CTAs cutting
+    heads mid-way), every head against the oracle."""
     w = wl.Workload("decode_q8_long", 2, 16, 32768, d, nq=8, seed=56 + d)
     run_decode(w, cuda)
 
@@ -104,7 +103,7 @@ def test_decode_eight_rows_long_cache_every_head(cuda, d):
 @pytest.mark.parametrize("d", [64, 128])
 def test_decode_one_and_eight_rows_agree(cuda, d):
     """The one-row results equal the first row of an eight-row call on the same cache (within the
-    bf16 tolerance; at d = 64 the two come from different kernels)."""
+    bf16 tolerance): the zero-padded query rows do not disturb the others."""
     w8 = wl.Workload("decode_rows8", 1, 4, 5000, d, nq=8, seed=57)
     inp = wl.make_inputs(w8)
     q, k, v = (H.to_device(inp, n, cuda) for n in ("q", "k", "v"))
