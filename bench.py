@@ -8,9 +8,10 @@ N=8192, d=128, bf16 (the largest specified problem); the same line carries a `pe
 with one entry for each of the other specified workloads (the fp32 single head, the multi-head
 N=2048 forward, the block-sparse N=16384 forward and the causal N=4096 backward), each timed
 the same way, with its own roofline fraction, clocks and oracle baseline, and a `next_rows` object
-with the FP8 (e4m3) forward on the long-sequence shape, measured against the fp8 peak, and the
-bf16 forwards of the long-sequence and multi-head workloads with part of the exponentials computed
-in software (fa_set_exp2_emulation), which is off by default.
+with the FP8 (e4m3) forward on the long-sequence shape, measured against the fp8 peak, the bf16
+forwards of the long-sequence and multi-head workloads with part of the exponentials computed in
+software (fa_set_exp2_emulation), which is off by default, and decoding with eight query rows per
+head against a 32768-key cache, in GB/s against the measured copy bandwidth.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--backward]
                   [--no-per-config] [--impl ours|reference]
@@ -90,6 +91,8 @@ def per_config_names(main_name: str):
 # Workloads of rows past the specified ones, measured beside them on the default line: the FP8
 # forward on the long-sequence causal shape.
 NEXT_ROWS = ["causal_N8192_d128_fp8"]
+# ... and decoding (split keys + merge) with eight new query rows per head, in GB/s against HBM.
+NEXT_DECODE = "decode_N32768_d128_q8_b2"
 EXP2_EMULATION_PER32 = 4  # fa_set_exp2_emulation's setting measured on the default line
 
 
@@ -603,10 +606,12 @@ def run_ours(args):
     others = per_config_names(w.name) if default_line else []
     nexts = list(NEXT_ROWS) if default_line else []
     cfg_w = {n: wl.WORKLOADS[n] for n in others + nexts}
+    dec_w = wl.WORKLOADS[NEXT_DECODE] if default_line else None
 
     # host inputs first; the oracle's worker pool (spawned) runs before CUDA is touched
     inp = wl.make_inputs(w, with_do=w.backward)
     cfg_inp = {n: wl.make_inputs(cw, with_do=cw.backward) for n, cw in cfg_w.items()}
+    dec_inp = wl.make_inputs(dec_w) if dec_w is not None else None
     cpu, cfg_cpu = None, {}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = host_cores()
@@ -615,6 +620,8 @@ def run_ours(args):
             cpu = cpu_baseline_leg(pool, cores, w, inp, budget_s=20.0, min_s=10.0)
             for n, cw in cfg_w.items():
                 cfg_cpu[n] = cpu_baseline_leg(pool, cores, cw, cfg_inp[n], budget_s=6.0)
+            if dec_w is not None:
+                cfg_cpu[NEXT_DECODE] = cpu_baseline_leg(pool, cores, dec_w, dec_inp, budget_s=6.0)
         finally:
             pool.terminate()
 
@@ -674,6 +681,9 @@ def run_ours(args):
             e["roofline"]["kernel"] += f" ({EXP2_EMULATION_PER32} of 32 exponentials in software)"
             e["roofline"]["traffic"] = None  # the traffic record is the default instance's
             next_rows[f"{n}+exp2_emulation"] = e
+        next_rows[NEXT_DECODE] = decode_entry(dec_w, dec_inp, fa, dev, flush_buf, K,
+                                              max(3, args.warmup), world, local,
+                                              cfg_cpu.get(NEXT_DECODE))
 
     if rank != 0:
         if world > 1:
@@ -704,6 +714,64 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def decode_entry(w, inp, fa, dev, flush_buf, steps, warmup, world, local, cpu=None):
+    """A decoding workload timed like the per-configuration entries (CUDA events around each
+    fa_decode call, L2 flushed before each, clocks sampled), reported in GB/s of algorithmic bytes
+    against the measured copy bandwidth."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from exact_attention_fa_gb300 import workloads as wl
+
+    def dev_tensor(name):
+        return torch.from_numpy(inp.raw(name).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q, k, v = dev_tensor("q"), dev_tensor("k"), dev_tensor("v")
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    n_ctas = fa.fa_decode_ctas(w.B, w.H, w.nq, w.N, w.d)
+    ws = torch.empty(fa.fa_decode_workspace_bytes(w.B, w.H, w.nq, w.N, w.d), dtype=torch.uint8,
+                     device=dev)
+    algo_bytes = wl.decode_bytes(w)
+
+    def timed(n):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for i in range(n):
+            flush_buf.zero_()
+            ev[i][0].record()
+            fa.fa_decode(q, k, v, o, lse, w.softmax_scale, n_ctas, ws)
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        return statistics.fmean(ev[i][0].elapsed_time(ev[i][1]) for i in range(n))
+
+    for _ in range(warmup):
+        flush_buf.zero_()
+        fa.fa_decode(q, k, v, o, lse, w.softmax_scale, n_ctas, ws)
+    fa.fa_check_device_error(dev)
+    n = per_config_steps(timed(3), steps)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(os.path.join("/tmp", f"fa_clocks_{os.getpid()}.csv")) as clocks:
+        time.sleep(0.1)
+        t = timed(n)
+        time.sleep(0.1)
+    fa.fa_check_device_error(dev)
+    t = aggregate_over_ranks([t], world, dev)[0]
+    peaks, peak_src = load_peaks()
+    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    achieved = algo_bytes / (t * 1e-3) / 1e9
+    kname = f"decode_tc_kernel<{w.d}> (+ decode_merge_kernel<{w.d}>)"
+    return {"config": {**config_of(w, world), "n_ctas": n_ctas}, "ms_per_step": t, "steps": n,
+            "gbs": world * achieved,
+            "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
+                         "unit": "GB/s", "frac": achieved / peak,
+                         "peak_source": f"{peak_src} copy bandwidth",
+                         "algorithmic_bytes": algo_bytes,
+                         "traffic": recorded_traffic(kname, w)},
+            "cpu_baseline": cpu, "gpu_launches": 2 * n, "clocks": clocks.summary(local)}
 
 
 def run_decode(args, w, fa, inp, cpu, world, rank, local, dev, flush_buf):

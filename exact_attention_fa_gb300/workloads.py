@@ -175,6 +175,11 @@ WORKLOADS["decode_N32768_d128_q8"] = Workload("decode_N32768_d128_q8", 8, 32, 32
 WORKLOADS["decode_N32768_d64_q8"] = Workload("decode_N32768_d64_q8", 8, 32, 32768, 64, nq=8,
                                              seed=16)
 
+# The eight-row decoding problem on 2 x 32 heads (K, V 1.07 GB: larger than L2), measured on the
+# default bench line.
+WORKLOADS["decode_N32768_d128_q8_b2"] = Workload("decode_N32768_d128_q8_b2", 2, 32, 32768, 128,
+                                                 nq=8, seed=17)
+
 # Counter-capture cases of the e4m3 forward and of the backward on 8 heads (small device footprint).
 WORKLOADS["causal_N4096_d128_fp8_h8"] = Workload("causal_N4096_d128_fp8_h8", 1, 8, 4096, 128,
                                                  dtype="e4m3", causal=True, seed=13)

@@ -76,6 +76,9 @@ def test_bench_default_line_has_per_config_entries(cuda):
     assert f8["config"]["dtype"] == "e4m3" and 0 < f8["roofline"]["frac"] < 1.2
     assert f8["roofline"]["kernel"] == "fwd_pair_kernel<128, true>"
     assert f8["roofline"]["peak"] > 1.9 * d["roofline"]["peak"]  # the fp8 peak
+    dec = d["next_rows"]["decode_N32768_d128_q8_b2"]
+    assert dec["roofline"]["bound"] == "hbm" and 0 < dec["roofline"]["frac"] < 1.3
+    assert dec["gbs"] > 0 and dec["cpu_baseline"]["unit"] == "GB/s"
     for n in ("causal_N8192_d128+exp2_emulation", "mha_N2048_d64+exp2_emulation"):
         e = d["next_rows"][n]
         assert e["exp2_emulation_per32"] == 4 and e["tflops"] > 0 and e["roofline"]["frac"] > 0
