@@ -280,6 +280,8 @@ int bwd_bf16(const void* q, const void* k, const void* v, const void* o, const v
   p.lse2 = static_cast<float*>(workspace);
   p.Dsum = static_cast<float*>(workspace) + rows;
   p.aug = d == 64 ? static_cast<uint8_t*>(workspace) + rows * 2 * sizeof(float) : nullptr;
+  p.ctr = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) +
+                                      rows * fa::bwd_row_workspace_bytes(d));
   p.BH = BH;
   p.N = N;
   p.d = d;
@@ -316,7 +318,7 @@ int fa::check_bwd_args(const void* q, const void* k, const void* v, const void* 
 
 extern "C" {
 
-int fa_abi_version(void) { return (2 << 16) | 7; }
+int fa_abi_version(void) { return (2 << 16) | 8; }
 
 const char* fa_status_string(int status) {
   switch (status) {
@@ -390,8 +392,8 @@ int fa_fwd_fp32_fa1(const float* q, const float* k, const float* v, float* o, fl
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
   const size_t rows = static_cast<size_t>(B) * H * ((static_cast<size_t>(N) + 127) / 128) * 128;
-  // lse2 and D; at d = 64 also their two 32-byte operand rows
-  return rows * (2 * sizeof(float) + (d == 64 ? 64 : 0));
+  // per row lse2 and D (and at d = 64 their operand rows), then the work counters
+  return rows * fa::bwd_row_workspace_bytes(d) + fa::bwd_counter_bytes(static_cast<size_t>(B) * H);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,

@@ -7,9 +7,18 @@
 //     dS = P * (dP - D),  dQ = scale * dS K,  dK = scale * dS^T Q.
 //
 // Kernel 1 (prep): per row, D_i and lse2_i = lse_i * log2(e) into the workspace (padded to whole
-// 128-row tiles: +inf / 0 on padding rows so that they contribute nothing), and dQ zeroed.
+// 128-row tiles: +inf / 0 on padding rows so that they contribute nothing); the work counters
+// and the dQ rows of the first head group zeroed.
 //
-// Kernel 2 (main), one CTA per (128-key tile j, head), 16 warps:
+// Kernel 2 (main), one CTA per (128-key tile j, head), 16 warps. Heads are taken in groups whose
+// inputs fit in L2. At d = 128 the prep kernel zeroes the dQ rows of the first groups, as many as
+// about 40 MB of dQ allows; after those, the CTAs of group g zero the rows of group g + 1 when
+// they start, and a CTA of group g + 1 adds into dQ only once all of them have. Zeros are thus
+// written shortly before they are used, while they are still in L2 (zeroing all of a large dQ up
+// front wrote it to DRAM and read most of it back). Work items are then handed out in CTA start
+// order through a counter, so the CTAs a CTA waits for have all started before it. At d = 64 the
+// prep kernel zeroes all of dQ.
+//   * warps 12-15 (d = 128) first zero this CTA's share of the next group's dQ rows;
 //   * warp 8 (one elected lane): TMA. K_j and V_j once; then per query tile i, Q_i, dO_i and the 128
 //     lse2 / D values of that tile into a ring of stages;
 //   * warp 9 (one elected lane): MMAs. S^T = K Q_i^T and dP^T = V dO_i^T (keys on TMEM lanes, queries on
@@ -96,6 +105,10 @@ struct BCfg {
   // (128-byte-swizzled fp32 boxes of 64 rows x 32 columns, 32 KB) in its own buffer for TMA bulk
   // reductions. Either way the ring stage is free as soon as the MMAs have read Q_i and dO_i.
   static constexpr bool kDQTransposed = D == 128;
+  // d = 128: the main kernel zeroes dQ rows itself, one head group ahead, past the groups the
+  // prep kernel zeroes; d = 64 (whose dQ rows are half the size) leaves all of it to the prep
+  // kernel: measured, the in-kernel form cost the d = 64 kernel 5% and saved it no time.
+  static constexpr bool kZeroInKernel = D == 128;
   static constexpr int kOffDQStage = kOffStage + kStages * kStageBytes;
   static constexpr int kDQStageBytes = kDQTransposed ? 0 : 128 * D * 4;
   static constexpr int kOffOnes = kOffDQStage + kDQStageBytes;  // 4 KB constant A tile (d = 64)
@@ -119,6 +132,7 @@ struct BCfg {
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffTmemPtr = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemPtr + 4;
+  static constexpr int kOffTicket = kOffAbort + 4;  // this CTA's work item
   static constexpr int kOffQMask = kOffAbort + 12;  // block-sparse: query tiles to visit (bits)
   static constexpr int kSmemBytes = kOffQMask + kMaxMaskTiles / 8;  // base 1024-aligned (checked)
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
@@ -137,15 +151,85 @@ struct BCfg {
                 "register split exceeds the launch's 512 x 128 registers");
 };
 
-// CTA -> (head, key tile). Heads in L2-sized groups; inside a group the key tiles with the most
-// query tiles to visit (causal: the first ones) come first.
-__device__ __forceinline__ void decode_bwd(const BwdParams& p, int group, int& bh, int& j) {
+// Work item -> (head, key tile). Heads in L2-sized groups of `group`; inside a group the key
+// tiles with the most query tiles to visit (causal: the first ones) come first.
+struct BwdItem {
+  int bh, j;
+  int g, within;  // head group, index of the item within its group
+};
+__device__ __forceinline__ BwdItem decode_bwd(const BwdParams& p, int group, int item) {
+  BwdItem w;
   const int per_group = group * p.n_tiles;
-  const int g = blockIdx.x / per_group;
-  const int within = blockIdx.x - g * per_group;
-  const int gsize = min(group, p.BH - g * group);
-  j = within / gsize;
-  bh = g * group + within % gsize;
+  w.g = item / per_group;
+  w.within = item - w.g * per_group;
+  const int gsize = min(group, p.BH - w.g * group);
+  w.j = w.within / gsize;
+  w.bh = w.g * group + w.within % gsize;
+  return w;
+}
+
+// L2 cache policies: O and dO are read once by the prep kernel (evict first); zeroed dQ rows are
+// written to be kept (evict last), so that the main kernel's reductions find them in L2.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint4 ld_evict_first(const __nv_bfloat16* ptr, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void st_zero_evict_last(float* ptr, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %1, %1, %1}, %2;" ::"l"(ptr), "f"(0.f),
+               "l"(pol)
+               : "memory");
+}
+
+// The dQ drain warpgroup (warps 12-15), at its start: unless the prep kernel zeroes it (groups
+// below zgroups), zero this CTA's share of the dQ rows of head group g + 1 (the group's rows split
+// evenly over its CTAs, 16 bytes per store), then count the share done. The counter is raised
+// after a barrier of the four warps and a fence, so the stores of all 128 threads are visible at
+// gpu scope before it moves.
+template <int D>
+__device__ void zero_next_group(const BwdParams& p, int group, int zgroups, const BwdItem& w) {
+  const int n_groups = (p.BH + group - 1) / group;
+  if (w.g + 1 < zgroups || w.g + 1 >= n_groups) return;
+  const int t = static_cast<int>(threadIdx.x) - kDrainWarp0 * 32;
+  const long long ncta = static_cast<long long>(min(group, p.BH - w.g * group)) * p.n_tiles;
+  const int next = min(group, p.BH - (w.g + 1) * group);
+  const long long units = static_cast<long long>(next) * p.N * (D / 4);  // float4 units
+  const long long u0 = units * w.within / ncta, u1 = units * (w.within + 1) / ncta;
+  float* base = p.dq + static_cast<size_t>(w.g + 1) * group * p.N * D;
+  const uint64_t pol = l2_policy_evict_last();
+  for (long long u = u0 + t; u < u1; u += 128) st_zero_evict_last(base + 4 * u, pol);
+  bar_sync(1, 128);
+  if (t == 0) {
+    __threadfence();
+    atomicAdd(p.ctr + 1 + w.g + 1, 1u);
+  }
+}
+
+// Before any reduction into dQ (right after its own zeroing, while the first dQ_i is still being
+// computed), the drain of a CTA of head group g >= zgroups waits until every CTA of group g - 1
+// has zeroed its share of group g's rows (the prep kernel zeroes the groups below zgroups). Those
+// CTAs took earlier work items, so they have started, and each zeroes before anything else it
+// does: the wait ends unless a CTA failed. One thread waits; the caller's barrier of the four
+// drain warps orders the others' reductions after it.
+__device__ __forceinline__ bool wait_group_zeroed(const BwdParams& p, const Ctl& ctl, int group,
+                                                  int zgroups, const BwdItem& w) {
+  if (w.g < zgroups || threadIdx.x != kDrainWarp0 * 32) return true;
+  if (!wait_counter_geq(p.ctr + 1 + w.g, static_cast<unsigned>(group * p.n_tiles), ctl))
+    return false;
+  __threadfence();
+  return true;
 }
 
 // P^T / dS^T as the TMEM operand of dV / dK: the warpgroup owning query columns [64c, 64c+64)
@@ -635,7 +719,7 @@ __device__ void bwd_drain_transposed(const BwdParams& p, uint32_t sbase, uint32_
 
 template <int D, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_constant__ BwdParams p,
-                                                             int group, int npad) {
+                                                             int group, int zgroups, int npad) {
   using C = BCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -648,8 +732,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     return;
   }
   const int warp = threadIdx.x / 32;
-  int bh, j;
-  decode_bwd(p, group, bh, j);
+  // the work item: the next one in CTA start order
+  // The work item: at d = 128 the next one in CTA start order (the dQ zeroing of later head
+  // groups relies on it); at d = 64 the prep kernel zeroes all of dQ and the block index serves.
+  int item = static_cast<int>(blockIdx.x);
+  if constexpr (C::kZeroInKernel) {
+    volatile int* ticket = reinterpret_cast<volatile int*>(smem + C::kOffTicket);
+    if (threadIdx.x == 0) *ticket = static_cast<int>(atomicAdd(p.ctr, 1u));
+    __syncthreads();
+    item = *ticket;
+  }
+  const BwdItem w = decode_bwd(p, group, item);
+  const int bh = w.bh, j = w.j;
   uint32_t* qbits = reinterpret_cast<uint32_t*>(smem + C::kOffQMask);
   const QueryPlan<kMask> plan{qbits, p.causal ? j : 0, p.n_tiles};
   if (kMask) {
@@ -717,10 +811,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
       regs_inc<C::kRegsDrain>();
     else
       regs_dec<C::kRegsDrain>();
-    if (C::kDQTransposed)
-      bwd_drain_transposed<D>(p, sbase, tmem, ctl, bh, plan);
-    else
+    if constexpr (C::kZeroInKernel) {
+      // zero this CTA's share of the next group's dQ rows, then wait until this group's rows
+      // are zero, before the first dQ_i is ready
+      zero_next_group<D>(p, group, zgroups, w);
+      if (!bar_red_or(1, 128, !wait_group_zeroed(p, ctl, group, zgroups, w)))
+        bwd_drain_transposed<D>(p, sbase, tmem, ctl, bh, plan);
+    } else {
       bwd_drain<D>(p, sbase, smem, tmem, ctl, bh, plan);
+    }
   }
 
   tc_fence_before();
@@ -731,44 +830,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
   }
 }
 
-// L2 cache policies: O and dO are read once here (evict first); the zeroed dQ rows are written
-// to be kept (evict last), so that the main kernel's reductions find them in L2.
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-__device__ __forceinline__ uint4 ld_evict_first(const __nv_bfloat16* ptr, uint64_t pol) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(ptr), "l"(pol));
-  return v;
-}
-__device__ __forceinline__ void st_zero_evict_last(float* ptr, uint64_t pol) {
-  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %1, %1, %1}, %2;" ::"l"(ptr), "f"(0.f),
-               "l"(pol)
-               : "memory");
-}
-
 // ---------------------------------------------------------------------------------------------
 // prep: D_i = sum_k dO_ik O_ik, lse2_i = lse_i * log2(e) (padding rows: D = 0, lse2 = +inf),
-// dQ rows zeroed. D / 8 threads per row, 8 elements each. The rows are walked from the last head
-// to the first: the main kernel starts with the first heads, whose zeroed dQ rows (and D, lse2)
-// are then the ones most recently written, still in L2, instead of being read back from DRAM.
+// the dQ rows of the first zgroups head groups (the main kernel's first zgroups * group heads)
+// zeroed, and the main kernel's work counters zeroed. D / 8 threads per row, 8 elements each. The
+// rows are walked from the last head to the first: the main kernel starts with the first heads,
+// whose zeroed dQ rows (and D, lse2) are then the ones most recently written, still in L2.
 template <int D>
-__global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ BwdParams p, int npad) {
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ BwdParams p, int npad,
+                                                       int group, int zgroups) {
   constexpr int kTpr = D / 8;
   const long long rows_total = static_cast<long long>(p.BH) * npad;
   const long long total = rows_total * kTpr;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   const int lane = threadIdx.x % 32;
   const uint64_t pol_first = l2_policy_evict_first(), pol_last = l2_policy_evict_last();
+  if (blockIdx.x == 0)
+    for (int c = threadIdx.x; c < 1 + (p.BH + group - 1) / group; c += blockDim.x) p.ctr[c] = 0u;
   for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t - lane < total;
        t += stride) {
     const bool valid = t < total;
@@ -790,8 +868,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ B
         acc = fmaf(x.x, y.x, acc);
         acc = fmaf(x.y, y.y, acc);
       }
-      st_zero_evict_last(p.dq + off, pol_last);
-      st_zero_evict_last(p.dq + off + 4, pol_last);
+      if (bh < zgroups * group) {
+        st_zero_evict_last(p.dq + off, pol_last);
+        st_zero_evict_last(p.dq + off + 4, pol_last);
+      }
     }
 #pragma unroll
     for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(~0u, acc, off);
@@ -841,18 +921,26 @@ template <int D>
 cudaError_t launch_d(const BwdParams& p, int num_sms, cudaStream_t s) {
   using C = BCfg<D>;
   const int npad = p.n_tiles * BT;
-  bwd_prep_kernel<D><<<num_sms * 8, 256, 0, s>>>(p, npad);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   const long long head_bytes = 4ll * p.N * D * 2;
   long long g = (32ll << 20) / head_bytes;
   const int group = static_cast<int>(g < 1 ? 1 : (g > p.BH ? p.BH : g));
+  // head groups whose dQ rows the prep kernel zeroes: about 40 MB of dQ, which stays in L2 until
+  // the main kernel's first groups use it (at least one group)
+  const int n_groups = (p.BH + group - 1) / group;
+  const long long group_dq_bytes = static_cast<long long>(group) * p.N * D * 4;
+  const long long zg = C::kZeroInKernel ? (40ll << 20) / group_dq_bytes : n_groups;
+  const int zgroups = static_cast<int>(zg < 1 ? 1 : (zg > n_groups ? n_groups : zg));
+  bwd_prep_kernel<D><<<num_sms * 8, 256, 0, s>>>(p, npad, group, zgroups);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.n_tiles) * p.BH;
   if (grid > 0x7fffffffll) return cudaErrorInvalidConfiguration;
   if (p.block_mask)
-    bwd_tc_kernel<D, true><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, s>>>(p, group, npad);
+    bwd_tc_kernel<D, true><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, s>>>(
+        p, group, zgroups, npad);
   else
-    bwd_tc_kernel<D, false><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, s>>>(p, group, npad);
+    bwd_tc_kernel<D, false><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, s>>>(
+        p, group, zgroups, npad);
   return cudaGetLastError();
 }
 

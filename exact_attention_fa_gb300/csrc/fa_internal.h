@@ -62,6 +62,10 @@ struct BwdParams {
   // workspace, d = 64: per 128-row tile two 4 KB bf16 operand tiles (128 rows x 16, K-major,
   // no swizzle) holding -lse2 / scale_log2 and -D, each split into three bf16 parts
   uint8_t* aug;
+  // workspace: the main kernel's work counters, zeroed by the prep kernel: [0] hands out work
+  // items in CTA start order, [1 + g] counts the CTAs that have zeroed their share of head group
+  // g's dQ rows
+  unsigned* ctr;
   const uint8_t* block_mask;  // [n_tiles][n_tiles] tile mask (row = query tile), or null
   int BH, N, d;
   int n_tiles;
@@ -99,6 +103,12 @@ struct DecodeParams {
   unsigned* err;
   unsigned long long timeout_ns;
 };
+
+// Backward workspace layout: per padded row (B*H*ceil(N/128)*128 rows) lse2 and D, 8 bytes, and
+// at d = 64 their two 32-byte operand rows; then the work counters (1 + B*H words), rounded up
+// to 16 bytes.
+inline size_t bwd_row_workspace_bytes(int d) { return 2 * sizeof(float) + (d == 64 ? 64 : 0); }
+inline size_t bwd_counter_bytes(size_t BH) { return ((1 + BH) * sizeof(unsigned) + 15) / 16 * 16; }
 
 // Argument checks shared by the backward entry points (fa_bwd, fa_bwd_blocksparse,
 // fa_bwd_noalloc), so that all of them report the same status for the same bad argument: null

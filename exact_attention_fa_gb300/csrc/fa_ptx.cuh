@@ -14,7 +14,7 @@ namespace fa {
 // ------------------------------------------------------------------------------------------
 // Bits of the device error word (the host reads and clears it through fa_check_device_error).
 enum : unsigned {
-  kErrTimeout = 1u,      // an mbarrier wait gave up
+  kErrTimeout = 1u,      // a bounded wait (mbarrier or counter) gave up
   kErrSmemAlign = 2u,    // dynamic shared memory not 1024-byte aligned
 };
 
@@ -243,6 +243,28 @@ __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
 // tensor cores).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Bounded wait until the 32-bit counter at ctr reaches at least want (the counter only grows
+// while the wait lasts). Polls with acquire loads at gpu scope; gives up like mbar_wait.
+__device__ __forceinline__ bool wait_counter_geq(const unsigned* ctr, unsigned want,
+                                                 const Ctl& ctl) {
+  auto load = [&]() {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    return v;
+  };
+  if (load() >= want) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    __nanosleep(256);
+    if (load() >= want) return true;
+    if (*ctl.abort_flag) return false;
+    if (globaltimer() - t0 > ctl.timeout_ns) {
+      raise_error(ctl, kErrTimeout);
+      return false;
+    }
+  }
 }
 
 // ------------------------------------------------------------------------------------------

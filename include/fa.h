@@ -115,9 +115,10 @@ int fa_set_exp2_emulation(int per32);
 /* The current per32 setting of fa_set_exp2_emulation (0 or 4). */
 int fa_get_exp2_emulation(void);
 
-/* Bytes of device workspace fa_bwd needs, per row of B*H*ceil(N/128)*128 rows (rows padded to
- * whole 128-row tiles): two fp32 row statistics (8 bytes) and, at d = 64, two 32-byte bf16
- * operand rows made from them (72 bytes in all). 0 for B, H, N < 1 or d not in {64, 128}. */
+/* Bytes of device workspace fa_bwd needs: per row of B*H*ceil(N/128)*128 rows (rows padded to
+ * whole 128-row tiles) two fp32 row statistics (8 bytes) and, at d = 64, two 32-byte bf16
+ * operand rows made from them (72 bytes in all); then 4 * (1 + B*H) bytes of work counters,
+ * rounded up to a multiple of 16. 0 for B, H, N < 1 or d not in {64, 128}. */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
 /* Backward by recomputation ("3 · FlashAttention", 3.4; "FlashAttention：在线 softmax 与
@@ -154,8 +155,8 @@ int fa_bwd_blocksparse(const void* q, const void* k, const void* v, const void* 
  * library's module is loaded on it until the process exits. fa_bwd's argument checks run first,
  * in its order (so a bad argument gets the same status from both); then problems whose
  * fa_bwd_workspace_bytes(B, H, N, d) exceeds the array are rejected with FA_ERR_SCRATCH_LIMIT,
- * before anything is enqueued. 4 MiB covers B*H*ceil(N/128)*128 <= 58240 rows at d = 64 and
- * <= 524288 rows at d = 128.
+ * before anything is enqueued. With B = H = 1, 4 MiB covers N up to 58240 at d = 64 and up to
+ * 524160 at d = 128.
  * Allocates nothing: no cudaMalloc/cudaFree or allocating library call. The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress, with that device current);
  * make that first call before any stream capture. All calls on a device share the one array and
@@ -212,7 +213,8 @@ const char* fa_status_string(int status);
  * fa_decode; minor 2: fa_bwd_blocksparse; minor 3: fa_fwd_fp32_fa1; minor 4:
  * fa_bwd_workspace_bytes depends on d (8 bytes per row at d = 128); minor 5: fa_fwd_fp8;
  * minor 6: fa_set_exp2_emulation, fa_get_exp2_emulation; minor 7: fa_decode on the tensor cores,
- * fa_decode_workspace_bytes counted with its blocks. */
+ * fa_decode_workspace_bytes counted with its blocks; minor 8: fa_bwd_workspace_bytes adds the
+ * work counters of the backward kernel (4 * (1 + B*H) bytes, rounded up to 16). */
 int fa_abi_version(void);
 
 #ifdef __cplusplus

@@ -128,8 +128,10 @@ def test_fp32_validation(lib):
 
 def test_bwd_validation_and_workspace(lib):
     # per padded row: lse2 and D (fp32), and at d = 64 their two 32-byte bf16 operand rows
-    assert lib.fa_bwd_workspace_bytes(2, 3, 100, 64) == 2 * 3 * 128 * 72
-    assert lib.fa_bwd_workspace_bytes(1, 1, 256, 128) == 256 * 8
+    # rows x (8 or 72 bytes), then 4 * (1 + B*H) bytes of counters rounded up to 16
+    assert lib.fa_bwd_workspace_bytes(2, 3, 100, 64) == 2 * 3 * 128 * 72 + 32
+    assert lib.fa_bwd_workspace_bytes(1, 1, 256, 128) == 256 * 8 + 16
+    assert lib.fa_bwd_workspace_bytes(4, 16, 4096, 128) == 64 * 4096 * 8 + 272
     assert lib.fa_bwd_workspace_bytes(0, 3, 100, 64) == 0
     assert lib.fa_bwd_workspace_bytes(1, 1, 256, 96) == 0
     ptrs = [fake()] * 9
@@ -177,14 +179,15 @@ def test_bwd_noalloc_reports_fa_bwds_status(lib, case):
 
 def test_bwd_noalloc_scratch_limit_after_argument_checks(lib):
     ptrs = [fake()] * 9
-    # 4 MiB: 58240 padded rows at d = 64 (72 bytes each), 524288 at d = 128 (8 bytes each)
+    # 4 MiB: 58240 padded rows at d = 64 (72 bytes each), 524160 at d = 128 (8 bytes each), plus
+    # 16 bytes of counters
     assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 58241, 64, 0.125, 0, None) == 8
-    assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 524289, 128, 0.125, 0, None) == 8
+    assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 524161, 128, 0.125, 0, None) == 8
     # within the limit the call goes on to the device, which this machine does not have
     import torch
     if not torch.cuda.is_available():
         assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 58240, 64, 0.125, 0, None) == 6
-        assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 524288, 128, 0.125, 0, None) == 6
+        assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 524160, 128, 0.125, 0, None) == 6
 
 
 def test_fp8_validation(lib):

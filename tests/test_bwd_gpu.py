@@ -129,3 +129,41 @@ def test_bwd_repeatable_within_tolerance(cuda):
     b = fa.attention_backward(q, k, v, o, lse, do, w.softmax_scale, causal=True)
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
     assert torch.allclose(a[0], b[0], rtol=0, atol=1e-5)
+
+
+@pytest.mark.parametrize("d,N,Hh,sparse", [
+    (128, 4096, 10, False),  # causal; heads in groups of 8: 8 + 2
+    (128, 4096, 10, True),
+    (64, 2048, 40, True),    # groups of 32: 32 + 8
+])
+def test_bwd_zeroes_dq_whatever_the_buffers_held(cuda, d, N, Hh, sparse):
+    """The backward zeroes dQ itself (the first head group's rows in the prep kernel, each later
+    group's rows in the main kernel, by the CTAs of the group before) and resets its work
+    counters: with dq, dk, dv full of NaN and the workspace full of 0xff bytes beforehand, the
+    result is that of fresh buffers, and a query tile that visits no key tile gets dQ = 0."""
+    T = (N + 127) // 128
+    m = np.ones((T, T), np.uint8)
+    m[1, :] = 0  # query tile 1 visits no key tile
+    w = wl.Workload("bwd_garbage", 1, Hh, N, d, causal=not sparse, block_sparse=sparse, seed=74)
+    inp = wl.make_inputs(w, with_do=True)
+    q, k, v, do = (H.to_device(inp, n, cuda) for n in ("q", "k", "v", "do"))
+    mt = torch.from_numpy(m).to(cuda) if sparse else None
+    o, lse = fa.attention_forward(q, k, v, w.softmax_scale, causal=w.causal, block_mask=mt)
+    ref = fa.attention_backward(q, k, v, o, lse, do, w.softmax_scale, causal=w.causal,
+                                block_mask=mt)
+    dq = torch.full(q.shape, float("nan"), dtype=torch.float32, device=cuda)
+    dk = torch.full_like(k, float("nan"))
+    dv = torch.full_like(v, float("nan"))
+    ws = torch.full((max(16, fa.fa_bwd_workspace_bytes(1, Hh, N, d)),), 255, dtype=torch.uint8,
+                    device=cuda)
+    if sparse:
+        fa.fa_bwd_blocksparse(q, k, v, o, do, lse, dq, dk, dv, w.softmax_scale, False, mt, ws)
+    else:
+        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, w.softmax_scale, True, ws)
+    fa.fa_check_device_error()
+    assert torch.all(torch.isfinite(dq))
+    if sparse:
+        assert torch.all(dq[:, :, 128:256] == 0)
+    err = (torch.linalg.vector_norm(dq - ref[0]) / torch.linalg.vector_norm(ref[0])).item()
+    assert err <= 1e-5, err
+    assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
