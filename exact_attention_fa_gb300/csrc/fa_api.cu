@@ -375,7 +375,7 @@ int fwd_fp32(const float* q, const float* k, const float* v, float* o, float* ls
   if ((st = device_state(&ds)) != FA_OK) return st;
   fa::Fp32FwdParams p{q, k, v, o, lse, B * H, N, d, causal ? 1 : 0,
                       scale * 1.4426950408889634f, fa1 ? 1 : 0};
-  return to_status(fa::launch_fwd_fp32(p, reinterpret_cast<cudaStream_t>(stream)));
+  return to_status(fa::launch_fwd_fp32(p, ds->num_sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 }  // namespace
 

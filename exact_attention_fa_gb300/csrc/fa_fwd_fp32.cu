@@ -1,8 +1,9 @@
 // fp32 forward: tiled online softmax on the FMA pipes, for fp32 inputs where a bf16/tf32 tensor-
 // core product would miss a 1e-5 accuracy bar.
 //
-// A CTA owns kRows consecutive query rows of one (b, h), one warp per row. Key/value blocks of
-// 32 rows are staged in shared memory and shared by the CTA's warps. Lane j scores key j of the
+// A CTA owns R consecutive query rows of one (b, h), one warp per row (R = 8; 2 or 4 when a grid
+// of 8-row CTAs would leave SMs idle, so that small problems spread over more SMs). Key/value
+// blocks of 32 rows are staged in shared memory and shared by the CTA's warps. Lane j scores key j of the
 // block (a d-long dot product from shared memory); the warp then applies the online-softmax
 // update of "FlashAttention：メモリ効率的なアテンション計算", section "オンライン softmax":
 //   m_new = max(m, block max),  alpha = exp(m - m_new),  l = l*alpha + sum p,  o = o*alpha + sum p v
@@ -26,12 +27,11 @@
 namespace fa {
 namespace {
 
-constexpr int kRows = 8;   // query rows (warps) per CTA
 constexpr int kKeys = 32;  // keys per shared-memory block
-constexpr int kThreads = kRows * 32;
 
-template <int D, bool kFA1>
+template <int D, bool kFA1, int kRows>
 __global__ void __launch_bounds__(kRows * 32) fwd_fp32_kernel(const Fp32FwdParams p) {
+  constexpr int kThreads = kRows * 32;
   constexpr int C = D / 32;
   __shared__ float ks[kKeys][D + 1];  // +1: lane j reads row j without bank conflicts
   __shared__ __align__(16) float vs[kKeys][D];
@@ -59,7 +59,8 @@ __global__ void __launch_bounds__(kRows * 32) fwd_fp32_kernel(const Fp32FwdParam
   // A key/value block is kKeys x D floats of each; thread t holds float4 number t + u * kThreads
   // of both. The next block's loads are issued before this block's arithmetic, so the latency of
   // global memory overlaps the work instead of adding to it once per block.
-  constexpr int kVec = kKeys * D / 4 / kThreads;  // D / 32
+  constexpr int kVec = kKeys * D / 4 / kThreads;  // D * 8 / kThreads
+  static_assert(kVec * kThreads * 4 == kKeys * D, "a block is a whole number of float4 per thread");
   float4 kr[kVec], vr[kVec];
   auto fetch = [&](int kb) {
 #pragma unroll
@@ -165,21 +166,34 @@ __global__ void __launch_bounds__(kRows * 32) fwd_fp32_kernel(const Fp32FwdParam
   }
 }
 
+template <int D, bool F, int R>
+cudaError_t launch_rows(const Fp32FwdParams& p, cudaStream_t s) {
+  fwd_fp32_kernel<D, F, R><<<dim3((p.N + R - 1) / R, p.BH), R * 32, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D, bool F>
+cudaError_t launch_d(const Fp32FwdParams& p, int num_sms, cudaStream_t s) {
+  // 8 rows per CTA unless that grid leaves SMs idle; then 2 (4 at d > 64, where a block's
+  // prefetch registers per thread would double again)
+  constexpr int kSmall = D <= 64 ? 2 : 4;
+  const long long ctas8 = static_cast<long long>((p.N + 7) / 8) * p.BH;
+  if (ctas8 < num_sms) return launch_rows<D, F, kSmall>(p, s);
+  return launch_rows<D, F, 8>(p, s);
+}
+
 }  // namespace
 
-cudaError_t launch_fwd_fp32(const Fp32FwdParams& p, cudaStream_t s) {
-  const dim3 grid((p.N + kRows - 1) / kRows, p.BH);
-  const dim3 block(kRows * 32);
+cudaError_t launch_fwd_fp32(const Fp32FwdParams& p, int num_sms, cudaStream_t s) {
   auto go = [&](auto fa1) {
     constexpr bool F = decltype(fa1)::value;
     switch (p.d) {
-      case 32: fwd_fp32_kernel<32, F><<<grid, block, 0, s>>>(p); break;
-      case 64: fwd_fp32_kernel<64, F><<<grid, block, 0, s>>>(p); break;
-      case 96: fwd_fp32_kernel<96, F><<<grid, block, 0, s>>>(p); break;
-      case 128: fwd_fp32_kernel<128, F><<<grid, block, 0, s>>>(p); break;
+      case 32: return launch_d<32, F>(p, num_sms, s);
+      case 64: return launch_d<64, F>(p, num_sms, s);
+      case 96: return launch_d<96, F>(p, num_sms, s);
+      case 128: return launch_d<128, F>(p, num_sms, s);
       default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
   };
   return p.fa1 ? go(std::true_type{}) : go(std::false_type{});
 }

@@ -128,7 +128,7 @@ constexpr int kExp2EmulationPer32 = 4;
 cudaError_t launch_fwd_pair(const FwdParams& p, int d, cudaStream_t s);               // 2 tiles/CTA
 // The same kernel on e4m3 Q, K, V at d = 128 (tm_q, tm_k, tm_v: 8-bit maps, box 128 x 128 x 1).
 cudaError_t launch_fwd_fp8(const FwdParams& p, cudaStream_t s);
-cudaError_t launch_fwd_fp32(const Fp32FwdParams& p, cudaStream_t s);
+cudaError_t launch_fwd_fp32(const Fp32FwdParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t s);
 // Decoding: the split kernel on the tensor cores (tensor maps in p), then the merge of the pieces.
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t s);

@@ -97,6 +97,17 @@ def run_fa1(w: wl.Workload, device):
     return worst
 
 
+@pytest.mark.parametrize("d", [32, 64, 96, 128])
+@pytest.mark.parametrize("B,Hh,N", [(1, 1, 700), (2, 16, 300)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp32_rows_per_cta(cuda, d, B, Hh, N, causal):
+    """The fp32 kernel takes 8 query rows per CTA, or 2 (4 at d > 64) when a grid of 8-row CTAs
+    would leave SMs idle: B1 H1 N700 takes the small form over 22 key blocks, B2 H16 N300 the
+    8-row form; every row against the oracle."""
+    w = wl.Workload("fp32_rows", B, Hh, N, d, dtype="fp32", causal=causal, seed=14)
+    run_and_compare(w, cuda)
+
+
 def test_single_head_fp32_fa1_form(cuda):
     assert run_fa1(wl.WORKLOADS["single_head_fp32"], cuda) < 1e-6
 
