@@ -345,8 +345,15 @@ class ClockSampler:
 
 def forward_kernel_name(w):
     """Name of the forward kernel the library runs for this workload (the two-query-tile kernel
-    for every bf16 and e4m3 forward)."""
+    for every bf16 and e4m3 forward). fp32: small problems at d <= 96 (8-row CTAs would leave SMs
+    idle, and a CTA's whole key range fits in 200 KB of shared memory) take the kernel that stages
+    all keys at once; the rest the key-block kernel."""
     if w.dtype == "fp32":
+        import torch
+        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        smem = 4 * (w.N * (w.d + 4) + w.N * w.d + 2 * w.d + 16 * (w.d + 2))
+        if (w.N + 7) // 8 * w.B * w.H < sms and w.d <= 96 and smem <= 200 * 1024:
+            return f"fwd_fp32_small_kernel<{w.d}>"
         return f"fwd_fp32_kernel<{w.d}>"
     if w.dtype == "e4m3":
         return f"fwd_pair_kernel<{w.d}, true>"

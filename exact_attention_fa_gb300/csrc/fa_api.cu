@@ -61,7 +61,7 @@ int device_state(DeviceState** out) {
     }
     if (st.status == FA_OK) {
       if (fa::configure_fwd_pair() != cudaSuccess || fa::configure_bwd() != cudaSuccess ||
-          fa::configure_decode() != cudaSuccess) {
+          fa::configure_decode() != cudaSuccess || fa::configure_fwd_fp32() != cudaSuccess) {
         cudaGetLastError();
         st.status = FA_ERR_CUDA;
       }

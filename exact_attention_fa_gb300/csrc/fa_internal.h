@@ -137,5 +137,6 @@ cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t s);
 cudaError_t configure_fwd_pair();
 cudaError_t configure_bwd();
 cudaError_t configure_decode();
+cudaError_t configure_fwd_fp32();
 
 }  // namespace fa

@@ -108,6 +108,16 @@ def test_fp32_rows_per_cta(cuda, d, B, Hh, N, causal):
     run_and_compare(w, cuda)
 
 
+@pytest.mark.parametrize("d,N", [(32, 740), (64, 375), (96, 250), (64, 40)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp32_small_problem_kernel(cuda, d, N, causal):
+    """Small fp32 problems at d <= 96 stage the whole key range in shared memory and split each
+    row's keys over 8 warps, merged with the softmax statistics: these sizes are the largest that
+    fit (up to 3 blocks of 32 keys per warp) and one where most warps get no key at all."""
+    w = wl.Workload("fp32_smem", 1, 1, N, d, dtype="fp32", causal=causal, seed=15)
+    run_and_compare(w, cuda)
+
+
 def test_single_head_fp32_fa1_form(cuda):
     assert run_fa1(wl.WORKLOADS["single_head_fp32"], cuda) < 1e-6
 
