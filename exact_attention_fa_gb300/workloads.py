@@ -154,7 +154,7 @@ WORKLOADS = {
     "decode_N32768_d128": Workload("decode_N32768_d128", 8, 32, 32768, 128, nq=1, seed=6),
     # the same per-head problem on 8 heads (134 MB of K, V: larger than L2, small enough for ncu)
     "decode_N32768_d128_h8": Workload("decode_N32768_d128_h8", 1, 8, 32768, 128, nq=1, seed=7),
-    # the same at d = 64 (64-key blocks), and its profile case on 16 heads (134 MB of K, V)
+    # the same at d = 64 (256-key blocks), and its profile case on 16 heads (134 MB of K, V)
     "decode_N32768_d64": Workload("decode_N32768_d64", 8, 32, 32768, 64, nq=1, seed=8),
     "decode_N32768_d64_h16": Workload("decode_N32768_d64_h16", 1, 16, 32768, 64, nq=1, seed=9),
     # the long-sequence causal forward's per-head problem on 8 heads, at N = 8192 and N = 4096
@@ -179,6 +179,12 @@ WORKLOADS["decode_N32768_d64_q8"] = Workload("decode_N32768_d64_q8", 8, 32, 3276
 # default bench line.
 WORKLOADS["decode_N32768_d128_q8_b2"] = Workload("decode_N32768_d128_q8_b2", 2, 32, 32768, 128,
                                                  nq=8, seed=17)
+
+# Decoding with serving-sized caches: one new row per head against 4096 cached keys, for a
+# batch of 8 (K, V 537 MB) and of 1 (67 MB: launch and ramp weigh most).
+WORKLOADS["decode_N4096_d128"] = Workload("decode_N4096_d128", 8, 32, 4096, 128, nq=1, seed=18)
+WORKLOADS["decode_N4096_d128_b1"] = Workload("decode_N4096_d128_b1", 1, 32, 4096, 128, nq=1,
+                                             seed=19)
 
 # Counter-capture cases of the e4m3 forward and of the backward on 8 heads (small device footprint).
 WORKLOADS["causal_N4096_d128_fp8_h8"] = Workload("causal_N4096_d128_fp8_h8", 1, 8, 4096, 128,
