@@ -34,10 +34,13 @@ __device__ __forceinline__ int cta_of_block(long long g, long long T, int G) {
 // One CTA of D threads per (head, query row): merges the pieces of the CTAs whose block ranges
 // cover the head (lse = log2 Σ 2^lse_c, O = Σ 2^(lse_c - lse) O_c). The pieces' weights are
 // formed in parallel in shared memory, so the loop over pieces issues independent loads.
+// It is launched as a programmatic dependent of the split kernel (the launch overlaps the split
+// kernel's tail) and waits here until that grid has completed and its pieces are visible.
 template <int D>
 __global__ void __launch_bounds__(D) decode_merge_kernel(const __grid_constant__ DecodeParams p) {
   __shared__ float wts[kDecodeMaxCtas];
   __shared__ float red[D / 32];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int row = blockIdx.x;  // h * Nq + i
   const int h = row / p.Nq, i = row - h * p.Nq;
   const int t = threadIdx.x, lane = t % 32, warp = t / 32;
@@ -172,6 +175,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
   const Ctl ctl{abort_flag, p.err, p.timeout_ns};
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // the merge kernel may be scheduled as soon as every CTA of this grid has started (it waits
+  // for this grid's completion before it reads anything)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const long long T = static_cast<long long>(p.BH) * p.blocks_per_head;
   const int G = gridDim.x, c = blockIdx.x;
@@ -483,8 +489,18 @@ cudaError_t launch_tc(const DecodeParams& p_in, cudaStream_t s) {
   decode_tc_kernel<D><<<p.n_ctas, kTcThreads, TcCfg<D>::kSmemBytes, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_merge_kernel<D><<<static_cast<unsigned>(p.BH) * p.Nq, D, 0, s>>>(p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the merge kernel's launch overlaps the split kernel's tail
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.BH) * p.Nq);
+  cfg.blockDim = dim3(D);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, p);
 }
 }  // namespace
 
