@@ -770,7 +770,7 @@ def decode_entry(w, inp, fa, dev, flush_buf, steps, warmup, world, local, cpu=No
     peaks, peak_src = load_peaks()
     peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     achieved = algo_bytes / (t * 1e-3) / 1e9
-    kname = f"decode_tc_kernel<{w.d}> (+ decode_merge_kernel<{w.d}>)"
+    kname = f"decode_kt_kernel<{w.d}> (+ decode_merge_kernel<{w.d}>)"
     return {"config": {**config_of(w, world), "n_ctas": n_ctas}, "ms_per_step": t, "steps": n,
             "gbs": world * achieved,
             "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
@@ -864,7 +864,7 @@ def run_decode(args, w, fa, inp, cpu, world, rank, local, dev, flush_buf):
     peaks, peak_src = load_peaks()
     peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     achieved = algo_bytes / (t_step * 1e-3) / 1e9
-    kname = f"decode_tc_kernel<{w.d}> (+ decode_merge_kernel<{w.d}>)"
+    kname = f"decode_kt_kernel<{w.d}> (+ decode_merge_kernel<{w.d}>)"
     line = {
         "metric": metric_name(w), "value": world * achieved, "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True,

@@ -455,8 +455,10 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.scale_log2 = scale * 1.4426950408889634f;
   p.err = ds->err;
   p.timeout_ns = kWaitTimeoutNs;
-  // rows past Nq of the 128-row Q tile and keys past Nk read as zero through the tensor maps
-  if (!encode_bf16_map(&p.tm_q, q, BH, Nq, d) || !encode_bf16_map(&p.tm_k, k, BH, Nk, d) ||
+  // rows past Nq of the Q tile (16 rows at d = 128, 128 at d = 64) and keys past Nk read as zero
+  // through the tensor maps
+  if (!encode_bf16_map(&p.tm_q, q, BH, Nq, d, 16) ||
+      !encode_bf16_map(&p.tm_k, k, BH, Nk, d) ||
       !encode_bf16_map(&p.tm_v, v, BH, Nk, d))
     return FA_ERR_CUDA;
   return to_status(fa::launch_decode(p, d, reinterpret_cast<cudaStream_t>(stream)));

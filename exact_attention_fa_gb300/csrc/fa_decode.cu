@@ -10,10 +10,11 @@
 // merges the pieces of each head with the same statistics merge as the blockwise forward
 // (lse = log sum_c exp lse_c, O = sum_c exp(lse_c - lse) O_c).
 //
-// The products run on the tensor cores (decode_tc_kernel below). A CUDA-core kernel (lane = key
+// The products run on the tensor cores (decode_kt_kernel below). A CUDA-core kernel (lane = key
 // for the scores, lane = output columns for P V) did 2 Nq d FMAs per key against 4 d bytes of K
 // and V: it reached 6091 GB/s (d = 128) and 6177 (d = 64) with one query row but only 1132 with
-// eight; the tensor-core kernel streams 6977 / 6556 GB/s with one row and 7061 / 6508 with eight.
+// eight; the tensor-core kernel streams about 7060 / 6650 GB/s with one row and 7030 / 6570
+// with eight.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -87,69 +88,6 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(const __grid_constant__
   if (t == 0) p.lse[row] = (mx + __log2f(den)) * kLn2;
 }
 
-// ---------------------------------------------------------------------------------------------
-// The decoding kernel. Each key block is a small forward tile: S = Q K^T and O += P V as
-// tcgen05.mma with Q zero-padded to a 128-row tile by the TMA (rows past Nq read as zero), so the
-// tensor core does 128 / Nq times the useful work but still needs far less time per block than
-// HBM needs to deliver the block's K and V.
-//   * the stretch of one head inside a CTA's range is a segment;
-//   * warp 1 loads Q of each segment and the (K, V) blocks with TMA into a ring;
-//   * warp 2 issues the MMAs: S of the next block as soon as the softmax has read this one (two
-//     TMEM buffers at d = 128, one of 256 keys at d = 64), then P V into the segment's O;
-//   * warps 0 and 4 are the softmax (both reach TMEM lanes 0-31): thread r of each owns query row
-//     r (rows >= Nq carry zeros and are never stored), warp 0 the first half of a block's keys and
-//     warp 4 the second; they exchange the block's row max through shared memory, so both use one reference
-//     max, and each keeps its own part of the running sum. Online softmax as in the forward, P as
-//     bf16 into TMEM; at the end of a segment O / l and the log-sum-exp are written as the piece
-//     (CTA, head), merged per head by decode_merge_kernel.
-// Blocks of 256 keys at d = 64 and 128 at d = 128: 32 KB of K and of V per block either way, so
-// that the per-block costs (barrier round trips, MMA issue) weigh the same per byte.
-// TMEM columns: d = 128: S_0 [0, 128), S_1 [128, 256), P [256, 320), O [320, 448); d = 64:
-// S [0, 256), P [256, 384), O [384, 448).
-template <int D>
-struct TcCfg {
-  static constexpr int kBK = decode_tc_block_keys(D);  // 32 KB of K and of V per block
-  static constexpr int kHalfKeys = kBK / 2;            // keys per softmax warp
-  static constexpr int kQTile = 128 * D * 2;           // the Q tile (bf16)
-  static constexpr int kKV = kBK * D * 2;              // a K or a V block
-  static constexpr int kBox = 128 * 64 * 2;            // one TMA box: 128 rows x 64 columns
-  static constexpr int kRowBoxes = kBK / 128;          // boxes along the keys of a block
-  static constexpr int kColBoxes = D / 64;             // boxes along d
-  static constexpr int kStages = 3;                    // (K, V) pairs in flight: 192 KB
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffRing = kQTile;
-  static constexpr int kOffBar = kOffRing + kStages * 2 * kKV;
-  // d = 128: two S buffers of 128 columns; d = 64: one of 256 (S of the next block is still
-  // issued as soon as both softmax warps have read this one)
-  static constexpr int kSBufs = D == 64 ? 1 : 2;
-  // barriers: full[S], empty[S], q_full, q_empty, s_full[2], s_free[2], p_full, pv_done, o_done,
-  // o_free, drain
-  static constexpr int kBarFull = 0;
-  static constexpr int kBarEmpty = kStages;
-  static constexpr int kBarQFull = 2 * kStages;
-  static constexpr int kBarQEmpty = kBarQFull + 1;
-  static constexpr int kBarSFull = kBarQFull + 2;
-  static constexpr int kBarSFree = kBarSFull + 2;
-  static constexpr int kBarPFull = kBarSFree + 2;
-  static constexpr int kBarPVDone = kBarPFull + 1;
-  static constexpr int kBarODone = kBarPVDone + 1;
-  static constexpr int kBarOFree = kBarODone + 1;
-  static constexpr int kBarDrain = kBarOFree + 1;
-  static constexpr int kBarX = kBarDrain + 1;  // [2] the softmax warps' row maxima, per parity
-  static constexpr int kBarL = kBarX + 2;      // their running sums at the end of a segment
-  static constexpr int kNumBars = kBarL + 1;
-  // the two softmax warps' row maxima per block parity and their running sums: [2][2][32] + [2][32]
-  static constexpr int kOffX = kOffBar + 8 * kNumBars;
-  static constexpr int kOffTmemPtr = kOffX + (2 * 2 * 32 + 2 * 32) * 4;
-  static constexpr int kOffAbort = kOffTmemPtr + 4;
-  static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1 KB
-  static constexpr uint32_t kColS = 0;
-  static constexpr uint32_t kColP = kSBufs * kBK;    // kBK / 2 columns of bf16 pairs
-  static constexpr uint32_t kColO = kColP + kBK / 2;  // D columns; at most 448 in all
-  static_assert(kColO + D <= 512, "TMEM columns");
-};
-constexpr int kTcThreads = 160;  // warps: 0 and 4 softmax, 1 TMA, 2 MMA, 3 idle
-
 // The CTA's range [g0, g0 + nblk) of global block indices (head-major) and the segment of head h
 // inside it.
 struct TcRange {
@@ -163,9 +101,74 @@ struct TcRange {
   }
 };
 
+// ---------------------------------------------------------------------------------------------
+// The decoding kernel: each key block's two products on the tensor cores, with the keys on the
+// TMEM lanes:
+//     S^T = K Q^T    (M = 128 keys, N = 16 query columns: Q zero-padded by the TMA)
+//     O^T += V^T P^T (M = 128: the d columns of O, N = 16, K = the block's keys; P^T from shared
+//                     memory)
+// so that thread t of the four softmax warps (warp t / 32 reaches TMEM lanes 32 (t / 32) ...)
+// owns key t of each 128-key row box: one exponential per useful query row, spread over all four
+// SM sub-partitions. (With the query rows on the lanes instead, every exponential fell on the one
+// sub-partition whose warps reach lanes 0-31, one instruction per key whatever Nq; measured on
+// the same shapes the transposed form streams 0.7-2% more and calls with few blocks per CTA run 8%
+// faster.) The block's max per query is a shuffle reduction in each warp and a bounded exchange
+// between the four warps; each thread keeps its own part of the running sums; at the end of a
+// segment thread t reads row t of O^T, i.e. column d = t of the piece.
+//   * the stretch of one head inside a CTA's range is a segment;
+//   * warp 4 loads Q of each segment and the (K, V) blocks with TMA into a ring;
+//   * warp 5 issues the MMAs: S^T of the next block as soon as the softmax has read this one (two
+//     TMEM buffers), then O^T of this block once P^T is in shared memory;
+//   * warps 0-3 are the softmax, conditional rescaling as in the forward.
+// A block is 32 KB of K and 32 KB of V at either head dimension (128 keys at d = 128, two row
+// boxes of 128 keys at d = 64), so that the per-block costs weigh the same per byte. At d = 64
+// the 128-row A operand V^T has only 64 rows: its second 64-row half aliases the first (box
+// stride 0), and rows 64-127 of O^T repeat rows 0-63, unread.
+// TMEM columns: S^T buffer sb, row box rb at (sb * kRB + rb) * 16; O^T after them (16 columns).
 template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_constant__ DecodeParams p) {
-  using C = TcCfg<D>;
+struct KtCfg {
+  // a block is kRB row boxes of 128 keys (TMEM lanes of S^T): 32 KB of K and of V either way
+  static constexpr int kRB = D == 64 ? 2 : 1;
+  static constexpr int kBK = 128 * kRB;            // keys per block
+  static_assert(kBK == decode_tc_block_keys(D), "the pieces' layout follows the block size");
+  static constexpr int kNP = 16;                   // query columns of S^T, O^T (Nq <= 8)
+  static constexpr int kKV = kBK * D * 2;          // a K or a V block: 32 KB
+  static constexpr int kBox = 128 * 128;           // a 128-row, 64-column box of it: 16 KB
+  static constexpr int kColBoxes = D / 64;         // boxes of row box rb at (rb * kColBoxes + b)
+  static constexpr int kSmallBox = kNP * 128;      // a 64-column box of 16 rows: 2 KB
+  static constexpr int kSteps = D / 16;            // K-steps of S^T
+  static constexpr int kStages = 3;                // 192 KB of K and V in flight
+  static constexpr int kOffRing = 0;
+  static constexpr int kOffQ = kStages * 2 * kKV;                 // Q: 16 rows, D / 64 boxes
+  static constexpr int kOffP = kOffQ + kColBoxes * kSmallBox;      // P^T: 16 rows x kBK keys
+  static constexpr int kOffBar = kOffP + 2 * kRB * kSmallBox;
+  static constexpr int kBarFull = 0;
+  static constexpr int kBarEmpty = kStages;
+  static constexpr int kBarQFull = 2 * kStages;
+  static constexpr int kBarQEmpty = kBarQFull + 1;
+  static constexpr int kBarSFull = kBarQFull + 2;  // [2]
+  static constexpr int kBarSFree = kBarSFull + 2;  // [2]
+  static constexpr int kBarPFull = kBarSFree + 2;
+  static constexpr int kBarPVDone = kBarPFull + 1;
+  static constexpr int kBarODone = kBarPVDone + 1;
+  static constexpr int kBarOFree = kBarODone + 1;
+  static constexpr int kBarDrain = kBarOFree + 1;
+  static constexpr int kBarX = kBarDrain + 1;  // [2] the warps' block maxima, per block parity
+  static constexpr int kBarL = kBarX + 2;      // their running sums at the end of a segment
+  static constexpr int kNumBars = kBarL + 1;
+  static constexpr int kOffX = kOffBar + 8 * kNumBars;  // [2][4][8] maxima, then [4][8] sums
+  static constexpr int kOffTmemPtr = kOffX + (2 * 4 * 8 + 4 * 8) * 4;
+  static constexpr int kOffAbort = kOffTmemPtr + 4;
+  static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1 KB
+  // S^T buffer sb, row box rb at kColS + (sb * kRB + rb) * kNP
+  static constexpr uint32_t kColS = 0, kColO = 2 * kRB * kNP;
+  static constexpr uint32_t kTmemCols = kColO + kNP <= 64 ? 64 : 128;
+};
+constexpr int kKtThreads = 192;  // warps: 0-3 softmax (thread = key), 4 TMA, 5 MMA
+
+template <int D>
+__global__ void __launch_bounds__(kKtThreads, 1) decode_kt_kernel(const __grid_constant__ DecodeParams p) {
+  using C = KtCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -175,8 +178,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
   const Ctl ctl{abort_flag, p.err, p.timeout_ns};
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // the merge kernel may be scheduled as soon as every CTA of this grid has started (it waits
-  // for this grid's completion before it reads anything)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const long long T = static_cast<long long>(p.BH) * p.blocks_per_head;
@@ -196,20 +197,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
     mbar_init(bar(C::kBarQEmpty), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(C::kBarSFull + b), 1);
-      mbar_init(bar(C::kBarSFree + b), 64);
+      mbar_init(bar(C::kBarSFree + b), 128);
+      mbar_init(bar(C::kBarX + b), 128);
     }
-    mbar_init(bar(C::kBarPFull), 64);
+    mbar_init(bar(C::kBarPFull), 128);
     mbar_init(bar(C::kBarPVDone), 1);
     mbar_init(bar(C::kBarODone), 1);
-    mbar_init(bar(C::kBarOFree), 64);
+    mbar_init(bar(C::kBarOFree), 128);
     mbar_init(bar(C::kBarDrain), 1);
-    mbar_init(bar(C::kBarX + 0), 64);
-    mbar_init(bar(C::kBarX + 1), 64);
-    mbar_init(bar(C::kBarL), 64);
+    mbar_init(bar(C::kBarL), 128);
     fence_barrier_init();
   }
-  if (warp == 2) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 1) {
+  if (warp == 4) {
     // ------------------------------------------------------------------- TMA (whole warp)
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
@@ -228,20 +228,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
       const int h = rg.head(rg.g0 + i);
       const int e = rg.seg_end(i);
       if (seg > 0 && !(ok = mbar_wait_warp(bar(C::kBarQEmpty), (seg - 1) & 1, ctl))) break;
-      mbar_arrive_expect_tx(bar(C::kBarQFull), C::kQTile);
+      mbar_arrive_expect_tx(bar(C::kBarQFull), C::kColBoxes * C::kSmallBox);
       for (int b = 0; b < C::kColBoxes; ++b)
-        tma_load_3d(sbase + C::kOffQ + b * C::kBox, &p.tm_q, bar(C::kBarQFull), b * 64, 0, h);
+        tma_load_3d(sbase + C::kOffQ + b * C::kSmallBox, &p.tm_q, bar(C::kBarQFull), b * 64, 0, h);
       for (; i < e; ++i) {
         const int st = i % C::kStages, round = i / C::kStages;
         if (!(ok = mbar_wait_warp(bar(C::kBarEmpty + st), (round & 1) ^ 1, ctl))) break;
         const int jb = static_cast<int>((rg.g0 + i) % rg.nb);
         const uint32_t dst = sbase + C::kOffRing + st * 2 * C::kKV;
         mbar_arrive_expect_tx(bar(C::kBarFull + st), 2 * C::kKV);
-        // column box b (64 of d) at b * kBK * 128 bytes, row box rb (128 keys) at rb * 16 KB
-        // inside it: the 128-byte-swizzled layout of the whole kBK x D tile
-        for (int rb = 0; rb < C::kRowBoxes; ++rb)
+        for (int rb = 0; rb < C::kRB; ++rb)
           for (int b = 0; b < C::kColBoxes; ++b) {
-            const uint32_t off = b * C::kBK * 128 + rb * C::kBox;
+            const uint32_t off = (rb * C::kColBoxes + b) * C::kBox;
             const int row = jb * C::kBK + rb * 128;
             tma_load_3d(dst + off, &p.tm_k, bar(C::kBarFull + st), b * 64, row, h);
             tma_load_3d(dst + C::kKV + off, &p.tm_v, bar(C::kBarFull + st), b * 64, row, h);
@@ -258,33 +256,49 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
       for (int b = max(0, issued_last - C::kStages + 1); b <= issued_last; ++b)
         mbar_wait_warp(bar(C::kBarFull + b % C::kStages), (b / C::kStages) & 1, drain);
     }
-  } else if (warp == 2) {
+  } else if (warp == 5) {
     // ------------------------------------------------------------------- MMA (whole warp)
-    constexpr uint32_t kIdescS = idesc_bf16(128, C::kBK, 0, 0);  // A = Q, B = K, both K-major
-    constexpr uint32_t kIdescPV = idesc_bf16(128, D, 0, 1);      // A = P (TMEM), B = V MN-major
+    constexpr uint32_t kIdescS = idesc_bf16(128, C::kNP, 0, 0);  // A = K, B = Q: both K-major
+    constexpr uint32_t kIdescO = idesc_bf16(128, C::kNP, 1, 0);  // A = V^T MN-major, B = P^T
     constexpr uint32_t kHi = sdesc_hi_sw128(1024);
-    uint64_t qd[D / 16];
-#pragma unroll
-    for (int k = 0; k < D / 16; ++k)
-      qd[k] = sdesc64(sdesc_lo(sbase + C::kOffQ + (k / 4) * C::kBox + (k % 4) * 32, 16), kHi);
-    const uint64_t kd0 = sdesc64(sdesc_lo(sbase + C::kOffRing, 16), kHi);
-    const uint64_t vd0 = sdesc64(sdesc_lo(sbase + C::kOffRing + C::kKV, C::kBK * 128), kHi);
     constexpr uint64_t kStageStep = (2 * C::kKV) >> 4;
+    // per K-step of 16: K rows (32 bytes into the 128-byte swizzled rows, 64-column boxes 16 KB
+    // apart), Q and P^T rows (boxes 2 KB apart), V^T (16 key rows = 2 KB further each step).
+    // V^T is the 128-row A operand of O^T; at d = 64 its second 64 rows (the MN-major layout's
+    // second 64-column box) alias the first (box stride 0): O^T rows 64-127 repeat rows 0-63
+    // and are never read.
+    uint64_t ka[8], qb[8], pb[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      ka[k] = sdesc64(sdesc_lo(sbase + C::kOffRing + (k / 4) * C::kBox + (k % 4) * 32, 16), kHi);
+      qb[k] = sdesc64(sdesc_lo(sbase + C::kOffQ + (k / 4) * C::kSmallBox + (k % 4) * 32, 16), kHi);
+      pb[k] = sdesc64(sdesc_lo(sbase + C::kOffP + (k / 4) * C::kSmallBox + (k % 4) * 32, 16), kHi);
+    }
+    const uint64_t va =
+        sdesc64(sdesc_lo(sbase + C::kOffRing + C::kKV, D == 128 ? C::kBox : 0), kHi);
     bool ok = true;
-    int ns = 0;  // S products issued (buffer ns % 2)
-    auto issue_s = [&](int i) {  // S of CTA-local block i (its K stage must be full)
-      const int b = ns % C::kSBufs;
-      if (ns >= C::kSBufs) {
-        if (!mbar_wait_warp(bar(C::kBarSFree + b), (ns / C::kSBufs - 1) & 1, ctl)) return false;
+    int ns = 0;  // S^T products issued (buffer ns % 2)
+    auto issue_s = [&](int i) {  // S^T of CTA-local block i (its K stage must be full)
+      const int b = ns % 2;
+      if (ns >= 2) {
+        if (!mbar_wait_warp(bar(C::kBarSFree + b), (ns / 2 - 1) & 1, ctl)) return false;
         tc_fence_after();
       }
       const int st = i % C::kStages;
       if (!mbar_wait_warp(bar(C::kBarFull + st), (i / C::kStages) & 1, ctl)) return false;
       tc_fence_after();
-      if constexpr (D == 128)
-        mma_qk_d128(tmem + C::kColS + C::kBK * b, qd, kd0 + st * kStageStep, kIdescS);
-      else
-        mma_qk_d64(tmem + C::kColS + C::kBK * b, qd, kd0 + st * kStageStep, kIdescS);
+#pragma unroll
+      for (int rb = 0; rb < C::kRB; ++rb) {
+        uint64_t a[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          a[k] = ka[k] + st * kStageStep + ((rb * C::kColBoxes * C::kBox) >> 4);
+        const uint32_t dst = tmem + C::kColS + (b * C::kRB + rb) * C::kNP;
+        if constexpr (C::kSteps == 8)
+          mma_ss_k8(dst, a, qb, kIdescS, 0u);
+        else
+          mma_ss_k4(dst, a, qb, kIdescS);
+      }
       mma_commit(bar(C::kBarSFull + b));
       ++ns;
       return true;
@@ -299,20 +313,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
         if (i + 1 < e) {
           if (!(ok = issue_s(i + 1))) break;
         } else {
-          mma_commit(bar(C::kBarQEmpty));  // every S of the segment issued: Q is free after them
+          mma_commit(bar(C::kBarQEmpty));  // every S^T of the segment issued: Q is free after them
         }
         if (!(ok = mbar_wait_warp(bar(C::kBarPFull), i & 1, ctl))) break;
         tc_fence_after();
-        if (i == i0 && seg > 0) {  // O still holds the previous segment until the softmax read it
+        if (i == i0 && seg > 0) {  // O^T still holds the previous segment until the softmax read it
           if (!(ok = mbar_wait_warp(bar(C::kBarOFree), (seg - 1) & 1, ctl))) break;
           tc_fence_after();
         }
-        // 128 keys per call: P columns 64 apart, V rows 16 KB apart (1024 in 16-byte units)
 #pragma unroll
-        for (int rb = 0; rb < C::kRowBoxes; ++rb)
-          mma_pv_k128(tmem + C::kColO, tmem + C::kColP + 64u * rb,
-                      vd0 + (i % C::kStages) * kStageStep + 1024u * rb, kIdescPV,
-                      (i > i0 || rb > 0) ? 1u : 0u);
+        for (int rb = 0; rb < C::kRB; ++rb) {
+          // keys of row box rb: its V rows, P^T boxes 2 rb and 2 rb + 1
+          uint64_t a[8], bp[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            a[k] = va + (i % C::kStages) * kStageStep + ((rb * C::kColBoxes * C::kBox) >> 4) +
+                   128u * k;
+            bp[k] = pb[k] + ((rb * 2 * C::kSmallBox) >> 4);
+          }
+          mma_ss_k8(tmem + C::kColO, a, bp, kIdescO, (i > i0 || rb > 0) ? 1u : 0u);
+        }
         mma_commit(bar(C::kBarPVDone));
         mma_commit(bar(C::kBarEmpty + i % C::kStages));
         if (i + 1 == e) mma_commit(bar(C::kBarODone));
@@ -326,130 +346,150 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
       mma_commit(bar(C::kBarDrain));
       mbar_wait_warp(bar(C::kBarDrain), 0, drain);
     }
-  } else if (warp == 0 || warp == 4) {
-    // ------------------------------------------------------------------- softmax (thread = row)
-    const int hf = warp >> 2;  // half of the block's keys: [64 hf, 64 hf + 64)
-    const int r = lane;
-    const uint32_t trow = tmem;  // lanes 0-31: the quarter of warps 0 and 4
-    float* xm = reinterpret_cast<float*>(smem + C::kOffX);  // [parity][half][row]
-    float* xl = xm + 2 * 2 * 32;                              // [half][row]
+  } else {
+    // --------------------------------------------------- softmax (warps 0-3, thread = key t)
+    const int t = threadIdx.x;  // key t of each block; row t of O^T (column d = t of O)
+    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float* xm = reinterpret_cast<float*>(smem + C::kOffX);  // [parity][warp][query]
+    float* xl = xm + 2 * 4 * 8;                              // [warp][query]
+    uint8_t* pt = smem + C::kOffP;
     const float sl2 = p.scale_log2;
+    const int nq = p.Nq;
+    constexpr float kSlack = 8.f;  // log2 units: P stays <= 256, like the forward
     bool ok = true;
     int seg = 0;
     for (int i = 0; ok && i < rg.nblk; ++seg) {
       const int h = rg.head(rg.g0 + i);
       const int e = rg.seg_end(i);
-      float m = -INFINITY, l = 0.f;  // l: this warp's part of the running sum
+      float m[8], l[8];  // per query: the reference max (the same in every thread), this
+                         // thread's part of the running sum
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        m[q] = -INFINITY;
+        l[q] = 0.f;
+      }
       for (int i0 = i; i < e; ++i) {
-        constexpr int kH = C::kHalfKeys;
-        const int sb = i % C::kSBufs;
-        if (!(ok = mbar_wait(bar(C::kBarSFull + sb), (i / C::kSBufs) & 1, ctl))) break;
+        const int sb = i & 1;
+        if (!(ok = mbar_wait(bar(C::kBarSFull + sb), (i >> 1) & 1, ctl))) break;
         tc_fence_after();
-        uint32_t sc[kH];
-        if constexpr (kH == 128)
-          tmem_ld128(trow + C::kColS + C::kBK * sb + kH * hf, sc);
-        else
-          tmem_ld64(trow + C::kColS + C::kBK * sb + kH * hf, sc);
+        constexpr int R = C::kRB;  // this thread's keys: t + 128 rb
+        float x[R][8], wm[8];
+        const int jb = static_cast<int>((rg.g0 + i) % rg.nb);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) wm[q] = -INFINITY;
+#pragma unroll
+        for (int rb = 0; rb < R; ++rb) {
+          uint32_t sv[16];
+          tmem_ld16(tl + C::kColS + (sb * R + rb) * C::kNP, sv);
+          const bool valid = jb * C::kBK + rb * 128 + t < p.Nk;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            x[rb][q] = (valid && q < nq) ? __uint_as_float(sv[q]) * sl2 : -INFINITY;
+            wm[q] = fmaxf(wm[q], x[rb][q]);
+          }
+        }
         tc_fence_before();
         mbar_arrive(bar(C::kBarSFree + sb));
-        const int b = i & 1;  // exchange slot
-        const int jb = static_cast<int>((rg.g0 + i) % rg.nb);
-        const int n = min(C::kBK, p.Nk - jb * C::kBK) - kH * hf;  // keys of this half
-        if (n < kH) {
 #pragma unroll
-          for (int k = 0; k < kH; ++k)
-            if (k >= n) sc[k] = __float_as_uint(-INFINITY);
-        }
-        float mxa[8];
+        for (int off = 16; off > 0; off >>= 1)
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          mxa[u] = max3(-INFINITY, __uint_as_float(sc[2 * u]), __uint_as_float(sc[2 * u + 1]));
+          for (int q = 0; q < 8; ++q) wm[q] = fmaxf(wm[q], __shfl_xor_sync(~0u, wm[q], off));
+        // the block max per query over the four warps: slots and barriers by block parity (a
+        // warp reaches slot b again only after every warp has arrived for the block in between,
+        // so after all of them read it), bounded waits
+        const int b = i & 1;
+        if (lane == 0)
 #pragma unroll
-        for (int k = 16; k < kH; k += 16)
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            mxa[u] = max3(mxa[u], __uint_as_float(sc[k + 2 * u]), __uint_as_float(sc[k + 2 * u + 1]));
-        const float mh = max3(max3(mxa[0], mxa[1], mxa[2]), max3(mxa[3], mxa[4], mxa[5]),
-                              fmaxf(mxa[6], mxa[7])) * sl2;  // -inf for a half with no key
-        // the block's row max over both halves: two slots and barriers by block parity (a warp
-        // reaches slot b again only after the partner has arrived for the block in between, so
-        // after it read the slot), bounded waits, so that a warp that gave up cannot strand the
-        // other one
-        xm[(b * 2 + hf) * 32 + r] = mh;
+          for (int q = 0; q < 8; ++q) xm[(b * 4 + warp) * 8 + q] = wm[q];
         mbar_arrive(bar(C::kBarX + b));
         if (!(ok = mbar_wait(bar(C::kBarX + b), (i >> 1) & 1, ctl))) break;
-        const float mx = fmaxf(mh, xm[(b * 2 + (hf ^ 1)) * 32 + r]);
-        const float m_new = fmaxf(m, mx);  // finite: a block holds at least one key
-        // the exponentials first, into registers: they overlap the previous block's P V, which
-        // has to be done only before P is rewritten and O rescaled
-        const unsigned long long k2 = f2_pack(sl2, sl2);
-        const unsigned long long nm2 = f2_pack(-m_new, -m_new);
-        unsigned long long rs[4];
+        float mb[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) rs[u] = f2_pack(0.f, 0.f);
-        uint32_t pk[kH / 2];
+        for (int q = 0; q < 8; ++q)
+          mb[q] = fmaxf(fmaxf(xm[(b * 4 + 0) * 8 + q], xm[(b * 4 + 1) * 8 + q]),
+                        fmaxf(xm[(b * 4 + 2) * 8 + q], xm[(b * 4 + 3) * 8 + q]));
+        // conditional rescaling: the reference moves only when a query's block max passes it by
+        // more than kSlack (the same decision in every thread: the same inputs)
+        bool move = false;
 #pragma unroll
-        for (int u = 0; u < kH / 2; ++u) {
-          const unsigned long long x = f2_fma(
-              f2_pack(__uint_as_float(sc[2 * u]), __uint_as_float(sc[2 * u + 1])), k2, nm2);
-          float x0, x1;
-          f2_unpack(x, x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          rs[u & 3] = f2_add(rs[u & 3], f2_pack(p0, p1));
-          pk[u] = pack_bf16(p0, p1);
+        for (int q = 0; q < 8; ++q) move |= q < nq && mb[q] > m[q] + kSlack;
+        float alpha[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) alpha[q] = 1.f;
+        if (move) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            if (q >= nq) continue;
+            const float m_new = fmaxf(m[q], mb[q]);
+            alpha[q] = m[q] == -INFINITY ? 0.f : ex2(m[q] - m_new);
+            m[q] = m_new;
+            l[q] *= alpha[q];
+          }
         }
+        // the exponentials first: they overlap the previous block's O^T product, which has to
+        // be done only before P^T is rewritten and O^T rescaled
+        float pv[R][8];
+#pragma unroll
+        for (int rb = 0; rb < R; ++rb)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            pv[rb][q] = q < nq ? ex2(x[rb][q] - m[q]) : 0.f;  // 0 for keys past Nk (x = -inf)
+            l[q] += pv[rb][q];
+          }
         if (i > 0) {
           if (!(ok = mbar_wait(bar(C::kBarPVDone), (i - 1) & 1, ctl))) break;
           tc_fence_after();
         }
-        if (i > i0 && __any_sync(~0u, m_new > m)) {  // the same decision in both warps
-          const float alpha = ex2(m - m_new);
-#pragma unroll 1
-          for (int cc = hf * (D / 2); cc < (hf + 1) * (D / 2); cc += 32) {
-            uint32_t o[32];
-            tmem_ld32(trow + C::kColO + cc, o);
+        if (move && i > i0) {
+          uint32_t o[16];
+          tmem_ld16(tl + C::kColO, o);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            tmem_st32(trow + C::kColO + cc, o);
-          }
-          l *= alpha;
+          for (int q = 0; q < 8; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha[q]);
+          tmem_st16(tl + C::kColO, o);
+          tmem_st_wait();
         }
-        m = m_new;
+        // P^T (row q, key t + 128 rb) as bf16 into the 128-byte-swizzled B tile: 64-key boxes
+        // 2 KB apart
 #pragma unroll
-        for (int u = 0; u < kH / 32; ++u)
-          tmem_st16(trow + C::kColP + (kH / 2) * hf + 16u * u, pk + 16 * u);
-        float rs0, rs1;
-        f2_unpack(f2_add(f2_add(rs[0], rs[1]), f2_add(rs[2], rs[3])), rs0, rs1);
-        l += rs0 + rs1;
-        tmem_st_wait();
+        for (int rb = 0; rb < R; ++rb) {
+          const int kk = t + 128 * rb;
+          uint8_t* prow = pt + (kk / 64) * C::kSmallBox + (kk % 8) * 2;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (q < nq)
+              *reinterpret_cast<__nv_bfloat16*>(prow + q * 128 + ((((kk % 64) / 8) ^ q) << 4)) =
+                  __float2bfloat16_rn(pv[rb][q]);
+        }
+        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(C::kBarPFull));
       }
       if (!ok) break;
-      // the segment's piece: O / l and its log-sum-exp (log2 units), rows < Nq, each warp half
-      // of the columns
+      // the segment's piece: O / l and its log-sum-exp (log2 units), rows < Nq
       if (!(ok = mbar_wait(bar(C::kBarODone), seg & 1, ctl))) break;
       tc_fence_after();
-      xl[hf * 32 + r] = l;
+      float ws[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        ws[q] = l[q];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ws[q] += __shfl_xor_sync(~0u, ws[q], off);
+      }
+      if (lane == 0)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) xl[warp * 8 + q] = ws[q];
       mbar_arrive(bar(C::kBarL));
       if (!(ok = mbar_wait(bar(C::kBarL), seg & 1, ctl))) break;
-      const float lt = xl[r] + xl[32 + r];
+      uint32_t o[16];
+      tmem_ld16(tl + C::kColO, o);
       const size_t slot = static_cast<size_t>(c) + h;
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;
-#pragma unroll 1
-      for (int cc = hf * (D / 2); cc < (hf + 1) * (D / 2); cc += 32) {
-        uint32_t o[32];
-        tmem_ld32(trow + C::kColO + cc, o);
-        if (r < p.Nq) {
-          float4* dst = reinterpret_cast<float4*>(p.ws_o + (slot * p.Nq + r) * D + cc);
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
-                                 __uint_as_float(o[4 * k + 2]) * inv,
-                                 __uint_as_float(o[4 * k + 3]) * inv);
-        }
+      for (int q = 0; q < 8; ++q) {
+        if (q >= nq) continue;
+        const float lt = xl[q] + xl[8 + q] + xl[16 + q] + xl[24 + q];
+        if (t < D) p.ws_o[(slot * nq + q) * D + t] = lt > 0.f ? __uint_as_float(o[q]) / lt : 0.f;
+        if (t == q) p.ws_lse[slot * nq + q] = lt > 0.f ? m[q] + __log2f(lt) : -INFINITY;
       }
-      if (hf == 0 && r < p.Nq) p.ws_lse[slot * p.Nq + r] = lt > 0.f ? m + __log2f(lt) : -INFINITY;
       tc_fence_before();
       mbar_arrive(bar(C::kBarOFree));
     }
@@ -458,21 +498,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == 5) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
 }  // namespace
 
 cudaError_t configure_decode() {
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<64>,
+  cudaError_t e = cudaFuncSetAttribute(decode_kt_kernel<64>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       TcCfg<64>::kSmemBytes);
+                                       KtCfg<64>::kSmemBytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             TcCfg<128>::kSmemBytes);
+    e = cudaFuncSetAttribute(decode_kt_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             KtCfg<128>::kSmemBytes);
   return e;
 }
 
@@ -482,11 +522,11 @@ cudaError_t launch_tc(const DecodeParams& p_in, cudaStream_t s) {
   // the block size is the kernel's: blocks per head, the CTA count (at most one per block) and
   // the pieces' layout in the workspace follow from it
   DecodeParams p = p_in;
-  p.blocks_per_head = (p.Nk + TcCfg<D>::kBK - 1) / TcCfg<D>::kBK;
+  p.blocks_per_head = (p.Nk + KtCfg<D>::kBK - 1) / KtCfg<D>::kBK;
   const long long blocks = static_cast<long long>(p.BH) * p.blocks_per_head;
   if (p.n_ctas > blocks) p.n_ctas = static_cast<int>(blocks);
   p.ws_lse = p.ws_o + static_cast<size_t>(p.n_ctas + p.BH) * p.Nq * D;
-  decode_tc_kernel<D><<<p.n_ctas, kTcThreads, TcCfg<D>::kSmemBytes, s>>>(p);
+  decode_kt_kernel<D><<<p.n_ctas, kKtThreads, KtCfg<D>::kSmemBytes, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the merge kernel's launch overlaps the split kernel's tail

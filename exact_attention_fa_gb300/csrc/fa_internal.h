@@ -84,8 +84,8 @@ constexpr int kDecodeMaxCtas = 1024;
 // Keys per block: 32 KB of K and of V per block at either head dimension.
 constexpr int decode_tc_block_keys(int d) { return d == 64 ? 256 : 128; }
 struct DecodeParams {
-  // 3-D views [BH][rows][d] of q (rows Nq), k and v (rows Nk), box 64 x 128 x 1, 128-byte
-  // swizzle; rows past the extent read as zero
+  // 3-D views [BH][rows][d] of q (rows Nq, box 64 x 16 x 1), k and v (rows Nk, box 64 x 128 x 1),
+  // 128-byte swizzle; rows past the extent read as zero
   CUtensorMap tm_q;
   CUtensorMap tm_k;
   CUtensorMap tm_v;

@@ -373,6 +373,16 @@ __device__ __forceinline__ void tmem_ld64x2(uint32_t taddr, uint32_t* r) {
       : "r"(taddr), "r"(taddr + 64u)
       : "memory");
 }
+// 16 consecutive columns in one load and one wait.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : FA_R8(0), FA_R8(8)
+      : "r"(taddr)
+      : "memory");
+}
 // 64 consecutive columns in one load and one wait.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t* r) {
   asm volatile(
@@ -473,6 +483,42 @@ __device__ __forceinline__ void mma_qk_d64(uint32_t d_tmem, const uint64_t (&a)[
       "add.s64 tb, %5, 6;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, tb, %6, 1;\n\t"
       "}\n" ::"r"(d_tmem),
       "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b), "r"(idesc)
+      : "memory");
+}
+// Eight K-steps of a product with both operands in shared memory, each step's descriptors given
+// (a[k], b[k]); the first step overwrites D unless accumulate is set.
+__device__ __forceinline__ void mma_ss_k8(uint32_t d_tmem, const uint64_t (&a)[8],
+                                          const uint64_t (&b)[8], uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %18, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %17, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %17, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %17, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %17, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %17, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %17, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %17, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %17, 1;\n\t"
+      "}\n" ::"r"(d_tmem),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]),
+      "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
+      "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// The same over four K-steps, overwriting D.
+__device__ __forceinline__ void mma_ss_k4(uint32_t d_tmem, const uint64_t (&a)[8],
+                                          const uint64_t (&b)[8], uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %9, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %9, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %9, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %9, 1;\n\t"
+      "}\n" ::"r"(d_tmem),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]),
+      "r"(idesc)
       : "memory");
 }
 // O (+)= P V over 128 keys: A = P in TMEM (8 columns per K-step), B = V MN-major (16 rows = 2 KB

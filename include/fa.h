@@ -174,8 +174,9 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
  * The work is a matrix-vector product bound by HBM bandwidth. The key blocks of all heads (128
  * keys at d = 128, 256 at d = 64) are split into n_ctas equal contiguous ranges streamed by
  * separate CTAs (a range may cut a head and span several), each block's products on the tensor
- * cores with the query rows zero-padded to a 128-row tile; the pieces of each head are merged
- * with the softmax statistics merge.
+ * cores with the keys on the accumulator's rows (S^T = K q^T, O^T += V^T P^T, the query rows
+ * zero-padded to 16); the pieces of each head are merged with the softmax statistics merge by a
+ * second kernel, launched as a programmatic dependent of the first.
  * n_ctas = 0 takes as many CTAs as the device holds at once (fa_decode_ctas); 1 .. 1024 forces
  * the count (capped at the number of key blocks). `workspace`: fa_decode_workspace_bytes(...)
  * bytes of device scratch, contents undefined on entry and on exit. Errors: FA_ERR_INVALID_ARG
