@@ -40,13 +40,14 @@ def run_decode(w, device, n_ctas=0, heads=None):
     (1, 77, 128, 0),     # one ragged block per head
     (3, 1000, 64, 1),    # one CTA streams all six heads
     (8, 1000, 128, 7),   # the most query rows; ranges cut heads mid-way
-    (2, 4097, 64, 0),    # a key past a 64-key block boundary
+    (2, 4097, 64, 0),    # one key past a 256-key block (its second 128-key row box empty)
     (1, 129, 128, 18),   # one block per CTA
     (5, 300, 128, 1024), # more CTAs asked for than there are blocks (capped)
     (4, 2048, 64, 0),
     (1, 4097, 64, 0),    # a key past a 256-key block boundary
     (1, 1000, 64, 7),
-    (1, 129, 64, 1024),
+    (1, 129, 64, 1024),  # one block per head: its second row box holds one key
+    (2, 200, 64, 0),     # the second row box partly valid
 ])
 def test_decode_small(cuda, nq, nk, d, ctas):
     w = wl.Workload("decode_small", 2, 3, nk, d, nq=nq, seed=40 + nq)
