@@ -250,6 +250,42 @@ def backward_head(q, k, v, do, scale, causal=False, block_mask=None, tile=128):
     return dQ, dK, dV
 
 
+def backward_head_sampled(q, k, v, do, scale, rows, cols, causal=False, block_mask=None, tile=128,
+                          row_block=1024):
+    """dQ at query ``rows`` and dK, dV at key ``cols`` of one head, by the same definition as
+    ``backward_head`` without materialising the whole N x N P: the query rows are walked
+    ``row_block`` at a time, each block's P (and O, D) formed in full, and only the sampled
+    columns of dS and P kept. dQ rows are independent of each other; a key column of dK or dV
+    sums over every query row, which every block contributes to.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    rows = np.asarray(rows)
+    cols = np.asarray(cols)
+    n = q.shape[0]
+    dq = np.zeros((rows.size, q.shape[1]))
+    dk = np.zeros((cols.size, k.shape[1]))
+    dv = np.zeros((cols.size, v.shape[1]))
+    for r0 in range(0, n, row_block):
+        rr = np.arange(r0, min(n, r0 + row_block))
+        S = scale * (q[rr] @ k.T)
+        P, _ = softmax_rows(S, allowed_keys(rr, k.shape[0], causal, block_mask, tile))
+        O = P @ v
+        D = (do[rr] * O).sum(axis=1)
+        Pc = P[:, cols]
+        dSc = Pc * (do[rr] @ v[cols].T - D[:, None])
+        dv += Pc.T @ do[rr]
+        dk += scale * (dSc.T @ q[rr])
+        sel = np.nonzero((rows >= r0) & (rows < r0 + rr.size))[0]
+        if sel.size:
+            lr = rows[sel] - r0
+            dS = P[lr] * (do[rows[sel]] @ v.T - D[lr][:, None])
+            dq[sel] = scale * (dS @ k)
+    return dq, dk, dv
+
+
 def backward(q, k, v, do, scale, causal=False, block_mask=None, tile=128):
     """Batched backward over [B, H, N, d] arrays; returns (dQ, dK, dV)."""
     dq = np.empty(q.shape)

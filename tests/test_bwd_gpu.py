@@ -110,6 +110,32 @@ def test_bwd_causal_N4096_d128_every_head(cuda):
     run_bwd(wl.WORKLOADS["bwd_causal_N4096_d128"], cuda)
 
 
+@pytest.mark.parametrize("N,d,causal", [(32768, 128, True), (16384, 64, False)])
+def test_bwd_long_sequence_sampled(cuda, N, d, causal):
+    """Sequences 4-8 times longer than the specified backward workload (up to 256 key tiles add
+    into a dQ row): dQ at one random row of every query tile and dK, dV at one random key of
+    every key tile (plus the first and last), against the oracle's row-blocked backward."""
+    w = wl.Workload("bwd_long_seq", 1, 1, N, d, causal=causal, seed=76)
+    inp = wl.make_inputs(w, with_do=True)
+    q, k, v, do = (H.to_device(inp, n, cuda) for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_forward(q, k, v, w.softmax_scale, causal=causal)
+    dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, w.softmax_scale, causal=causal)
+    fa.fa_check_device_error()
+    rng = np.random.default_rng(77)
+    pick = lambda: np.unique(np.concatenate([[0, N - 1], np.arange(0, N, 128) + rng.integers(0, 128, N // 128)]))
+    rows, cols = pick(), pick()
+    qf, kf, vf, dof = (inp.f64_head(n, 0, 0) for n in ("q", "k", "v", "do"))
+    gq, gk, gv = orc.backward_head_sampled(qf, kf, vf, dof, w.softmax_scale, rows, cols,
+                                           causal=causal)
+    got = {"dq": dq[0, 0].float().cpu().numpy()[rows], "dk": dk[0, 0].float().cpu().numpy()[cols],
+           "dv": dv[0, 0].float().cpu().numpy()[cols]}
+    for n, t in got.items():
+        assert np.all(np.isfinite(t)), f"{n} has non-finite entries"
+    errs = head_errors(got, {"dq": gq, "dk": gk, "dv": gv})
+    for n, e in errs.items():
+        assert e <= H.GRAD_REL_FRO, f"{n}: relative Frobenius error {e:.3e}"
+
+
 @pytest.mark.parametrize("B,Hh,N,d,causal", [
     (1, 17, 2048, 128, True),   # the backward groups heads whose Q, K, V, dO fit in 32 MB: 16 + 1
     (1, 33, 2048, 64, False),   # 32 + 1

@@ -161,6 +161,25 @@ def test_causal_N8192_d128_every_cta(cuda):
     run_and_compare(wl.WORKLOADS["causal_N8192_d128"], cuda, rows="tiles")
 
 
+@pytest.mark.parametrize("N,d,causal", [(131072, 128, True), (65536, 64, False)])
+def test_long_sequence_one_row_per_query_tile(cuda, N, d, causal):
+    """Sequences 8-16 times longer than the specified workloads (1024 / 512 query tiles, up to
+    1024 key tiles per row): one random row of every 128-row query tile, plus the first and last
+    rows, against the oracle."""
+    w = wl.Workload("long_seq", 1, 1, N, d, causal=causal, seed=74)
+    inp = wl.make_inputs(w)
+    q, k, v = (H.to_device(inp, n, cuda) for n in ("q", "k", "v"))
+    o, lse = fa.attention_forward(q, k, v, w.softmax_scale, causal=causal)
+    fa.fa_check_device_error()
+    rng = np.random.default_rng(75)
+    rows = np.unique(np.concatenate([[0, N - 1], np.arange(0, N, 128) + rng.integers(0, 128, N // 128)]))
+    qf, kf, vf = (inp.f64_head(n, 0, 0) for n in ("q", "k", "v"))
+    O_ref, lse_ref = orc.forward_head(qf, kf, vf, w.softmax_scale, causal=causal, rows=rows,
+                                      row_block=256)
+    H.compare_o(o[0, 0].float().cpu().numpy()[rows], O_ref, bf16=True)
+    H.compare_lse(lse[0, 0].cpu().numpy()[rows], lse_ref)
+
+
 @pytest.mark.parametrize("B,Hh,N,d,causal", [
     (1, 9, 8192, 128, True),    # K/V of 8 heads fill the 32 MB head group: groups of 8 + 1
     (3, 11, 2048, 128, False),  # groups of 32 + 1

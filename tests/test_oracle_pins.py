@@ -375,6 +375,44 @@ def test_backward_invariants(causal):
     assert abs(float((dk @ c).sum())) < 1e-12
 
 
+@pytest.mark.parametrize("n,causal,masked", [(11, False, False), (10, True, True)])
+def test_backward_sampled_matches_finite_differences(n, causal, masked):
+    """The row-blocked backward of sampled query rows and key columns (blocks of 3 rows, so that
+    several blocks add into each dK, dV column), against central differences of L = sum(O * dO),
+    ragged and with the tile mask and causal mask combined."""
+    d, tile = 4, 4
+    rng = np.random.default_rng(23)
+    q, k, v, do = (rng.standard_normal((n, d)) for _ in range(4))
+    bm = np.array([[1, 0, 1], [1, 1, 0], [1, 1, 1]], np.uint8) if masked else None
+    rows, cols = np.array([0, 4, n - 1]), np.array([1, 5, n - 2])
+    dq, dk, dv = orc.backward_head_sampled(q, k, v, do, 0.5, rows, cols, causal=causal,
+                                           block_mask=bm, tile=tile, row_block=3)
+    h = 1e-6
+    for name, x, g, idx_rows in (("q", q, dq, rows), ("k", k, dk, cols), ("v", v, dv, cols)):
+        num = np.zeros_like(g)
+        for a_i, r in enumerate(idx_rows):
+            for c in range(d):
+                xp, xm = x.copy(), x.copy()
+                xp[r, c] += h
+                xm[r, c] -= h
+                a_p = {"q": q, "k": k, "v": v, name: xp}
+                a_m = {"q": q, "k": k, "v": v, name: xm}
+                num[a_i, c] = (loss(a_p["q"], a_p["k"], a_p["v"], do, 0.5, causal, bm, tile)
+                               - loss(a_m["q"], a_m["k"], a_m["v"], do, 0.5, causal, bm, tile)) / (2 * h)
+        assert np.max(np.abs(num - g)) < 1e-7 * max(1.0, np.max(np.abs(g))), name
+
+
+def test_backward_sampled_invariants():
+    """Every row and column sampled: rows of dS sum to zero and rows of P to one, so the key
+    columns of dK sum to zero and those of dV to the column sums of dO."""
+    q, k, v = rand_head(40, 8, 24)
+    do = np.random.default_rng(25).standard_normal((40, 8))
+    allr = np.arange(40)
+    dq, dk, dv = orc.backward_head_sampled(q, k, v, do, 0.3, allr, allr, causal=True, row_block=7)
+    assert np.allclose(dk.sum(axis=0), 0.0, atol=1e-12)
+    assert np.allclose(dv.sum(axis=0), do.sum(axis=0), atol=1e-12)
+
+
 def test_backward_batched_matches_per_head():
     rng = np.random.default_rng(22)
     q, k, v, do = (rng.standard_normal((1, 2, 10, 4)) for _ in range(4))
