@@ -521,7 +521,10 @@ def parts_of(pr, t, peak):
     out["fwd"]["frac_of_bf16_peak"] = out["fwd"]["tflops"] / peak
     if pr.w.backward:
         tf = pr.f_bwd / (t["bwd_ms"] * 1e-3) / 1e12
-        out["bwd"] = {"ms": t["bwd_ms"], "tflops": tf, "frac_of_bf16_peak": tf / peak}
+        # the backward counts its five contractions (2.5x the forward's FLOP); the metric's
+        # literal 4*B*H*N^2*d (causal halved) over the backward's time is reported beside it
+        out["bwd"] = {"ms": t["bwd_ms"], "tflops": tf, "frac_of_bf16_peak": tf / peak,
+                      "tflops_at_literal_4BHN2d": pr.f_fwd / (t["bwd_ms"] * 1e-3) / 1e12}
     return out
 
 
