@@ -485,9 +485,12 @@ def time_problem(pr, steps, warmup, flush_buf, world, dev, local):
     fwd_ms = statistics.fmean(ev[i][0].elapsed_time(ev[i][1]) for i in range(steps))
     bwd_ms = (statistics.fmean(ev[i][1].elapsed_time(ev[i][2]) for i in range(steps))
               if pr.w.backward else 0.0)
-    step_ms, fwd_ms, bwd_ms = aggregate_over_ranks([step_ms, fwd_ms, bwd_ms], world, dev)
-    return {"step_ms": step_ms, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
-            "clocks": clocks.summary(local), "wall_s": wall}
+    per_step = [ev[i][0].elapsed_time(ev[i][2]) for i in range(steps)]
+    med_ms, min_ms = statistics.median(per_step), min(per_step)
+    step_ms, fwd_ms, bwd_ms, med_ms, min_ms = aggregate_over_ranks(
+        [step_ms, fwd_ms, bwd_ms, med_ms, min_ms], world, dev)
+    return {"step_ms": step_ms, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_ms_median": med_ms,
+            "step_ms_min": min_ms, "clocks": clocks.summary(local), "wall_s": wall}
 
 
 def roofline_of(pr, kname, kflops, kms, peaks, peak_src):
@@ -716,6 +719,7 @@ def run_ours(args):
         "metric": metric_name(w), "value": job_tflops(world, pr.f_fwd + pr.f_bwd, t["step_ms"]),
         "unit": "TFLOPS", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": t["step_ms"], "higher_is_better": True, "scaling": "weak",
+        "ms_per_step_median": t["step_ms_median"], "ms_per_step_min": t["step_ms_min"],
         "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic: i.i.d. N(0,1) inputs, seeded"
                 + {"bf16": ", rounded to bf16", "e4m3": ", rounded to e4m3"}.get(w.dtype, ""),
