@@ -35,6 +35,11 @@ def test_bench_line(cuda, workload):
     assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
     assert d["roofline"]["peak"] > 0 and 0 < d["roofline"]["frac"]
     assert d["config"]["workload"] == workload
+    if workload != "decode_N32768_d128_h8":
+        assert 0 < d["ms_per_step_min"] <= d["ms_per_step_median"]
+    if workload == "mha_N2048_d64":  # the metric's literal count beside the five contractions
+        bwd = d["parts"]["bwd"]
+        assert abs(bwd["tflops_at_literal_4BHN2d"] / bwd["tflops"] - 0.4) < 1e-9
     # the fp32 path runs on the FMA pipes; bf16 on the tensor cores, also against the sustained
     # and datasheet peaks; decoding against HBM
     want = {"single_head_fp32": "alu", "mha_N2048_d64": "tensor", "decode_N32768_d128_h8": "hbm"}
