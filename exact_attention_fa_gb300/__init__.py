@@ -5,7 +5,7 @@ marshals torch tensors to it. The entry points below are loaded from the binding
 that importing the seeded input generator (exact_attention_fa_gb300.workloads) loads neither the
 binding nor torch.
 """
-_EXPORTS = ("FAError", "attention_backward", "attention_decode", "attention_forward", "fa_bwd",
+_EXPORTS = ("FAError", "attention", "attention_backward", "attention_decode", "attention_forward", "fa_bwd",
             "fa_bwd_blocksparse", "fa_bwd_noalloc", "fa_bwd_workspace_bytes",
             "fa_check_device_error", "fa_decode", "fa_decode_ctas", "fa_decode_workspace_bytes",
             "fa_fwd", "fa_fwd_blocksparse", "fa_fwd_fp8", "fa_fwd_fp32", "fa_fwd_fp32_fa1",

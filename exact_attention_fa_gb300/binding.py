@@ -323,3 +323,35 @@ def attention_backward(q, k, v, o, lse, do, scale: float | None = None, causal: 
     else:
         fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, causal, ws)
     return dq, dk, dv
+
+
+class _Attention(torch.autograd.Function):
+    """Forward and backward through the library, for use inside autograd graphs: the forward
+    saves Q, K, V, O and lse, the backward runs fa_bwd (fa_bwd_blocksparse with a tile mask) on
+    them."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, scale, causal, block_mask):
+        o, lse = attention_forward(q, k, v, scale, causal=causal, block_mask=block_mask)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.scale, ctx.causal, ctx.block_mask = scale, causal, block_mask
+        ctx.mark_non_differentiable(lse)
+        return o, lse
+
+    @staticmethod
+    def backward(ctx, do, _dlse):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = attention_backward(q, k, v, o, lse, do.contiguous(), ctx.scale,
+                                        causal=ctx.causal, block_mask=ctx.block_mask)
+        return dq.to(q.dtype), dk, dv, None, None, None
+
+
+def attention(q, k, v, scale: float | None = None, causal: bool = False, block_mask=None):
+    """O (and lse) of bf16 [B, H, N, d] inputs, differentiable with respect to Q, K and V: the
+    gradients come from the library's backward (dQ, computed in fp32, is returned in Q's dtype;
+    call attention_backward directly to keep it in fp32)."""
+    if q.dtype != torch.bfloat16:
+        raise ValueError("attention() differentiates the bf16 path; use attention_forward for "
+                         "fp32 or e4m3 inputs")
+    scale = q.shape[-1] ** -0.5 if scale is None else float(scale)
+    return _Attention.apply(q, k, v, scale, bool(causal), block_mask)
