@@ -70,6 +70,16 @@ def test_fp32_shapes(cuda, N, d, causal):
     run_and_compare(w, cuda)
 
 
+@pytest.mark.parametrize("N,d,causal", [(8192, 128, True), (4096, 64, False)])
+def test_fp32_long_sequence(cuda, N, d, causal):
+    """The fp32 path at sequence lengths far past the specified one (256 and 128 key blocks of
+    32 per row, 8-row CTAs): one row of every 32-row group, the first and last rows, against the
+    oracle at the fp32 bar (max-abs 1e-5)."""
+    w = wl.Workload("fp32_long", 1, 2, N, d, dtype="fp32", causal=causal, seed=16)
+    worst, _, _ = run_and_compare(w, cuda, rows="tiles")
+    assert worst < 1e-5
+
+
 def run_fa1(w: wl.Workload, device):
     """fa_fwd_fp32_fa1 on every row against the oracle's plain definition; dense workloads also
     against the oracle's FA-1 form with the kernel's 32-key blocks."""
